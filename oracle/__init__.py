@@ -1,0 +1,272 @@
+"""CPU oracle for the dropless MoE layer hot path (Python access layer).
+
+TEST INFRASTRUCTURE: only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package. The library
+(``dropless_moe_expert_router_gb300``) never imports it, and this package never
+imports the library: the oracle and the CUDA path share no code.
+
+The arithmetic lives in ``moe_oracle.c`` (plain single-threaded C, double
+precision); this module compiles it with gcc on first use (or through
+``build()``) and wraps each function with numpy marshalling only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MAT_BF16, MAT_F64, MAT_MXFP8 = 0, 1, 2
+H_NONE, H_BF16, H_MXFP8 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/libmoe_oracle.so (gcc, -O2, IEEE)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + ".%d.tmp" % os.getpid()
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+             "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            P = C.c_void_p
+            i32, i64, dbl = C.c_int, C.c_long, C.c_double
+            L.oracle_bf16_to_double.restype = dbl
+            L.oracle_bf16_to_double.argtypes = [C.c_uint16]
+            L.oracle_double_to_bf16.restype = C.c_uint16
+            L.oracle_double_to_bf16.argtypes = [dbl]
+            L.oracle_e4m3_decode.restype = dbl
+            L.oracle_e4m3_decode.argtypes = [C.c_uint8]
+            L.oracle_e4m3_encode.restype = C.c_uint8
+            L.oracle_e4m3_encode.argtypes = [dbl]
+            L.oracle_e8m0_scale_byte.restype = i32
+            L.oracle_e8m0_scale_byte.argtypes = [dbl]
+            L.oracle_quant_rows_bf16.restype = None
+            L.oracle_quant_rows_bf16.argtypes = [P, i64, i64, P, P]
+            L.oracle_quant_cols_grouped_bf16.restype = None
+            L.oracle_quant_cols_grouped_bf16.argtypes = [P, i64, P, i32, P, P]
+            L.oracle_route_topk.restype = None
+            L.oracle_route_topk.argtypes = [P, i32, i32, i32, i32, P, P]
+            L.oracle_permute.restype = i64
+            L.oracle_permute.argtypes = [P, i32, i32, P, i32, i32, P, P, P, P, P]
+            L.oracle_combine.restype = None
+            L.oracle_combine.argtypes = [P, P, P, i32, i32, i32, P]
+            L.oracle_swiglu_rows.restype = None
+            L.oracle_swiglu_rows.argtypes = [i32, P, P, i32, P, P, P, P, P, P, P, i32, i32, i32,
+                                             i64, P, i64, i32, P, P, P, P, P, P, P, P]
+            L.oracle_swiglu_dgrad_rows.restype = None
+            L.oracle_swiglu_dgrad_rows.argtypes = [i32, P, P, i32, P, P, i32, i32, P, P, P, P, P,
+                                                   P, P, i32, i32, i32, i64, P, i64, P, P, P, P]
+            L.oracle_wgrad_expert.restype = None
+            L.oracle_wgrad_expert.argtypes = [i32, P, P, i64, i32, P, P, i64, P, i32, i32, i64,
+                                              P, i64, P]
+            L.oracle_expert_of_row.restype = i32
+            L.oracle_expert_of_row.argtypes = [P, i32, i64]
+            _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+# ----------------------------------------------------------------- formats
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    L = lib()
+    flat = np.asarray(v, dtype=np.float64).ravel()
+    out = np.fromiter((L.oracle_double_to_bf16(float(x)) for x in flat), dtype=np.uint16,
+                      count=flat.size)
+    return out.reshape(np.shape(v))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([L.oracle_e4m3_decode(int(x)) for x in c]).reshape(np.shape(codes))
+
+
+def e4m3_encode(v) -> np.ndarray:
+    L = lib()
+    flat = np.asarray(v, dtype=np.float64).ravel()
+    return np.array([L.oracle_e4m3_encode(float(x)) for x in flat],
+                    dtype=np.uint8).reshape(np.shape(v))
+
+
+def e8m0_scale_byte(amax: float) -> int:
+    return lib().oracle_e8m0_scale_byte(float(amax))
+
+
+def quant_rows(x_bf16):
+    """Row-wise 1x32 MXFP8 of a bf16 matrix -> (q [rows, cols] u8, s [rows, cols/32] u8)."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    s = np.zeros((rows, cols // 32), np.uint8)
+    lib().oracle_quant_rows_bf16(_p(x), rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def colwise_scale_rows(R_cap: int, E: int) -> int:
+    """Rows of the padded group-aware column-wise scale layout."""
+    return E + R_cap // 32 + 1
+
+
+def quant_cols_grouped(x_bf16, group_offsets, fill_q=0, fill_s=0):
+    """Group-aware column-wise (32x1) MXFP8 of a bf16 matrix [R_cap, cols]."""
+    x = _c(x_bf16, np.uint16)
+    off = _c(group_offsets, np.int32)
+    R_cap, cols = x.shape
+    E = off.size - 1
+    q = np.full((R_cap, cols), fill_q, np.uint8)
+    s = np.full((colwise_scale_rows(R_cap, E), cols), fill_s, np.uint8)
+    lib().oracle_quant_cols_grouped_bf16(_p(x), cols, _p(off), E, _p(q), _p(s))
+    return q, s
+
+
+# ------------------------------------------------------------------ router
+def route_topk(logits, K: int, renorm: bool = False):
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    ids = np.zeros((T, K), np.int32)
+    probs = np.zeros((T, K), np.float32)
+    lib().oracle_route_topk(_p(lg), T, E, K, int(bool(renorm)), _p(ids), _p(probs))
+    return ids, probs
+
+
+# ----------------------------------------------------------------- permute
+def permute(x_bf16, ids, E: int):
+    """Returns dict(x_perm [T*K, H] (rows >= R zero), group_sizes, group_offsets,
+    row_map [T,K], perm_src [T*K] (entries >= R are -1), R)."""
+    idv = _c(ids, np.int32)
+    T, K = idv.shape
+    if x_bf16 is None:
+        x, H = None, 0
+    else:
+        x = _c(x_bf16, np.uint16)
+        H = x.shape[1]
+    xp = None if x is None else np.zeros((T * K, H), np.uint16)
+    gs = np.zeros(E, np.int32)
+    go = np.zeros(E + 1, np.int32)
+    rm = np.zeros((T, K), np.int32)
+    ps = np.full(T * K, -1, np.int32)
+    R = lib().oracle_permute(_p(x), T, H, _p(idv), K, E, _p(xp), _p(gs), _p(go), _p(rm), _p(ps))
+    return dict(x_perm=xp, group_sizes=gs, group_offsets=go, row_map=rm, perm_src=ps, R=int(R))
+
+
+# ----------------------------------------------------------------- combine
+def combine(y_perm_bf16, row_map, probs):
+    yp = _c(y_perm_bf16, np.uint16)
+    rm = _c(row_map, np.int32)
+    pr = _c(probs, np.float32)
+    T, K = rm.shape
+    H = yp.shape[1]
+    y = np.zeros((T, H), np.uint16)
+    lib().oracle_combine(_p(yp), _p(rm), _p(pr), T, K, H, _p(y))
+    return y
+
+
+# ------------------------------------------------------------ grouped MLP
+class Operand:
+    """An oracle operand: kind MAT_BF16 (uint16 bits), MAT_F64 or MAT_MXFP8 (codes + scales)."""
+
+    def __init__(self, kind, v, s=None):
+        self.kind = kind
+        dt = {MAT_BF16: np.uint16, MAT_F64: np.float64, MAT_MXFP8: np.uint8}[kind]
+        self.v = np.ascontiguousarray(v, dtype=dt)
+        self.s = None if s is None else np.ascontiguousarray(s, dtype=np.uint8)
+
+
+def swiglu_rows(x: Operand, w1: Operand, w3: Operand, w2: Operand, group_offsets, rows,
+                h_mode=H_BF16, want=("y_bf16",)):
+    """Grouped SwiGLU MLP for the listed permuted rows. `want` picks outputs among
+    y_bf16, y_f64, h_bf16, h_q, h_s, h_f64, a_f64, b_f64."""
+    off = _c(group_offsets, np.int32)
+    E = off.size - 1
+    R_cap, H = x.v.shape
+    F = w1.v.shape[-1]
+    rw = _c(rows, np.int32)
+    n = rw.size
+    outs = {
+        "y_bf16": np.zeros((n, H), np.uint16) if "y_bf16" in want else None,
+        "y_f64": np.zeros((n, H)) if "y_f64" in want else None,
+        "h_bf16": np.zeros((n, F), np.uint16) if "h_bf16" in want else None,
+        "h_q": np.zeros((n, F), np.uint8) if "h_q" in want else None,
+        "h_s": np.zeros((n, F // 32), np.uint8) if "h_s" in want else None,
+        "h_f64": np.zeros((n, F)) if "h_f64" in want else None,
+        "a_f64": np.zeros((n, F)) if "a_f64" in want else None,
+        "b_f64": np.zeros((n, F)) if "b_f64" in want else None,
+    }
+    lib().oracle_swiglu_rows(
+        x.kind, _p(x.v), _p(x.s), w1.kind, _p(w1.v), _p(w1.s), _p(w3.v), _p(w3.s),
+        _p(w2.v), _p(w2.s), _p(off), E, H, F, R_cap, _p(rw), n, h_mode,
+        _p(outs["y_bf16"]), _p(outs["y_f64"]), _p(outs["h_bf16"]), _p(outs["h_q"]),
+        _p(outs["h_s"]), _p(outs["h_f64"]), _p(outs["a_f64"]), _p(outs["b_f64"]))
+    return {k: v for k, v in outs.items() if v is not None}
+
+
+def swiglu_dgrad_rows(dy: Operand, a: Operand, b: Operand, w1: Operand, w3: Operand,
+                      w2: Operand, group_offsets, rows, w_blk_rows=0,
+                      want=("dx_bf16",)):
+    off = _c(group_offsets, np.int32)
+    E = off.size - 1
+    R_cap, H = dy.v.shape
+    F = w1.v.shape[-1]
+    rw = _c(rows, np.int32)
+    n = rw.size
+    outs = {
+        "dx_bf16": np.zeros((n, H), np.uint16) if "dx_bf16" in want else None,
+        "dx_f64": np.zeros((n, H)) if "dx_f64" in want else None,
+        "da_f64": np.zeros((n, F)) if "da_f64" in want else None,
+        "db_f64": np.zeros((n, F)) if "db_f64" in want else None,
+    }
+    assert a.kind == b.kind
+    lib().oracle_swiglu_dgrad_rows(
+        dy.kind, _p(dy.v), _p(dy.s), a.kind, _p(a.v), _p(b.v), w1.kind, int(w_blk_rows),
+        _p(w1.v), _p(w1.s), _p(w3.v), _p(w3.s), _p(w2.v), _p(w2.s), _p(off), E, H, F, R_cap,
+        _p(rw), n, _p(outs["dx_bf16"]), _p(outs["dx_f64"]), _p(outs["da_f64"]),
+        _p(outs["db_f64"]))
+    return {k: v for k, v in outs.items() if v is not None}
+
+
+def wgrad_expert(A: Operand, B: Operand, group_offsets, e: int, cols=None):
+    """dW[c1, c2] = sum over group e's rows of A[r, c1] * B[r, c2], for c2 in cols."""
+    off = _c(group_offsets, np.int32)
+    E = off.size - 1
+    R_cap, n1 = A.v.shape
+    n2 = B.v.shape[1]
+    cl = np.arange(n2, dtype=np.int32) if cols is None else _c(cols, np.int32)
+    out = np.zeros((n1, cl.size))
+    lib().oracle_wgrad_expert(A.kind, _p(A.v), _p(A.s), n1, B.kind, _p(B.v), _p(B.s), n2,
+                              _p(off), E, int(e), R_cap, _p(cl), cl.size, _p(out))
+    return out
+
+
+def expert_of_row(group_offsets, r: int) -> int:
+    off = _c(group_offsets, np.int32)
+    return lib().oracle_expert_of_row(_p(off), off.size - 1, int(r))

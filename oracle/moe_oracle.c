@@ -1,0 +1,655 @@
+/*
+ * moe_oracle.c -- plain, slow, single-threaded CPU oracle for the dropless
+ * Mixture-of-Experts layer hot path.
+ *
+ * TEST INFRASTRUCTURE. This file is the correctness reference that the GPU
+ * kernels are checked against. Only the test suite, the package smoke check
+ * and the benchmark's CPU-baseline leg load it (through oracle/__init__.py).
+ * The library never includes, links or calls anything here, and nothing here
+ * includes or calls the library: the two share no code.
+ *
+ * Every floating-point step is evaluated in double precision; results are
+ * rounded once, to the output format, at the end (round-to-nearest-even).
+ * Loops follow the definitions one to one: no blocking, no fusion, no
+ * reordering beyond what a definition states.
+ *
+ * Sources (web pages on the subject; cited by title and section):
+ *   [SPARSER]  "Sparser MoE end-to-end" (harryzhou2000 blog):
+ *              sections "The workload changes the bottleneck",
+ *              "Preserve a compact route", "Remove work that has no selected route".
+ *   [TEJAX]    "Dropless MoE acceleration in JAX with NVIDIA Transformer Engine"
+ *              (news.bpdata.com): sections "Dropless vs capacity-based MoE",
+ *              "Transformer Engine building blocks for dropless MoE in JAX" (and
+ *              its MoE-layer figure), "Optimization 1: Grouped GEMM",
+ *              "Optimization 2: Expert parallelism to fuse Dispatch and Combine".
+ *   [CLARITY]  "NVIDIA's unoptimized DeepSeek-V3 baseline spends 84% of kernel
+ *              time moving tokens between GPUs" (theclarity.today).
+ * Where the pages leave a step open, the reading taken is stated beside the
+ * code (and listed with the other readings in the design notes).
+ *
+ * Parity status: every exported function is pinned by the CPU tests
+ * (tests/test_oracle_*.py) against brute force, library routines, closed
+ * forms or invariants.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16 -> double: bf16 is the upper half of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a finite |a| > 0 to a binary format with `p` significand bits
+ * (including the implicit one) and minimum normal exponent `emin`; values
+ * below 2^emin use the fixed subnormal quantum 2^(emin - p + 1).
+ * Round-to-nearest, ties-to-even (nearbyint under the default rounding mode).
+ * Division and multiplication by powers of two are exact here.
+ */
+static double round_to_format(double a, int p, int emin)
+{
+    int e;
+    frexp(a, &e);            /* a in [2^(e-1), 2^e) */
+    int ex = e - 1;
+    if (ex < emin)
+        ex = emin;
+    double quantum = ldexp(1.0, ex - (p - 1));
+    return nearbyint(a / quantum) * quantum;
+}
+
+/* double -> bfloat16, round to nearest even, overflow to infinity. */
+uint16_t oracle_double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return 0x7FC0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    double q = round_to_format(a, 8, -126);
+    if (q >= 0x1p128)
+        return (uint16_t)(sign | 0x7F80u);
+    float f = (float)q;      /* exact: q has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/*
+ * E4M3 (the "FN" variant used by MXFP8): 1 sign, 4 exponent bits (bias 7),
+ * 3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448.
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, E = (c >> 3) & 0xF, M = c & 7;
+    double v;
+    if (E == 15 && M == 7)
+        v = NAN;
+    else if (E == 0)
+        v = ldexp((double)M, -9);          /* subnormal: M * 2^-9 */
+    else
+        v = ldexp(1.0 + M / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* double -> E4M3, round to nearest even, saturating to +-448 ("satfinite").
+ * The sign of zero is kept. */
+uint8_t oracle_e4m3_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs(v);
+    if (a == 0.0 || isnan(a))
+        return sign;
+    double q = isinf(a) ? 448.0 : round_to_format(a, 4, -6);
+    if (q > 448.0)
+        q = 448.0;
+    if (q == 0.0)
+        return sign;
+    int e;
+    frexp(q, &e);
+    int ex = e - 1;
+    if (ex < -6)                              /* subnormal code 1..7 */
+        return (uint8_t)(sign | (uint8_t)(q / ldexp(1.0, -9)));
+    int mant = (int)((q / ldexp(1.0, ex) - 1.0) * 8.0);
+    return (uint8_t)(sign | (uint8_t)(((ex + 7) << 3) | mant));
+}
+
+/*
+ * Shared E8M0 block exponent of one MXFP8 block ([TEJAX] "Transformer Engine
+ * building blocks": MXFP8 with 1x32 E8M0 block scales). Reading taken: the
+ * Microscaling convention -- exponent = floor(log2(amax)) - 8, where 8 is the
+ * exponent of E4M3's largest power of two (448 = 1.75 * 2^8); the stored byte
+ * is exponent + 127 clamped to [0, 254]; an all-zero block gets byte 127 (2^0).
+ */
+int oracle_e8m0_scale_byte(double amax)
+{
+    if (amax == 0.0)
+        return 127;
+    int e;
+    frexp(amax, &e);                 /* floor(log2(amax)) = e - 1 */
+    int b = (e - 1) - 8 + 127;
+    if (b < 0)
+        b = 0;
+    if (b > 254)
+        b = 254;
+    return b;
+}
+
+/* Quantise n = 32 consecutive values (stride `stride` apart) to one MXFP8
+ * block: writes 32 E4M3 codes (same stride) and returns the scale byte. */
+static int quant_block(const double *x, long stride, int n, uint8_t *q, long qstride)
+{
+    double amax = 0.0;
+    for (int i = 0; i < n; i++) {
+        double a = fabs(x[i * stride]);
+        if (a > amax)
+            amax = a;
+    }
+    int sb = oracle_e8m0_scale_byte(amax);
+    double inv = ldexp(1.0, 127 - sb);   /* x / 2^(sb-127) */
+    for (int i = 0; i < n; i++)
+        q[i * qstride] = oracle_e4m3_encode(x[i * stride] * inv);
+    return sb;
+}
+
+/* Row-wise 1x32 MXFP8 quantisation of a bf16 matrix [rows, cols]
+ * (cols % 32 == 0). Payload q[rows, cols]; scales s[rows, cols/32]. */
+void oracle_quant_rows_bf16(const uint16_t *x, long rows, long cols, uint8_t *q, uint8_t *s)
+{
+    double buf[32];
+    for (long r = 0; r < rows; r++)
+        for (long b = 0; b < cols / 32; b++) {
+            for (int i = 0; i < 32; i++)
+                buf[i] = oracle_bf16_to_double(x[r * cols + b * 32 + i]);
+            s[r * (cols / 32) + b] = (uint8_t)quant_block(buf, 1, 32, q + r * cols + b * 32, 1);
+        }
+}
+
+/* Dequantise one MXFP8 element. */
+static double mx_value(uint8_t code, uint8_t sbyte)
+{
+    return ldexp(oracle_e4m3_decode(code), (int)sbyte - 127);
+}
+
+/*
+ * Group-aware column-wise MXFP8 quantisation of a bf16 matrix x[R_cap, cols]
+ * whose rows [off[e], off[e+1]) form group e ([TEJAX] "group-aware MXFP8
+ * quantization"). Blocks are 32 consecutive rows of one column and never
+ * cross a group boundary: they start at each group's first row; a group's
+ * last block may be partial and then takes its amax over its valid rows only.
+ * Scale layout: block b of group e is scale row (e + off[e] / 32 + b) of
+ * s[E + R_cap/32 + 1, cols] -- a padded layout that needs no scan (rows of
+ * the block index space that no block uses are left untouched). Payload
+ * rows >= off[E] are not written.
+ */
+void oracle_quant_cols_grouped_bf16(const uint16_t *x, long cols, const int32_t *off, int E,
+                                    uint8_t *q, uint8_t *s)
+{
+    double buf[32];
+    uint8_t qb[32];
+    for (int e = 0; e < E; e++) {
+        long r0 = off[e], r1 = off[e + 1];
+        for (long b = 0; r0 + 32 * b < r1; b++) {
+            long rs = r0 + 32 * b;
+            int n = (int)((r1 - rs) < 32 ? (r1 - rs) : 32);
+            long srow = e + r0 / 32 + b;
+            for (long c = 0; c < cols; c++) {
+                for (int i = 0; i < n; i++)
+                    buf[i] = oracle_bf16_to_double(x[(rs + i) * cols + c]);
+                s[srow * cols + c] = (uint8_t)quant_block(buf, 1, n, qb, 1);
+                for (int i = 0; i < n; i++)
+                    q[(rs + i) * cols + c] = qb[i];
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router: softmax scores + top-K on raw logits                              */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float v;
+    int idx;
+} scored;
+
+/* Descending logit; equal logits (IEEE compare, so -0 == +0): lower index first. */
+static int cmp_scored(const void *pa, const void *pb)
+{
+    const scored *a = pa, *b = pb;
+    if (a->v > b->v)
+        return -1;
+    if (a->v < b->v)
+        return 1;
+    return (a->idx > b->idx) - (a->idx < b->idx);
+}
+
+/*
+ * Router top-K ([SPARSER] "Preserve a compact route": selected expert ids
+ * carried as a dense [T, K] list; [TEJAX] "Optimization 2": the router kernels
+ * assign tokens before permutation).
+ * Readings taken: (1) selection is on the raw logits, ties go to the lower
+ * expert index, ids are stored in selection order (descending logit);
+ * (2) probs[t,k] is the softmax over all E logits of the row, taken at the
+ * selected id; with renorm != 0 the denominator is the sum over the K
+ * selected experts only.
+ * ids is int32 [T,K]; probs is float [T,K] (each rounded once from double).
+ */
+void oracle_route_topk(const float *logits, int T, int E, int K, int renorm,
+                       int32_t *ids, float *probs)
+{
+    scored *row = (scored *)malloc(sizeof(scored) * (size_t)E);
+    for (int t = 0; t < T; t++) {
+        const float *l = logits + (size_t)t * E;
+        for (int e = 0; e < E; e++) {
+            row[e].v = l[e];
+            row[e].idx = e;
+        }
+        qsort(row, (size_t)E, sizeof(scored), cmp_scored);
+        double m = (double)row[0].v;          /* row maximum */
+        double denom = 0.0;
+        if (renorm) {
+            for (int k = 0; k < K; k++)
+                denom += exp((double)row[k].v - m);
+        } else {
+            for (int e = 0; e < E; e++)
+                denom += exp((double)l[e] - m);
+        }
+        for (int k = 0; k < K; k++) {
+            ids[(size_t)t * K + k] = row[k].idx;
+            probs[(size_t)t * K + k] = (float)(exp((double)row[k].v - m) / denom);
+        }
+    }
+    free(row);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Permute (dispatch into expert-contiguous order)                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Dropless permutation ([TEJAX] "Dropless vs capacity-based MoE": every
+ * routed token is processed, no drop, no pad; figure: dispatch groups tokens
+ * by expert, combine restores token order; [SPARSER] "Preserve a compact
+ * route": -1 marks an invalid route, which is skipped).
+ * Readings taken: a route (t,k) is valid iff 0 <= ids[t,k] < E (anything else,
+ * -1 included, is skipped); within a group, rows are ordered by ascending
+ * flattened route index t*K + k.
+ * Outputs: group_sizes[E], group_offsets[E+1] (exclusive scan, offsets[E] = R),
+ * row_map[T,K] (destination row or -1), perm_src[R] (source token of each
+ * destination row), x_perm[R, H] (bitwise copies of x rows; x_perm may be NULL).
+ * Returns R, the number of valid routes.
+ */
+long oracle_permute(const uint16_t *x, int T, int H, const int32_t *ids, int K, int E,
+                    uint16_t *x_perm, int32_t *group_sizes, int32_t *group_offsets,
+                    int32_t *row_map, int32_t *perm_src)
+{
+    for (int e = 0; e < E; e++)
+        group_sizes[e] = 0;
+    for (long i = 0; i < (long)T * K; i++)
+        if (ids[i] >= 0 && ids[i] < E)
+            group_sizes[ids[i]]++;
+    group_offsets[0] = 0;
+    for (int e = 0; e < E; e++)
+        group_offsets[e + 1] = group_offsets[e] + group_sizes[e];
+    int32_t *cursor = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (long i = 0; i < (long)T * K; i++) {
+        int e = ids[i];
+        if (e < 0 || e >= E) {
+            row_map[i] = -1;
+            continue;
+        }
+        long r = group_offsets[e] + cursor[e]++;
+        long t = i / K;
+        row_map[i] = (int32_t)r;
+        perm_src[r] = (int32_t)t;
+        if (x_perm)
+            memcpy(x_perm + r * H, x + t * H, sizeof(uint16_t) * (size_t)H);
+    }
+    free(cursor);
+    return group_offsets[E];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Unpermute / combine                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Probability-weighted combine back to token order ([TEJAX] figure and
+ * "Optimization 2": results are routed back and accumulated; [SPARSER]
+ * "Remove work that has no selected route": combine with probabilities).
+ * y[t,:] = bf16( sum over k ascending with row_map[t,k] >= 0 of
+ *                probs[t,k] * y_perm[row_map[t,k], :] ), accumulated in double.
+ * A token with no valid route gets zeros.
+ */
+void oracle_combine(const uint16_t *y_perm, const int32_t *row_map, const float *probs,
+                    int T, int K, int H, uint16_t *y)
+{
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int t = 0; t < T; t++) {
+        for (int j = 0; j < H; j++)
+            acc[j] = 0.0;
+        for (int k = 0; k < K; k++) {
+            long r = row_map[(size_t)t * K + k];
+            if (r < 0)
+                continue;
+            double p = (double)probs[(size_t)t * K + k];
+            for (int j = 0; j < H; j++)
+                acc[j] += p * oracle_bf16_to_double(y_perm[r * H + j]);
+        }
+        for (int j = 0; j < H; j++)
+            y[(size_t)t * H + j] = oracle_double_to_bf16(acc[j]);
+    }
+    free(acc);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped SwiGLU expert MLP                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A 2-D operand view. Element (r, c) of a [rows, cols] row-major matrix of
+ * kind MAT_BF16 (uint16 bits), MAT_F64 (double) or MAT_MXFP8 (E4M3 codes plus
+ * E8M0 scales; blocks of 32 run along rows when blk_rows, i.e. scale
+ * [rows/32, cols], else along columns, i.e. scale [rows, cols/32]).
+ */
+enum { MAT_BF16 = 0, MAT_F64 = 1, MAT_MXFP8 = 2 };
+
+typedef struct {
+    int kind;
+    const void *v;
+    const uint8_t *s;
+    long rows, cols;
+    int blk_rows;
+} mat;
+
+/* Row r of the matrix as doubles. */
+static void mat_row(const mat *m, long r, double *out)
+{
+    long c;
+    switch (m->kind) {
+    case MAT_BF16: {
+        const uint16_t *p = (const uint16_t *)m->v + r * m->cols;
+        for (c = 0; c < m->cols; c++)
+            out[c] = oracle_bf16_to_double(p[c]);
+        break;
+    }
+    case MAT_F64:
+        memcpy(out, (const double *)m->v + r * m->cols, sizeof(double) * (size_t)m->cols);
+        break;
+    default: {
+        const uint8_t *p = (const uint8_t *)m->v + r * m->cols;
+        for (c = 0; c < m->cols; c++) {
+            uint8_t sb = m->blk_rows ? m->s[(r / 32) * m->cols + c] : m->s[r * (m->cols / 32) + c / 32];
+            out[c] = mx_value(p[c], sb);
+        }
+    }
+    }
+}
+
+/* Expert e's slice of a stacked [E, rows, cols] weight view. */
+static mat expert_slice(const mat *w, int e)
+{
+    mat m = *w;
+    long n = w->rows * w->cols;
+    size_t esz = (w->kind == MAT_BF16) ? 2 : (w->kind == MAT_F64) ? 8 : 1;
+    m.v = (const char *)w->v + (size_t)e * (size_t)n * esz;
+    if (w->kind == MAT_MXFP8)
+        m.s = w->s + (size_t)e * (size_t)(n / 32);
+    return m;
+}
+
+static int expert_of_row(const int32_t *off, int E, long r)
+{
+    int lo = 0, hi = E - 1;            /* last e with off[e] <= r < off[e+1] */
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (off[mid] <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    while (lo < E - 1 && off[lo + 1] <= r)
+        lo++;
+    return lo;
+}
+
+static double silu(double a) { return a / (1.0 + exp(-a)); }
+
+/* Rounding applied to the intermediate h before the second GEMM. */
+enum { H_NONE = 0, H_BF16 = 1, H_MXFP8 = 2 };
+
+/*
+ * Grouped SwiGLU MLP on the listed rows of the permuted activations
+ * ([TEJAX] "Optimization 1: Grouped GEMM": every expert with its actual token
+ * count, only valid regions computed; figure: the grouped MLP is two grouped
+ * GEMMs on variable-length groups). For a row r of group e:
+ *   a[f] = sum_h x[r,h] W1[e][h,f],  b[f] = sum_h x[r,h] W3[e][h,f]
+ *   h[f] = silu(a[f]) * b[f],        silu(a) = a / (1 + exp(-a))
+ *   y[r,j] = sum_f round_h(h)[f] W2[e][f,j]
+ * Readings taken: silu gates the W1 product and W3 is the linear branch;
+ * round_h is none (h_mode 0), bf16 (1) or MXFP8 1x32 along F (2), applied to
+ * the unrounded h. Operand kinds: x [R_cap, H], W1/W3 [E][H, F], W2 [E][F, H]
+ * (weights in MXFP8 carry blocks along their contraction dimension).
+ * Outputs for row list entry i: y_bf16[i, H] (if not NULL), y_f64[i, H] (if not
+ * NULL, unrounded), h_bf16[i, F] (if not NULL), h_q[i, F] + h_s[i, F/32]
+ * (MXFP8 mode, if not NULL), h_f64[i, F] (if not NULL, unrounded),
+ * a_f64[i, F] and b_f64[i, F] (if not NULL: the two pre-activations).
+ */
+void oracle_swiglu_rows(int x_kind, const void *x_v, const uint8_t *x_s,
+                        int w_kind, const void *w1_v, const uint8_t *w1_s,
+                        const void *w3_v, const uint8_t *w3_s,
+                        const void *w2_v, const uint8_t *w2_s,
+                        const int32_t *group_offsets, int E, int H, int F, long R_cap,
+                        const int32_t *rows, long nrows, int h_mode,
+                        uint16_t *y_bf16, double *y_f64, uint16_t *h_bf16,
+                        uint8_t *h_q, uint8_t *h_s, double *h_f64,
+                        double *a_f64, double *b_f64)
+{
+    mat X = {x_kind, x_v, x_s, R_cap, H, 0};
+    mat W1 = {w_kind, w1_v, w1_s, H, F, 1};
+    mat W3 = {w_kind, w3_v, w3_s, H, F, 1};
+    mat W2 = {w_kind, w2_v, w2_s, F, H, 1};
+    double *xr = malloc(sizeof(double) * H), *a = malloc(sizeof(double) * F);
+    double *b = malloc(sizeof(double) * F), *hv = malloc(sizeof(double) * F);
+    double *wr = malloc(sizeof(double) * (F > H ? F : H)), *wr3 = malloc(sizeof(double) * F);
+    double *y = malloc(sizeof(double) * H);
+    uint8_t *qb = malloc((size_t)F), *sbuf = malloc((size_t)F / 32 + 1);
+    for (long i = 0; i < nrows; i++) {
+        long r = rows[i];
+        int e = expert_of_row(group_offsets, E, r);
+        mat w1 = expert_slice(&W1, e), w3 = expert_slice(&W3, e), w2 = expert_slice(&W2, e);
+        mat_row(&X, r, xr);
+        for (int f = 0; f < F; f++)
+            a[f] = b[f] = 0.0;
+        for (int h = 0; h < H; h++) {
+            mat_row(&w1, h, wr);
+            mat_row(&w3, h, wr3);
+            for (int f = 0; f < F; f++) {
+                a[f] += xr[h] * wr[f];
+                b[f] += xr[h] * wr3[f];
+            }
+        }
+        for (int f = 0; f < F; f++)
+            hv[f] = silu(a[f]) * b[f];
+        if (a_f64)
+            memcpy(a_f64 + i * F, a, sizeof(double) * F);
+        if (b_f64)
+            memcpy(b_f64 + i * F, b, sizeof(double) * F);
+        if (h_f64)
+            memcpy(h_f64 + i * F, hv, sizeof(double) * F);
+        if (h_mode == H_BF16) {
+            for (int f = 0; f < F; f++) {
+                uint16_t hb = oracle_double_to_bf16(hv[f]);
+                if (h_bf16)
+                    h_bf16[i * F + f] = hb;
+                hv[f] = oracle_bf16_to_double(hb);
+            }
+        } else if (h_mode == H_MXFP8) {
+            for (int blk = 0; blk < F / 32; blk++)
+                sbuf[blk] = (uint8_t)quant_block(hv + 32 * blk, 1, 32, qb + 32 * blk, 1);
+            for (int f = 0; f < F; f++)
+                hv[f] = mx_value(qb[f], sbuf[f / 32]);
+            if (h_q)
+                memcpy(h_q + i * F, qb, (size_t)F);
+            if (h_s)
+                memcpy(h_s + i * (F / 32), sbuf, (size_t)F / 32);
+        }
+        for (int j = 0; j < H; j++)
+            y[j] = 0.0;
+        for (int f = 0; f < F; f++) {
+            mat_row(&w2, f, wr);
+            for (int j = 0; j < H; j++)
+                y[j] += hv[f] * wr[j];
+        }
+        for (int j = 0; j < H; j++) {
+            if (y_bf16)
+                y_bf16[i * H + j] = oracle_double_to_bf16(y[j]);
+            if (y_f64)
+                y_f64[i * H + j] = y[j];
+        }
+    }
+    free(xr); free(a); free(b); free(hv); free(wr); free(wr3); free(y); free(qb); free(sbuf);
+}
+
+/*
+ * Backward of the grouped SwiGLU MLP, activation gradient (dgrad), for the
+ * listed rows. Given the forward pre-activations a, b of each row (as the
+ * forward computed them, see oracle_swiglu_rows' a_f64 / b_f64 outputs):
+ *   dh[f] = sum_j dy[r,j] W2[e][f,j]
+ *   da[f] = dh[f] * b[f] * silu'(a[f]),   silu'(a) = s(a) (1 + a (1 - s(a))), s = logistic
+ *   db[f] = dh[f] * silu(a[f])
+ *   dx[r,h] = sum_f da[f] W1[e][h,f] + db[f] W3[e][h,f]
+ * Operand views: dy [R_cap, H], a and b [R_cap, F] (bf16 or f64), weights as in
+ * the forward; for MXFP8 weights w_blk_rows says along which dimension of the
+ * stored [H,F] / [F,H] matrices the 32-blocks run (the backward contracts
+ * W2 over its columns and W1, W3 over their columns, so a caller quantising for
+ * the backward passes column blocks, w_blk_rows = 0).
+ * Outputs per listed row (each optional): dx_bf16 / dx_f64 [H], da_f64 / db_f64 [F].
+ */
+void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s,
+                              int ab_kind, const void *a_v, const void *b_v,
+                              int w_kind, int w_blk_rows,
+                              const void *w1_v, const uint8_t *w1_s,
+                              const void *w3_v, const uint8_t *w3_s,
+                              const void *w2_v, const uint8_t *w2_s,
+                              const int32_t *group_offsets, int E, int H, int F, long R_cap,
+                              const int32_t *rows, long nrows,
+                              uint16_t *dx_bf16, double *dx_f64, double *da_f64, double *db_f64)
+{
+    mat DY = {dy_kind, dy_v, dy_s, R_cap, H, 0};
+    mat A = {ab_kind, a_v, NULL, R_cap, F, 0};
+    mat B = {ab_kind, b_v, NULL, R_cap, F, 0};
+    mat W1 = {w_kind, w1_v, w1_s, H, F, w_blk_rows};
+    mat W3 = {w_kind, w3_v, w3_s, H, F, w_blk_rows};
+    mat W2 = {w_kind, w2_v, w2_s, F, H, w_blk_rows};
+    double *dyr = malloc(sizeof(double) * H);
+    double *a = malloc(sizeof(double) * F), *b = malloc(sizeof(double) * F);
+    double *dh = malloc(sizeof(double) * F), *da = malloc(sizeof(double) * F);
+    double *db = malloc(sizeof(double) * F), *dx = malloc(sizeof(double) * H);
+    double *wr = malloc(sizeof(double) * (F > H ? F : H)), *wr3 = malloc(sizeof(double) * F);
+    for (long i = 0; i < nrows; i++) {
+        long r = rows[i];
+        int e = expert_of_row(group_offsets, E, r);
+        mat w1 = expert_slice(&W1, e), w3 = expert_slice(&W3, e), w2 = expert_slice(&W2, e);
+        mat_row(&DY, r, dyr);
+        mat_row(&A, r, a);
+        mat_row(&B, r, b);
+        for (int f = 0; f < F; f++) {
+            mat_row(&w2, f, wr);
+            double acc = 0.0;
+            for (int j = 0; j < H; j++)
+                acc += dyr[j] * wr[j];
+            dh[f] = acc;
+        }
+        for (int f = 0; f < F; f++) {
+            double sg = 1.0 / (1.0 + exp(-a[f]));
+            da[f] = dh[f] * b[f] * (sg * (1.0 + a[f] * (1.0 - sg)));
+            db[f] = dh[f] * silu(a[f]);
+        }
+        for (int h = 0; h < H; h++) {
+            mat_row(&w1, h, wr);
+            mat_row(&w3, h, wr3);
+            double acc = 0.0;
+            for (int f = 0; f < F; f++)
+                acc += da[f] * wr[f] + db[f] * wr3[f];
+            dx[h] = acc;
+        }
+        for (int h = 0; h < H; h++) {
+            if (dx_bf16)
+                dx_bf16[i * H + h] = oracle_double_to_bf16(dx[h]);
+            if (dx_f64)
+                dx_f64[i * H + h] = dx[h];
+        }
+        if (da_f64)
+            memcpy(da_f64 + i * F, da, sizeof(double) * F);
+        if (db_f64)
+            memcpy(db_f64 + i * F, db, sizeof(double) * F);
+    }
+    free(dyr); free(a); free(b); free(dh); free(da); free(db); free(dx);
+    free(wr); free(wr3);
+}
+
+/*
+ * Weight gradient (wgrad) of one expert, contraction over the rows of its
+ * group (a ragged contraction length m_e = off[e+1] - off[e]):
+ *   dW[c1, c2] = sum_{r in group e} A[r, c1] * B[r, c2]
+ * for the listed output columns c2 only (all c1). With A = h, B = dy this is
+ * dW2[e]; with A = x, B = da (or db) it is dW1[e] (or dW3[e]).
+ * A [R_cap, n1] and B [R_cap, n2] are operand views (MXFP8 views carry
+ * group-aware column-wise scales, see oracle_quant_cols_grouped_bf16).
+ * Output dw_f64[n1, ncols] (column i of the output is c2 = cols[i]).
+ */
+void oracle_wgrad_expert(int a_kind, const void *a_v, const uint8_t *a_s, long n1,
+                         int b_kind, const void *b_v, const uint8_t *b_s, long n2,
+                         const int32_t *group_offsets, int E, int e, long R_cap,
+                         const int32_t *cols, long ncols, double *dw_f64)
+{
+    long r0 = group_offsets[e], r1 = group_offsets[e + 1];
+    double *ar = malloc(sizeof(double) * n1), *br = malloc(sizeof(double) * n2);
+    for (long i = 0; i < n1 * ncols; i++)
+        dw_f64[i] = 0.0;
+    for (long r = r0; r < r1; r++) {
+        /* group-aware column-wise MXFP8 views: scale row for r is
+         * e + off[e]/32 + (r - off[e])/32 (see oracle_quant_cols_grouped_bf16) */
+        long srow = e + r0 / 32 + (r - r0) / 32;
+        if (a_kind == MAT_MXFP8) {
+            for (long c = 0; c < n1; c++)
+                ar[c] = mx_value(((const uint8_t *)a_v)[r * n1 + c], a_s[srow * n1 + c]);
+        } else {
+            mat A = {a_kind, a_v, NULL, R_cap, n1, 0};
+            mat_row(&A, r, ar);
+        }
+        if (b_kind == MAT_MXFP8) {
+            for (long c = 0; c < n2; c++)
+                br[c] = mx_value(((const uint8_t *)b_v)[r * n2 + c], b_s[srow * n2 + c]);
+        } else {
+            mat B = {b_kind, b_v, NULL, R_cap, n2, 0};
+            mat_row(&B, r, br);
+        }
+        for (long c1 = 0; c1 < n1; c1++)
+            for (long i = 0; i < ncols; i++)
+                dw_f64[c1 * ncols + i] += ar[c1] * br[cols[i]];
+    }
+    free(ar);
+    free(br);
+    (void)E;
+}
+
+/* Expert of a permuted row (exported for the tests' sampling helpers). */
+int oracle_expert_of_row(const int32_t *group_offsets, int E, long r)
+{
+    return expert_of_row(group_offsets, E, r);
+}

@@ -1,0 +1,248 @@
+"""Pins for the oracle's grouped SwiGLU MLP (forward, dgrad, wgrad).
+
+Independent references: numpy float64 matmuls per expert on the logical
+layouts (a library routine), hand-built weights with known results, torch's
+float8 decode for MXFP8 operands, and central finite differences for the
+backward formulas.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+
+def _bf16(x):
+    t = torch.from_numpy(np.asarray(x, np.float64)).to(torch.float32).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _f(bits):
+    return O.bf16_to_f64(bits)
+
+
+def _problem(seed, E=4, H=64, F=96, sizes=(5, 0, 17, 9), R_extra=6, std=0.3):
+    rng = np.random.default_rng(seed)
+    sizes = np.array(sizes, np.int32)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R_cap = int(off[-1]) + R_extra
+    x = _bf16(rng.standard_normal((R_cap, H)) * std)
+    w1 = _bf16(rng.standard_normal((E, H, F)) * std)
+    w3 = _bf16(rng.standard_normal((E, H, F)) * std)
+    w2 = _bf16(rng.standard_normal((E, F, H)) * std)
+    return x, w1, w3, w2, off
+
+
+def _silu(a):
+    return a / (1 + np.exp(-a))
+
+
+def _np_forward(xv, w1v, w3v, w2v, off, round_h=None):
+    E = off.size - 1
+    y = np.zeros((int(off[-1]), xv.shape[1]))
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        a = xv[r0:r1] @ w1v[e]
+        b = xv[r0:r1] @ w3v[e]
+        h = _silu(a) * b
+        if round_h is not None:
+            h = round_h(h)
+        y[r0:r1] = h @ w2v[e]
+    return y
+
+
+def test_forward_f64_matches_numpy_per_expert():
+    x, w1, w3, w2, off = _problem(1)
+    R = int(off[-1])
+    rows = np.arange(R, dtype=np.int32)
+    out = O.swiglu_rows(O.Operand(O.MAT_BF16, x), O.Operand(O.MAT_BF16, w1),
+                        O.Operand(O.MAT_BF16, w3), O.Operand(O.MAT_BF16, w2), off, rows,
+                        h_mode=O.H_NONE, want=("y_f64", "h_f64"))
+    want = _np_forward(_f(x), _f(w1), _f(w3), _f(w2), off)
+    assert np.allclose(out["y_f64"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_bf16_h_rounding_and_output():
+    x, w1, w3, w2, off = _problem(2)
+    R = int(off[-1])
+    rows = np.arange(R, dtype=np.int32)[::-1].copy()          # any row order
+    out = O.swiglu_rows(O.Operand(O.MAT_BF16, x), O.Operand(O.MAT_BF16, w1),
+                        O.Operand(O.MAT_BF16, w3), O.Operand(O.MAT_BF16, w2), off, rows,
+                        h_mode=O.H_BF16, want=("y_bf16", "h_bf16", "h_f64"))
+    assert np.array_equal(out["h_bf16"], _bf16(out["h_f64"]))
+    want = _np_forward(_f(x), _f(w1), _f(w3), _f(w2), off, round_h=lambda h: _f(_bf16(h)))
+    got = _f(out["y_bf16"])
+    assert np.all(np.abs(got - want[rows]) <= np.abs(want[rows]) * 2.0 ** -8 + 1e-30)
+
+
+def test_forward_hand_cases():
+    E, H, F = 2, 32, 32
+    off = np.array([0, 3, 5], np.int32)
+    x = _bf16(np.random.default_rng(3).standard_normal((5, H)))
+    z = np.zeros((E, H, F), np.uint16)
+    w2 = _bf16(np.ones((E, F, H)))
+    rows = np.arange(5, dtype=np.int32)
+    out = O.swiglu_rows(O.Operand(O.MAT_BF16, x), O.Operand(O.MAT_BF16, z),
+                        O.Operand(O.MAT_BF16, z), O.Operand(O.MAT_BF16, w2), off, rows,
+                        want=("y_f64",))
+    assert np.all(out["y_f64"] == 0)
+    # one-hot: W1[e][h, f] = [h == f] * 8 (large a -> silu(a) ~ a), W3 = [h == f],
+    # W2[e] = I * (e + 1): y[r, j] = (e+1) * silu(8 x_j) * x_j
+    w1 = np.zeros((E, H, F))
+    w3 = np.zeros((E, H, F))
+    w2 = np.zeros((E, F, H))
+    for e in range(E):
+        w1[e] = np.eye(H) * 8
+        w3[e] = np.eye(H)
+        w2[e] = np.eye(H) * (e + 1)
+    out = O.swiglu_rows(O.Operand(O.MAT_BF16, x), O.Operand(O.MAT_BF16, _bf16(w1)),
+                        O.Operand(O.MAT_BF16, _bf16(w3)), O.Operand(O.MAT_BF16, _bf16(w2)),
+                        off, rows, h_mode=O.H_NONE, want=("y_f64",))
+    xv = _f(x)
+    scale = np.array([1, 1, 1, 2, 2])[:, None]
+    assert np.allclose(out["y_f64"], scale * _silu(8 * xv) * xv, rtol=1e-12)
+
+
+def _mx_decode(q, s, blk_rows):
+    v = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if blk_rows:
+        sc = np.repeat(s.astype(np.float64), 32, axis=-2)
+    else:
+        sc = np.repeat(s.astype(np.float64), 32, axis=-1)
+    return v * np.exp2(sc - 127)
+
+
+def test_forward_mxfp8_operands_match_numpy_on_decoded_values():
+    x, w1, w3, w2, off = _problem(4, H=64, F=64)
+    E = off.size - 1
+    xq, xs = O.quant_rows(x)
+    # weights quantised along their contraction dimension (rows of [H,F] / [F,H])
+    def qcols(w):
+        qs, ss = [], []
+        for e in range(E):
+            q, s = O.quant_rows(np.ascontiguousarray(w[e].T))
+            qs.append(q.T)
+            ss.append(s.T)
+        return np.ascontiguousarray(np.stack(qs)), np.ascontiguousarray(np.stack(ss))
+    w1q, w1s = qcols(w1)
+    w3q, w3s = qcols(w3)
+    w2q, w2s = qcols(w2)
+    R = int(off[-1])
+    rows = np.arange(R, dtype=np.int32)
+    out = O.swiglu_rows(O.Operand(O.MAT_MXFP8, xq, xs), O.Operand(O.MAT_MXFP8, w1q, w1s),
+                        O.Operand(O.MAT_MXFP8, w3q, w3s), O.Operand(O.MAT_MXFP8, w2q, w2s),
+                        off, rows, h_mode=O.H_MXFP8, want=("y_f64", "h_q", "h_s", "h_f64"))
+    xd = _mx_decode(xq, xs, False)
+    w1d, w3d, w2d = (_mx_decode(q, s, True) for q, s in ((w1q, w1s), (w3q, w3s), (w2q, w2s)))
+    # h is quantised row-wise along F, straight from the unrounded value
+    hq, hs = out["h_q"], out["h_s"]
+    hd = _mx_decode(hq, hs, False)
+    want_h = np.concatenate([_silu(xd[off[e]:off[e + 1]] @ w1d[e]) * (xd[off[e]:off[e + 1]] @ w3d[e])
+                             for e in range(E)])
+    assert np.allclose(out["h_f64"], want_h, rtol=1e-12, atol=1e-14)
+    err = np.abs(hd - want_h)
+    unit = np.exp2(np.repeat(hs - 127.0, 32, 1))
+    sat = np.abs(want_h) / unit > 448          # above E4M3's range at this block scale
+    assert np.all(err[~sat] <= (np.abs(want_h) * 2.0 ** -4 + unit * 2 ** -10)[~sat])
+    assert np.all(np.abs(hd[sat]) == 448 * unit[sat])
+    want_y = np.concatenate([hd[off[e]:off[e + 1]] @ w2d[e] for e in range(E)])
+    assert np.allclose(out["y_f64"], want_y, rtol=1e-12, atol=1e-14)
+
+
+def test_dgrad_matches_finite_differences():
+    E, H, F = 2, 8, 8
+    rng = np.random.default_rng(5)
+    off = np.array([0, 2, 5], np.int32)
+    x = rng.standard_normal((5, H))
+    w1, w3 = rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F))
+    w2 = rng.standard_normal((E, F, H))
+    dy = rng.standard_normal((5, H))
+    rows = np.arange(5, dtype=np.int32)
+    W = lambda a: O.Operand(O.MAT_F64, a)
+
+    def loss(xx, ww1, ww3):
+        y = O.swiglu_rows(W(xx), W(ww1), W(ww3), W(w2), off, rows, h_mode=O.H_NONE,
+                          want=("y_f64",))["y_f64"]
+        return float((y * dy).sum())
+
+    fw = O.swiglu_rows(W(x), W(w1), W(w3), W(w2), off, rows, h_mode=O.H_NONE,
+                       want=("a_f64", "b_f64"))
+    bw = O.swiglu_dgrad_rows(W(dy), W(fw["a_f64"]), W(fw["b_f64"]), W(w1), W(w3), W(w2),
+                             off, rows, want=("dx_f64", "da_f64", "db_f64"))
+    eps = 1e-6
+    for r in range(5):
+        for h in range(H):
+            xp, xm = x.copy(), x.copy()
+            xp[r, h] += eps
+            xm[r, h] -= eps
+            fd = (loss(xp, w1, w3) - loss(xm, w1, w3)) / (2 * eps)
+            assert abs(fd - bw["dx_f64"][r, h]) <= 1e-6 * (1 + abs(fd))
+    # wgrad of W1 / W3 from da / db: dW1[e] = x_e^T da_e
+    for e in range(E):
+        dW1 = O.wgrad_expert(W(x), W(bw["da_f64"]), off, e)
+        dW3 = O.wgrad_expert(W(x), W(bw["db_f64"]), off, e)
+        for (h, f) in [(0, 0), (3, 5), (7, 7), (2, 6)]:
+            for ww, dW in ((0, dW1), (1, dW3)):
+                wp = [w1.copy(), w3.copy()]
+                wm = [w1.copy(), w3.copy()]
+                wp[ww][e, h, f] += eps
+                wm[ww][e, h, f] -= eps
+                fd = (loss(x, *wp) - loss(x, *wm)) / (2 * eps)
+                assert abs(fd - dW[h, f]) <= 1e-6 * (1 + abs(fd))
+
+
+def test_wgrad_dw2_matches_finite_differences_and_numpy():
+    E, H, F = 3, 8, 16
+    rng = np.random.default_rng(6)
+    off = np.array([0, 4, 4, 7], np.int32)          # expert 1 is empty
+    x = rng.standard_normal((9, H))
+    w1, w3 = rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F))
+    w2 = rng.standard_normal((E, F, H))
+    dy = rng.standard_normal((9, H))
+    rows = np.arange(7, dtype=np.int32)
+    W = lambda a: O.Operand(O.MAT_F64, a)
+    fw = O.swiglu_rows(W(x), W(w1), W(w3), W(w2), off, rows, h_mode=O.H_NONE, want=("h_f64",))
+    h = np.zeros((9, F))
+    h[:7] = fw["h_f64"]
+    for e in range(E):
+        dW2 = O.wgrad_expert(W(h), W(dy), off, e)
+        r0, r1 = off[e], off[e + 1]
+        assert np.allclose(dW2, h[r0:r1].T @ dy[r0:r1], rtol=1e-13, atol=1e-13)
+        cols = np.array([H - 1, 0, 3], np.int32)
+        sub = O.wgrad_expert(W(h), W(dy), off, e, cols=cols)
+        assert np.allclose(sub, dW2[:, cols])
+    e, f, j = 2, 5, 3
+    eps = 1e-6
+
+    def loss(ww2):
+        y = O.swiglu_rows(W(x), W(w1), W(w3), W(ww2), off, rows, h_mode=O.H_NONE,
+                          want=("y_f64",))["y_f64"]
+        return float((y * dy[:7]).sum())
+    wp, wm = w2.copy(), w2.copy()
+    wp[e, f, j] += eps
+    wm[e, f, j] -= eps
+    fd = (loss(wp) - loss(wm)) / (2 * eps)
+    assert abs(fd - O.wgrad_expert(W(h), W(dy), off, e)[f, j]) <= 1e-6 * (1 + abs(fd))
+
+
+def test_wgrad_mxfp8_colwise_operands_decode_like_torch():
+    rng = np.random.default_rng(7)
+    sizes = np.array([40, 0, 33], np.int32)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R_cap = int(off[-1]) + 5
+    a = _bf16(rng.standard_normal((R_cap, 32)))
+    b = _bf16(rng.standard_normal((R_cap, 64)))
+    aq, as_ = O.quant_cols_grouped(a, off)
+    bq, bs = O.quant_cols_grouped(b, off)
+    for e in (0, 2):
+        got = O.wgrad_expert(O.Operand(O.MAT_MXFP8, aq, as_), O.Operand(O.MAT_MXFP8, bq, bs),
+                             off, e)
+        r0, r1 = off[e], off[e + 1]
+        ad = torch.from_numpy(aq[r0:r1]).view(torch.float8_e4m3fn).double().numpy()
+        bd = torch.from_numpy(bq[r0:r1]).view(torch.float8_e4m3fn).double().numpy()
+        srows = e + r0 // 32 + np.arange(r1 - r0) // 32
+        ad = ad * np.exp2(as_[srows].astype(np.float64) - 127)
+        bd = bd * np.exp2(bs[srows].astype(np.float64) - 127)
+        assert np.allclose(got, ad.T @ bd, rtol=1e-12, atol=1e-12)
+        # and the decoded operands approximate the bf16 ones
+        assert np.allclose(ad, _f(a[r0:r1]), rtol=2 ** -3, atol=1e-3)   # saturation: <= 1/8
