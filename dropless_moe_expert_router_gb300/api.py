@@ -1,0 +1,190 @@
+"""Thin Python binding of the C ABI (include/moe_gb300.h).
+
+Each function has the name of its C entry point and only marshals arguments:
+it checks devices and dtypes, allocates outputs with torch when the caller did
+not pass them, and hands raw pointers, sizes and the current CUDA stream to
+the library. Every step of the computation runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import _lib
+
+MOE_I16, MOE_I32, MOE_BF16, MOE_MXFP8 = 0, 1, 2, 3
+MOE_ROUTE_RENORM = 1
+MOE_PERMUTE_FUSE_MXFP8 = 2
+MOE_QUANT_COLWISE = 4
+MOE_DEVERR_BAD_ID = 1
+MOE_DEVERR_TIMEOUT = 2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        name = _lib.load().moe_status_string(status).decode()
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MoeError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _want(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def _id_code(dtype: torch.dtype) -> int:
+    if dtype == torch.int16:
+        return MOE_I16
+    if dtype == torch.int32:
+        return MOE_I32
+    raise ValueError("ids must be int16 or int32")
+
+
+# --------------------------------------------------------------------- router
+def moe_route_topk(logits: torch.Tensor, K: int, *, id_dtype=torch.int32, renorm: bool = False,
+                   ids: Optional[torch.Tensor] = None, probs: Optional[torch.Tensor] = None,
+                   stream=None):
+    """logits [T, E] fp32 -> (ids [T, K] int16/int32, probs [T, K] fp32)."""
+    _want(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    if ids is None:
+        ids = torch.empty((T, K), dtype=id_dtype, device=logits.device)
+    if probs is None:
+        probs = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    _want(ids, "ids", None, 2)
+    _want(probs, "probs", torch.float32, 2)
+    st = _lib.load().moe_route_topk(_ptr(logits), T, E, K, _ptr(ids), _id_code(ids.dtype), _ptr(probs),
+                                    MOE_ROUTE_RENORM if renorm else 0, _stream(stream))
+    _check("moe_route_topk", st)
+    return ids, probs
+
+
+# -------------------------------------------------------------------- permute
+class Permuted(NamedTuple):
+    x_perm: torch.Tensor          # [T*K, H] bf16, or uint8 E4M3 payloads when fused
+    x_perm_scales: Optional[torch.Tensor]  # [T*K, H/32] uint8 E8M0 (fused MXFP8 only)
+    group_sizes: torch.Tensor     # [E] int32
+    group_offsets: torch.Tensor   # [E+1] int32
+    row_map: torch.Tensor         # [T, K] int32
+    perm_src: torch.Tensor        # [T*K] int32
+
+
+def moe_permute_workspace_size(T: int, K: int, E: int) -> int:
+    return int(_lib.load().moe_permute_workspace_size(T, K, E))
+
+
+def permute_buffers(T: int, H: int, K: int, E: int, device, fuse_mxfp8: bool = False) -> Permuted:
+    R_cap = T * K
+    dev = torch.device(device)
+    if fuse_mxfp8:
+        xp = torch.empty((R_cap, H), dtype=torch.uint8, device=dev)
+        xs = torch.empty((R_cap, H // 32), dtype=torch.uint8, device=dev)
+    else:
+        xp = torch.empty((R_cap, H), dtype=torch.bfloat16, device=dev)
+        xs = None
+    return Permuted(xp, xs, torch.empty(E, dtype=torch.int32, device=dev),
+                    torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    torch.empty((T, K), dtype=torch.int32, device=dev),
+                    torch.empty(R_cap, dtype=torch.int32, device=dev))
+
+
+def moe_permute(x: torch.Tensor, ids: torch.Tensor, E: int, *, fuse_mxfp8: bool = False,
+                out: Optional[Permuted] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> Permuted:
+    """x [T, H] bf16, ids [T, K] -> Permuted (see the C header for each field)."""
+    _want(x, "x", torch.bfloat16, 2)
+    _want(ids, "ids", None, 2)
+    T, H = x.shape
+    K = ids.shape[1]
+    if out is None:
+        out = permute_buffers(T, H, K, E, x.device, fuse_mxfp8)
+    ws_bytes = moe_permute_workspace_size(T, K, E)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st = _lib.load().moe_permute(
+        _ptr(x), T, H, _ptr(ids), _id_code(ids.dtype), K, E, _ptr(out.x_perm), _ptr(out.x_perm_scales),
+        _ptr(out.group_sizes), _ptr(out.group_offsets), _ptr(out.row_map), _ptr(out.perm_src),
+        MOE_PERMUTE_FUSE_MXFP8 if fuse_mxfp8 else 0, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("moe_permute", st)
+    return out
+
+
+# ---------------------------------------------------------------- quantiser
+def colwise_scale_rows(R_cap: int, E: int) -> int:
+    return E + R_cap // 32 + 1
+
+
+def moe_quant_mxfp8_grouped(x: torch.Tensor, group_offsets: torch.Tensor, *, colwise: bool = False,
+                            q: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                            stream=None):
+    """x [R_cap, H] bf16 -> (q [R_cap, H] uint8, scales) row-wise or group-aware column-wise."""
+    _want(x, "x", torch.bfloat16, 2)
+    _want(group_offsets, "group_offsets", torch.int32, 1)
+    R_cap, H = x.shape
+    E = group_offsets.numel() - 1
+    if q is None:
+        q = torch.empty((R_cap, H), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        shape = (colwise_scale_rows(R_cap, E), H) if colwise else (R_cap, H // 32)
+        scales = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    st = _lib.load().moe_quant_mxfp8_grouped(_ptr(x), R_cap, H, _ptr(group_offsets), E, _ptr(q),
+                                             _ptr(scales), MOE_QUANT_COLWISE if colwise else 0,
+                                             _stream(stream))
+    _check("moe_quant_mxfp8_grouped", st)
+    return q, scales
+
+
+# ------------------------------------------------------------------- combine
+def moe_unpermute_combine(y_perm: torch.Tensor, row_map: torch.Tensor, probs: torch.Tensor, *,
+                          y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y_perm [R_cap, H] bf16, row_map [T, K], probs [T, K] -> y [T, H] bf16."""
+    _want(y_perm, "y_perm", torch.bfloat16, 2)
+    _want(row_map, "row_map", torch.int32, 2)
+    _want(probs, "probs", torch.float32, 2)
+    T, K = row_map.shape
+    H = y_perm.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=y_perm.device)
+    st = _lib.load().moe_unpermute_combine(_ptr(y_perm), _ptr(row_map), _ptr(probs), T, K, H, _ptr(y),
+                                           _stream(stream))
+    _check("moe_unpermute_combine", st)
+    return y
+
+
+# -------------------------------------------------------------------- errors
+def moe_get_device_errors(clear: bool = True) -> int:
+    v = C.c_uint32(0)
+    st = _lib.load().moe_get_device_errors(C.byref(v), 1 if clear else 0)
+    if st not in (0, 6):
+        _check("moe_get_device_errors", st)
+    return int(v.value)
+
+
+def moe_route_ids_bytes(T: int, K: int, id_dtype=torch.int16) -> int:
+    return int(_lib.load().moe_route_ids_bytes(T, K, _id_code(id_dtype)))
+
+
+def moe_route_probs_bytes(T: int, K: int) -> int:
+    return int(_lib.load().moe_route_probs_bytes(T, K))

@@ -1,0 +1,109 @@
+// combine.cu -- probability-weighted unpermute/combine back to token order.
+//
+// "Dropless MoE acceleration in JAX with NVIDIA Transformer Engine", section
+// "Optimization 2": after the experts ran, results are routed back and
+// accumulated in token order; "Sparser MoE end-to-end", section "Remove work
+// that has no selected route": combine pulls and reduces, and visits only the
+// selected slots of each token.
+//
+// One warp per token: a ballot over the token's K route slots (row_map >= 0)
+// gives the rows to pull; each lane owns 16-byte column chunks and accumulates
+// probs[t,k] * y_perm[row, chunk] in fp32, in ascending k, then rounds to bf16.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int CHUNKS = 2;  // 16-byte chunks in flight per lane and route
+
+template <int KC>
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
+                                                      const int* __restrict__ row_map,
+                                                      const float* __restrict__ probs, int T, int K, int H,
+                                                      uint4* __restrict__ y) {
+    const int lane = (int)lane_id();
+    const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    const int H8 = H >> 3;
+    for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
+        int rows[KC];
+        float p[KC];
+        unsigned mask[KC];
+#pragma unroll
+        for (int c = 0; c < KC; c++) {
+            int k = c * 32 + lane;
+            int r = -1;
+            float pk = 0.0f;
+            if (k < K) {
+                r = __ldg(row_map + t * K + k);
+                pk = __ldg(probs + t * K + k);
+            }
+            rows[c] = r;
+            p[c] = pk;
+            mask[c] = __ballot_sync(FULL, r >= 0);
+        }
+        for (int j0 = 0; j0 < H8; j0 += 32 * CHUNKS) {
+            float acc[CHUNKS][8];
+#pragma unroll
+            for (int u = 0; u < CHUNKS; u++)
+#pragma unroll
+                for (int i = 0; i < 8; i++) acc[u][i] = 0.0f;
+#pragma unroll
+            for (int c = 0; c < KC; c++) {
+                unsigned m = mask[c];
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int r = __shfl_sync(FULL, rows[c], b);
+                    const float pk = __shfl_sync(FULL, p[c], b);
+                    uint4 v[CHUNKS];
+#pragma unroll
+                    for (int u = 0; u < CHUNKS; u++) {
+                        const int j = j0 + u * 32 + lane;
+                        v[u] = j < H8 ? __ldg(y_perm + (long long)r * H8 + j) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < CHUNKS; u++) {
+                        float f[8];
+                        bf16x8_to_f32(v[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) acc[u][i] = fmaf(pk, f[i], acc[u][i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < CHUNKS; u++) {
+                const int j = j0 + u * 32 + lane;
+                if (j < H8) y[t * H8 + j] = f32_to_bf16x8(acc[u]);
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_unpermute_combine(const void* y_perm, const int32_t* row_map, const float* probs,
+                                            int T, int K, int H, void* y, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || K < 1 || K > 128 || H < 8 || (H % 8) != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !row_map || !probs || !y) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned(y_perm, 16) || !moe_host::aligned(y, 16) || !moe_host::aligned(row_map, 4) ||
+        !moe_host::aligned(probs, 4))
+        return MOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = ((long long)T + 7) / 8;
+    const long long cap = (long long)sms * 16;
+    if (blocks > cap) blocks = cap;
+    cudaStream_t s = moe_host::as_stream(stream);
+    const int KC = (K + 31) / 32;
+    if (KC == 1)
+        combine_kernel<1><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
+    else if (KC == 2)
+        combine_kernel<2><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
+    else
+        combine_kernel<4><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
+    return moe_host::launch_status();
+}

@@ -1,0 +1,112 @@
+// common.cuh -- shared device helpers of the GB300 dropless-MoE library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Device error word (MOE_DEVERR_* bits); one per device, read by moe_get_device_errors.
+extern __device__ unsigned int g_device_errors;
+
+__device__ __forceinline__ void raise_device_error(unsigned bits) { atomicOr(&g_device_errors, bits); }
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Read an expert id of either width.
+__device__ __forceinline__ int load_id(const void* ids, long long i, bool i16) {
+    return i16 ? (int)((const int16_t*)ids)[i] : ((const int32_t*)ids)[i];
+}
+
+// ---------------------------------------------------------------- MXFP8 block rule
+// E8M0 byte of a block with absolute maximum `amax` (finite, >= 0):
+// floor(log2(amax)) - 8 + 127, clamped to [0, 254]; 127 for amax == 0.
+__device__ __forceinline__ int e8m0_scale_byte(float amax) {
+    if (amax == 0.0f) return 127;
+    unsigned u = __float_as_uint(amax);
+    int ebits = (int)((u >> 23) & 0xffu);
+    int fl;  // floor(log2(amax))
+    if (ebits != 0) {
+        fl = ebits - 127;
+    } else {  // subnormal: mantissa m, amax = m * 2^-149, leading one at bit p -> 2^(p-149)
+        fl = (31 - __clz((int)(u & 0x7fffffu))) - 149;
+    }
+    int b = fl - 8 + 127;
+    return b < 0 ? 0 : (b > 254 ? 254 : b);
+}
+
+// 2^(127 - byte) as a float; exact for byte in [0, 253].
+__device__ __forceinline__ float e8m0_inv_scale(int byte) {
+    return __uint_as_float((unsigned)(254 - byte) << 23);
+}
+
+// Two floats -> two E4M3 codes (round to nearest even, saturate to +-448), packed lo|hi<<8.
+__device__ __forceinline__ unsigned short f32x2_to_e4m3x2(float lo, float hi) {
+    return (unsigned short)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// 8 bf16 (one uint4) -> floats.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(p[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+    uint4 v;
+    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; i++) p[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+// Quantise the 8 floats one lane holds, where four consecutive lanes hold one
+// 32-element block: returns the 8 E4M3 codes and (in *sbyte) the block's scale byte.
+__device__ __forceinline__ uint2 quant8_in_quad(const float* f, int* sbyte) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+    int sb = e8m0_scale_byte(amax);
+    float inv = e8m0_inv_scale(sb);
+    uint2 out;
+    out.x = (unsigned)f32x2_to_e4m3x2(f[0] * inv, f[1] * inv) |
+            ((unsigned)f32x2_to_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+    out.y = (unsigned)f32x2_to_e4m3x2(f[4] * inv, f[5] * inv) |
+            ((unsigned)f32x2_to_e4m3x2(f[6] * inv, f[7] * inv) << 16);
+    *sbyte = sb;
+    return out;
+}
+
+}  // namespace moe
+
+// Host-side helpers shared by the entry points.
+namespace moe_host {
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline moe_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline cudaStream_t as_stream(moe_stream_t s) { return (cudaStream_t)s; }
+
+}  // namespace moe_host

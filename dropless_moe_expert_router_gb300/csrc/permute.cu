@@ -1,0 +1,425 @@
+// permute.cu -- dropless dispatch into expert-contiguous order, the standalone
+// group-aware MXFP8 quantiser, and their entry points.
+//
+// The permutation is a deterministic device-side counting sort of the T*K
+// routes by expert ("Dropless MoE acceleration in JAX with NVIDIA Transformer
+// Engine", sections "Dropless vs capacity-based MoE" and "Optimization 1":
+// every route is kept, group sizes never leave the device; "Sparser MoE
+// end-to-end", section "Remove work that has no selected route": local
+// processing visits only the selected slots of a token, found by a warp ballot):
+//
+//   1. rank    (warp per tile of TT tokens): walks the tile's routes in
+//              flattened order, 32 at a time; __match_any groups the lanes of
+//              one expert, so each valid route gets its rank among the tile's
+//              earlier routes of the same expert. Writes per-(expert, tile)
+//              counts to the workspace table [E][tiles] and the tile-local rank
+//              into row_map.
+//   2. scan    (warp per expert, then the last block to finish): exclusive scan
+//              of each expert's counts over tiles -> per-tile bases, group_sizes;
+//              the last block scans group_sizes -> group_offsets.
+//   3. scatter (warp per token): row = group_offsets[e] + base[e][tile] + rank;
+//              a ballot over the token's valid slots gives the destinations,
+//              the token row is read once and stored to each of them with 16-byte
+//              vectors (optionally quantised to MXFP8 on the way).
+// Rows within an expert end up in ascending t*K + k order, independent of
+// scheduling.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int SCAN_THREADS = 1024;
+
+inline int tile_tokens(int E) { return E > 64 ? 32 : 128; }
+
+struct PermuteWs {
+    int* table;        // [E][tiles]
+    unsigned* ticket;  // completion counter of the scan kernel
+};
+
+inline size_t align16(size_t n) { return (n + 15) & ~(size_t)15; }
+
+inline PermuteWs carve(void* ws, int E, int tiles) {
+    PermuteWs w;
+    w.table = (int*)ws;
+    w.ticket = (unsigned*)((char*)ws + align16((size_t)E * (size_t)tiles * sizeof(int)));
+    return w;
+}
+
+// ---------------------------------------------------------------- 1. rank
+__global__ void perm_rank_kernel(const void* __restrict__ ids, bool i16, int T, int K, int E, int TT,
+                                 int tiles, int* __restrict__ table, int* __restrict__ row_map,
+                                 unsigned* __restrict__ ticket) {
+    extern __shared__ int s_cnt[];  // [warps][E]
+    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    const int nwarps = blockDim.x >> 5;
+    int* cnt = s_cnt + (size_t)warp * E;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
+    const int tile = blockIdx.x * nwarps + warp;
+    if (tile >= tiles) return;
+    for (int e = lane; e < E; e += 32) cnt[e] = 0;
+    __syncwarp();
+    const long long i0 = (long long)tile * TT * K;
+    long long i1 = (long long)(tile + 1) * TT * K;
+    const long long nroutes = (long long)T * K;
+    if (i1 > nroutes) i1 = nroutes;
+    for (long long c = i0; c < i1; c += 32) {
+        long long i = c + lane;
+        int e = -1;
+        if (i < i1) {
+            e = load_id(ids, i, i16);
+            if (e < -1 || e >= E) {
+                raise_device_error(MOE_DEVERR_BAD_ID);
+                e = -1;
+            }
+        }
+        unsigned grp = __match_any_sync(FULL, e);
+        int leader = __ffs(grp) - 1;
+        int rk = __popc(grp & lanemask_lt());
+        int old = 0;
+        if (lane == leader && e >= 0) {
+            old = cnt[e];
+            cnt[e] = old + __popc(grp);
+        }
+        old = __shfl_sync(FULL, old, leader);
+        if (i < i1) row_map[i] = (e >= 0) ? old + rk : -1;
+        __syncwarp();
+    }
+    for (int e = lane; e < E; e += 32) table[(size_t)e * tiles + tile] = cnt[e];
+}
+
+// ---------------------------------------------------------------- 2. scan
+__global__ void __launch_bounds__(SCAN_THREADS) perm_scan_kernel(int E, int tiles, int* __restrict__ table,
+                                                                 int* __restrict__ group_sizes,
+                                                                 int* __restrict__ group_offsets,
+                                                                 unsigned* __restrict__ ticket) {
+    __shared__ int s_warp[SCAN_THREADS / 32];
+    __shared__ bool s_last;
+    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    const int nwarps = SCAN_THREADS / 32;
+    // (a) warp per expert: exclusive scan of its per-tile counts, in place
+    for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
+        int* row = table + (size_t)e * tiles;
+        int carry = 0;
+        for (int j0 = 0; j0 < tiles; j0 += 32) {
+            int j = j0 + lane;
+            int v = j < tiles ? row[j] : 0;
+            int inc = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                int o = __shfl_up_sync(FULL, inc, d);
+                if (lane >= d) inc += o;
+            }
+            if (j < tiles) row[j] = carry + inc - v;
+            carry += __shfl_sync(FULL, inc, 31);
+        }
+        if (lane == 0) group_sizes[e] = carry;
+    }
+    // (b) the last block to finish scans group_sizes -> group_offsets
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int per = (E + SCAN_THREADS - 1) / SCAN_THREADS;
+    const int b0 = threadIdx.x * per;
+    int local = 0;
+    for (int j = 0; j < per; j++)
+        if (b0 + j < E) local += __ldcg(group_sizes + b0 + j);
+    int inc = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int o = __shfl_up_sync(FULL, inc, d);
+        if (lane >= d) inc += o;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
+        int wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int o = __shfl_up_sync(FULL, wi, d);
+            if (lane >= d) wi += o;
+        }
+        s_warp[lane] = wi - w;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    int run = s_warp[warp] + inc - local;
+    for (int j = 0; j < per; j++) {
+        if (b0 + j < E) {
+            group_offsets[b0 + j] = run;
+            run += __ldcg(group_sizes + b0 + j);
+        }
+    }
+    if (threadIdx.x == SCAN_THREADS - 1) group_offsets[E] = s_warp[warp] + inc;
+}
+
+// ---------------------------------------------------------------- 3. scatter
+// Up to KC*32 routes per token (K <= 128).
+template <int KC, bool FUSE>
+__global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restrict__ x, int T, int H,
+                                                           const void* __restrict__ ids, bool i16, int K,
+                                                           int TT, int tiles, const int* __restrict__ table,
+                                                           const int* __restrict__ group_offsets,
+                                                           int* __restrict__ row_map, int* __restrict__ perm_src,
+                                                           void* __restrict__ x_perm,
+                                                           uint8_t* __restrict__ scales) {
+    const int lane = (int)lane_id();
+    const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    const int H8 = H >> 3;     // 16-byte chunks per row
+    const int iters = (H8 + 31) >> 5;
+    for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
+        const int tile = (int)(t / TT);
+        int rows[KC];
+        unsigned mask[KC];
+#pragma unroll
+        for (int c = 0; c < KC; c++) {
+            int k = c * 32 + lane;
+            int r = -1;
+            if (k < K) {
+                long long i = t * K + k;
+                int lr = row_map[i];
+                if (lr >= 0) {
+                    int e = load_id(ids, i, i16);
+                    r = group_offsets[e] + table[(size_t)e * tiles + tile] + lr;
+                    perm_src[r] = (int)t;
+                }
+                row_map[i] = r;
+            }
+            rows[c] = r;
+            mask[c] = __ballot_sync(FULL, r >= 0);
+        }
+        const uint4* src = x + t * H8;
+        for (int it = 0; it < iters; it++) {
+            const int j = it * 32 + lane;
+            const bool in = j < H8;
+            uint4 v = in ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+            if (!FUSE) {
+#pragma unroll
+                for (int c = 0; c < KC; c++) {
+                    unsigned m = mask[c];
+                    while (m) {
+                        int b = __ffs(m) - 1;
+                        m &= m - 1;
+                        int r = __shfl_sync(FULL, rows[c], b);
+                        if (in) reinterpret_cast<uint4*>(x_perm)[(long long)r * H8 + j] = v;
+                    }
+                }
+            } else {
+                float f[8];
+                bf16x8_to_f32(v, f);
+                int sb;
+                uint2 qv = quant8_in_quad(f, &sb);
+#pragma unroll
+                for (int c = 0; c < KC; c++) {
+                    unsigned m = mask[c];
+                    while (m) {
+                        int b = __ffs(m) - 1;
+                        m &= m - 1;
+                        int r = __shfl_sync(FULL, rows[c], b);
+                        if (in) {
+                            reinterpret_cast<uint2*>(x_perm)[(long long)r * H8 + j] = qv;
+                            if ((lane & 3) == 0) scales[(long long)r * (H >> 5) + (j >> 2)] = (uint8_t)sb;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- standalone quantiser
+// Row-wise: warp per row, rows < R only.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x, int R_cap, int H,
+                                                         const int* __restrict__ group_offsets, int E,
+                                                         uint2* __restrict__ q, uint8_t* __restrict__ scales) {
+    const int lane = (int)lane_id();
+    const int R = __ldg(group_offsets + E);
+    const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    const int H8 = H >> 3;
+    const int iters = (H8 + 31) >> 5;
+    for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R && r < R_cap;
+         r += nwarps_total) {
+        for (int it = 0; it < iters; it++) {
+            const int j = it * 32 + lane;
+            const bool in = j < H8;
+            uint4 v = in ? __ldg(x + r * H8 + j) : make_uint4(0, 0, 0, 0);
+            float f[8];
+            bf16x8_to_f32(v, f);
+            int sb;
+            uint2 qv = quant8_in_quad(f, &sb);
+            if (in) {
+                q[r * H8 + j] = qv;
+                if ((lane & 3) == 0) scales[r * (H >> 5) + (j >> 2)] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+// Column-wise, group-aware: block (srow, column chunk of 256). Scale row srow
+// belongs to the group e with e + off[e]/32 <= srow < (e+1) + off[e+1]/32;
+// its block index within the group is b = srow - e - off[e]/32.
+__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x, int H,
+                                                         const int* __restrict__ group_offsets, int E,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ scales) {
+    __shared__ int s_e;
+    const int srow = blockIdx.x;
+    if (threadIdx.x == 0) {
+        int lo = 0, hi = E - 1;  // last e with e + off[e]/32 <= srow
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (mid + __ldg(group_offsets + mid) / 32 <= srow) lo = mid;
+            else hi = mid - 1;
+        }
+        s_e = lo;
+    }
+    __syncthreads();
+    const int e = s_e;
+    const int off0 = __ldg(group_offsets + e), off1 = __ldg(group_offsets + e + 1);
+    const int b = srow - e - off0 / 32;
+    if (b < 0) return;
+    const int r0 = off0 + 32 * b;
+    if (r0 >= off1) return;
+    const int n = min(32, off1 - r0);
+    const int col = blockIdx.y * blockDim.x + threadIdx.x;
+    if (col >= H) return;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        v[i] = i < n ? __bfloat162float(x[(long long)(r0 + i) * H + col]) : 0.0f;
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const int sb = e8m0_scale_byte(amax);
+    const float inv = e8m0_inv_scale(sb);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        unsigned short two = f32x2_to_e4m3x2(v[i] * inv, v[i + 1] * inv);
+        if (i < n) q[(long long)(r0 + i) * H + col] = (uint8_t)(two & 0xff);
+        if (i + 1 < n) q[(long long)(r0 + i + 1) * H + col] = (uint8_t)(two >> 8);
+    }
+    scales[(long long)srow * H + col] = (uint8_t)sb;
+}
+
+int sm_count() {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+int rank_warps_per_block(int E) {
+    int w = (48 * 1024) / (E * 4);
+    return w < 1 ? 1 : (w > 8 ? 8 : w);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
+    using namespace moe;
+    if (T < 0 || K < 1 || E < 1) return 0;
+    const int TT = tile_tokens(E);
+    const long long tiles = ((long long)T + TT - 1) / TT;
+    return align16((size_t)E * (size_t)(tiles > 0 ? tiles : 1) * sizeof(int)) + 16;
+}
+
+extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
+                                  int E, void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes,
+                                  int32_t* group_offsets, int32_t* row_map, int32_t* perm_src,
+                                  unsigned flags, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 32 || (H % 32) != 0 || K < 1 || E < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
+    if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
+    if (flags & ~MOE_PERMUTE_FUSE_MXFP8) return MOE_ERR_INVALID_ARG;
+    const bool fuse = (flags & MOE_PERMUTE_FUSE_MXFP8) != 0;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !ids || !x_perm || !row_map || !perm_src)) return MOE_ERR_INVALID_ARG;
+    if (fuse && T > 0 && !x_perm_scales) return MOE_ERR_INVALID_ARG;
+    if ((long long)E * 4 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < moe_permute_workspace_size(T, K, E)) return MOE_ERR_WORKSPACE;
+    if (!moe_host::aligned(x, 16) || !moe_host::aligned(x_perm, fuse ? 8 : 16) ||
+        !moe_host::aligned(workspace, 16) || !moe_host::aligned(row_map, 4) || !moe_host::aligned(perm_src, 4) ||
+        !moe_host::aligned(group_sizes, 4) || !moe_host::aligned(group_offsets, 4))
+        return MOE_ERR_ALIGNMENT;
+    cudaStream_t s = moe_host::as_stream(stream);
+    const bool i16 = id_dtype == MOE_I16;
+    const int TT = tile_tokens(E);
+    const int tiles = T > 0 ? (T + TT - 1) / TT : 1;
+    PermuteWs w = carve(workspace, E, tiles);
+
+    if (T == 0) {  // empty batch: all groups empty
+        if (cudaMemsetAsync(group_sizes, 0, sizeof(int) * (size_t)E, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(group_offsets, 0, sizeof(int) * (size_t)(E + 1), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    // 1. rank
+    const int wpb = rank_warps_per_block(E);
+    const size_t smem = (size_t)wpb * E * sizeof(int);
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    perm_rank_kernel<<<(tiles + wpb - 1) / wpb, wpb * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
+                                                                      row_map, w.ticket);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    // 2. scan
+    const int experts_per_block = SCAN_THREADS / 32;
+    int sblocks = (E + experts_per_block - 1) / experts_per_block;
+    const int cap = sm_count();
+    if (sblocks > cap) sblocks = cap;
+    perm_scan_kernel<<<sblocks, SCAN_THREADS, 0, s>>>(E, tiles, w.table, group_sizes, group_offsets, w.ticket);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    // 3. scatter: warp per token
+    const long long warps_needed = T;
+    long long blocks = (warps_needed + 7) / 8;
+    const long long bcap = (long long)cap * 16;
+    if (blocks > bcap) blocks = bcap;
+    const int KC = (K + 31) / 32;
+#define MOE_SCATTER(kc, fz)                                                                              \
+    perm_scatter_kernel<kc, fz><<<(int)blocks, 256, 0, s>>>((const uint4*)x, T, H, ids, i16, K, TT, tiles, \
+                                                            w.table, group_offsets, row_map, perm_src,     \
+                                                            x_perm, x_perm_scales)
+    if (fuse) {
+        if (KC == 1) MOE_SCATTER(1, true);
+        else if (KC == 2) MOE_SCATTER(2, true);
+        else MOE_SCATTER(4, true);
+    } else {
+        if (KC == 1) MOE_SCATTER(1, false);
+        else if (KC == 2) MOE_SCATTER(2, false);
+        else MOE_SCATTER(4, false);
+    }
+#undef MOE_SCATTER
+    return moe_host::launch_status();
+}
+
+extern "C" moe_status moe_quant_mxfp8_grouped(const void* x, int R_cap, int H, const int32_t* group_offsets,
+                                              int E, uint8_t* q, uint8_t* scales, unsigned flags,
+                                              moe_stream_t stream) {
+    using namespace moe;
+    if (R_cap < 0 || H < 32 || (H % 32) != 0 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (flags & ~MOE_QUANT_COLWISE) return MOE_ERR_INVALID_ARG;
+    if (R_cap == 0) return MOE_OK;
+    if (!x || !group_offsets || !q || !scales) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned(x, 16) || !moe_host::aligned(q, 8) || !moe_host::aligned(group_offsets, 4))
+        return MOE_ERR_ALIGNMENT;
+    cudaStream_t s = moe_host::as_stream(stream);
+    if (flags & MOE_QUANT_COLWISE) {
+        const long long srows = (long long)E + R_cap / 32 + 1;
+        if (srows > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+        dim3 grid((unsigned)srows, (unsigned)((H + 255) / 256));
+        quant_cols_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, H, group_offsets, E, q, scales);
+    } else {
+        long long blocks = ((long long)R_cap + 7) / 8;
+        const long long bcap = (long long)sm_count() * 16;
+        if (blocks > bcap) blocks = bcap;
+        quant_rows_kernel<<<(int)blocks, 256, 0, s>>>((const uint4*)x, R_cap, H, group_offsets, E, (uint2*)q,
+                                                      scales);
+    }
+    return moe_host::launch_status();
+}

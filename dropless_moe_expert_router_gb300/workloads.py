@@ -127,3 +127,11 @@ def invalid_mask(wl: Workload, seed: int = 0) -> torch.Tensor:
 def dy_perm(wl: Workload, seed: int = 0) -> torch.Tensor:
     """Upstream gradient of the permuted expert outputs [T*K, H] bf16 ~ N(0, 0.02)."""
     return _normal((wl.R_cap, wl.H), wl.act_std, seed, _DY)
+
+
+_YPERM = 9
+
+
+def expert_out(wl: Workload, seed: int = 0) -> torch.Tensor:
+    """Synthetic expert outputs in permuted order [T*K, H] bf16 ~ N(0, 0.02) (to test combine alone)."""
+    return _normal((wl.R_cap, wl.H), wl.act_std, seed, _YPERM)

@@ -1,0 +1,185 @@
+/*
+ * moe_gb300.h -- C ABI of the single-GPU dropless Mixture-of-Experts layer
+ * hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The path: router top-K -> permute (dispatch into expert-contiguous order,
+ * optionally quantising to MXFP8 on the way) -> grouped SwiGLU expert MLP
+ * (two ragged grouped GEMMs, BF16 or MXFP8) -> probability-weighted
+ * unpermute/combine back to token order; plus the grouped backward GEMMs.
+ *
+ * Sources (cited by page title and section):
+ *   [SPARSER] "Sparser MoE end-to-end" (harryzhou2000 blog)
+ *   [TEJAX]   "Dropless MoE acceleration in JAX with NVIDIA Transformer Engine"
+ *             (news.bpdata.com)
+ *   [CLARITY] "NVIDIA's unoptimized DeepSeek-V3 baseline spends 84% of kernel
+ *             time moving tokens between GPUs" (theclarity.today)
+ *
+ * Conventions shared by every entry point:
+ *  - Ownership: the caller allocates every buffer (device memory unless stated)
+ *    and keeps it alive until the enqueued work has finished. The library never
+ *    allocates, never synchronises and never copies device->host in the calls
+ *    below, except moe_get_device_errors. Group sizes stay on the device
+ *    ([TEJAX] "Optimization 1: Grouped GEMM": shapes must not need the CPU, so
+ *    CUDA graphs stay usable); every call is safe to capture in a CUDA graph.
+ *  - Streams: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and nowhere else.
+ *  - Layouts are row-major. bf16 tensors are passed as raw 16-bit payloads.
+ *    Device pointers must be 16-byte aligned; operands of the grouped GEMMs
+ *    (x_perm, h, packed weights and their scales) must be 128-byte aligned.
+ *  - Capacity: permuted buffers have R_cap = T*K rows. Only the first
+ *    R = group_offsets[E] rows are written or read; the rest are unspecified.
+ *  - Errors: argument checks are synchronous and return a status without
+ *    enqueuing anything. A failed launch returns MOE_ERR_CUDA. Conditions found
+ *    on the device never trap: they set bits in a device error word that
+ *    moe_get_device_errors reads.
+ *  - T = 0 (no tokens) is legal and enqueues nothing.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad shape, null pointer or flag combination */
+    MOE_ERR_UNSUPPORTED = 2,   /* legal but not implemented (e.g. H % 128 != 0 for the GEMM) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or too small */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_ALIGNMENT = 5,     /* a pointer is not aligned as required */
+    MOE_ERR_DEVICE = 6         /* the device error word is non-zero (moe_get_device_errors) */
+} moe_status;
+
+typedef enum {
+    MOE_I16 = 0,   /* int16 expert ids (E <= 32767) */
+    MOE_I32 = 1,   /* int32 expert ids */
+    MOE_BF16 = 2,  /* bfloat16 operands */
+    MOE_MXFP8 = 3  /* E4M3 payloads with one E8M0 scale byte per 32 elements */
+} moe_dtype;
+
+/* flags */
+#define MOE_ROUTE_RENORM 1u        /* probs normalised over the K selected experts */
+#define MOE_PERMUTE_FUSE_MXFP8 2u  /* permute writes MXFP8 rows instead of bf16 rows */
+#define MOE_QUANT_COLWISE 4u       /* group-aware 32x1 blocks along rows (wgrad operands) */
+
+/* device error bits */
+#define MOE_DEVERR_BAD_ID 1u       /* an expert id outside [-1, E) was seen (treated as invalid) */
+#define MOE_DEVERR_TIMEOUT 2u      /* a bounded wait inside a kernel gave up */
+
+/* ------------------------------------------------------------------------
+ * Router top-K ([SPARSER] "Preserve a compact route": radix/threshold
+ * selection with bounded histogram passes for large E and K, a separate fast
+ * path for small top-k, and routes carried as a dense [T, K] id list rather
+ * than a [T, E] map; [TEJAX] "Optimization 2": router kernels assign tokens
+ * before dispatch).
+ *
+ * logits [T, E] fp32. For every row: the K experts with the largest logits,
+ * ties to the lower expert index (-0 and +0 are equal), written to ids[T, K]
+ * in that order (int16 or int32 per id_dtype); probs[T, K] fp32 is the softmax
+ * over all E logits taken at the selected expert, or, with MOE_ROUTE_RENORM,
+ * the softmax over the K selected logits. The router never emits -1.
+ * Requires 1 <= K <= E, K <= 128, E <= 4096 (E <= 32767 for int16 ids), no NaN
+ * logits (NaN rows give unspecified ids). Small E (<= 256) and K (<= 16) use a
+ * warp-per-row arg-max path; the rest use the radix-select path.
+ * ------------------------------------------------------------------------ */
+moe_status moe_route_topk(const float *logits, int T, int E, int K,
+                          void *ids, moe_dtype id_dtype, float *probs,
+                          unsigned flags, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Permute / dispatch ([TEJAX] "Dropless vs capacity-based MoE": every routed
+ * token is processed, nothing dropped or padded; MoE-layer figure: tokens are
+ * grouped per expert and combine restores token order; [SPARSER] "Remove work
+ * that has no selected route": local processing visits only the selected
+ * slots, found by a warp ballot; invalid routes (-1) are preserved).
+ *
+ * A device-side counting sort of the T*K routes by expert:
+ *   group_sizes[E]      number of valid routes per expert (int32)
+ *   group_offsets[E+1]  exclusive scan of group_sizes; group_offsets[E] = R
+ *   row_map[T, K]       destination row of route (t, k), -1 if invalid (int32)
+ *   perm_src[R_cap]     source token of each destination row (int32; rows >= R untouched)
+ *   x_perm[R_cap, H]    x_perm[row_map[t,k]] = x[t] bit for bit (bf16), or with
+ *                       MOE_PERMUTE_FUSE_MXFP8: E4M3 payload bytes, with
+ *   x_perm_scales[R_cap, H/32]  the row-wise 1x32 E8M0 scale bytes (else NULL).
+ * Route (t, k) is valid iff 0 <= ids[t,k] < E; ids outside [-1, E) also set
+ * MOE_DEVERR_BAD_ID. Within an expert, rows are in ascending t*K + k order
+ * (deterministic; no dependence on atomic ordering). The MXFP8 rule: per 32
+ * consecutive elements, scale byte = clamp(floor(log2(amax)) - 8 + 127, 0, 254)
+ * (127 for an all-zero block), payload = E4M3(x / 2^(byte-127)) rounded to
+ * nearest even and saturated to +-448.
+ * Requires H % 32 == 0, 1 <= K <= E, and a workspace of
+ * moe_permute_workspace_size(T, K, E) bytes (16-byte aligned; its contents
+ * need not be initialised and are overwritten).
+ * ------------------------------------------------------------------------ */
+size_t moe_permute_workspace_size(int T, int K, int E);
+
+moe_status moe_permute(const void *x, int T, int H,
+                       const void *ids, moe_dtype id_dtype, int K, int E,
+                       void *x_perm, uint8_t *x_perm_scales,
+                       int32_t *group_sizes, int32_t *group_offsets,
+                       int32_t *row_map, int32_t *perm_src,
+                       unsigned flags, void *workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Group-aware MXFP8 quantisation ([TEJAX] "Transformer Engine building
+ * blocks": group-aware MXFP8 quantization feeding the MXFP8 grouped GEMM).
+ *
+ * x [R_cap, H] bf16, rows [group_offsets[e], group_offsets[e+1]) forming
+ * group e; only rows < group_offsets[E] are read or written.
+ *  - default (row-wise 1x32): q[R_cap, H] E4M3, scales[R_cap, H/32].
+ *  - MOE_QUANT_COLWISE (32x1 along rows, for the weight-gradient GEMMs whose
+ *    contraction runs over a group's rows): blocks start at each group's first
+ *    row and never cross a group; a partial last block takes its amax over its
+ *    valid rows. q[R_cap, H]; scales[E + R_cap/32 + 1, H] where block b of
+ *    group e is scale row e + group_offsets[e]/32 + b (rows no block uses are
+ *    left untouched).
+ * Same scale/payload rule as moe_permute. Requires H % 32 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_quant_mxfp8_grouped(const void *x, int R_cap, int H,
+                                   const int32_t *group_offsets, int E,
+                                   uint8_t *q, uint8_t *scales,
+                                   unsigned flags, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Unpermute / combine ([TEJAX] "Optimization 2": results are routed back and
+ * accumulated; [SPARSER] "Remove work that has no selected route": combine is a
+ * pull-and-reduce over each token's selected rows).
+ *
+ * y[t, :] = bf16( sum over k = 0..K-1 with row_map[t,k] >= 0 of
+ *                 probs[t,k] * y_perm[row_map[t,k], :] )
+ * accumulated in fp32 in ascending k; a token with no valid route gets zeros.
+ * y_perm [R_cap, H] bf16, row_map [T, K] int32, probs [T, K] fp32, y [T, H] bf16.
+ * Requires H % 8 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_unpermute_combine(const void *y_perm, const int32_t *row_map,
+                                 const float *probs, int T, int K, int H,
+                                 void *y, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device error word. Copies the word to *flags_out (synchronising the device)
+ * and clears it when `clear` is non-zero. Not for the hot path. Returns
+ * MOE_ERR_DEVICE when the word was non-zero.
+ * ------------------------------------------------------------------------ */
+moe_status moe_get_device_errors(uint32_t *flags_out, int clear);
+
+/* Human-readable name of a status code (static storage). */
+const char *moe_status_string(moe_status status);
+
+/* Byte sizes of the compact route ([SPARSER] "Preserve a compact route":
+ * [T, K] ids instead of a [T, E] map): ids of the given dtype, and fp32 probs. */
+size_t moe_route_ids_bytes(int T, int K, moe_dtype id_dtype);
+size_t moe_route_probs_bytes(int T, int K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,85 @@
+"""The C-ABI library loads and exports every entry point include/*.h declares;
+host-side helpers (no GPU needed)."""
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dropless_moe_expert_router_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_hot_path():
+    names = _declared_functions()
+    for required in ("moe_route_topk", "moe_permute", "moe_quant_mxfp8_grouped",
+                     "moe_unpermute_combine", "moe_get_device_errors"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from dropless_moe_expert_router_gb300 import _lib
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(1) == b"MOE_ERR_INVALID_ARG"
+    assert lib.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+def test_argument_errors_need_no_gpu(lib):
+    # bad shapes are rejected synchronously, before any CUDA call
+    assert lib.moe_route_topk(None, 4, 8, 9, None, 1, None, 0, None) == 1   # K > E
+    assert lib.moe_route_topk(None, 4, 40000, 2, None, 0, None, 0, None) == 1  # int16 ids, E too big
+    assert lib.moe_route_topk(None, 0, 8, 2, None, 1, None, 0, None) == 0   # T = 0 is a no-op
+    assert lib.moe_permute(None, 4, 30, None, 1, 2, 8, None, None, None, None, None, None,
+                           0, None, 0, None) == 1                            # H % 32 != 0
+    assert lib.moe_unpermute_combine(None, None, None, 4, 2, 12, None, None) == 1  # H % 8 != 0
+    assert lib.moe_quant_mxfp8_grouped(None, 4, 64, None, 2, None, None, 8, None) == 1  # bad flag
+
+
+def test_workspace_size_covers_the_tile_table(lib):
+    # one int32 per (expert, token tile) plus a 16-byte counter
+    assert lib.moe_permute_workspace_size(8192, 2, 8) >= 8 * (8192 // 128) * 4 + 16
+    assert lib.moe_permute_workspace_size(8192, 36, 2304) >= 2304 * (8192 // 32) * 4 + 16
+    assert lib.moe_permute_workspace_size(-1, 2, 8) == 0
+
+
+def test_compact_route_sizes_match_page(lib):
+    """Page values ("Sparser MoE end-to-end", "Preserve a compact route" and
+    "Remove work that has no selected route"): 18.87 MB -> 0.59 MB (32x), and a
+    9,216-byte FP32 prob row vs a 128-byte 32-expert slice."""
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "route_metadata_sizes.txt")):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = line.split("=")
+            vals[k.strip()] = float(v)
+    T, E, K = int(vals["T"]), int(vals["E"]), int(vals["K"])
+    ids_bytes = lib.moe_route_ids_bytes(T, K, 0)
+    assert round(ids_bytes / 1e6, 2) == vals["int16_ids_MB"]
+    assert round(T * E / 1e6, 2) == vals["bool_map_MB"]
+    assert (T * E) // ids_bytes == vals["ratio"]
+    assert lib.moe_route_probs_bytes(1, E) == vals["prob_row_bytes"]
+    assert lib.moe_route_probs_bytes(1, int(vals["local_experts"])) == vals["prob_slice_bytes"]
