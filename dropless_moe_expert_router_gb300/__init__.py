@@ -8,4 +8,5 @@ workloads (``workloads``).
 """
 from .api import (MoeError, Permuted, moe_get_device_errors, moe_permute,  # noqa: F401
                   moe_permute_workspace_size, moe_quant_mxfp8_grouped, moe_route_ids_bytes,
-                  moe_route_probs_bytes, moe_route_topk, moe_unpermute_combine, permute_buffers)
+                  moe_route_probs_bytes, moe_route_topk, moe_unpermute_combine, permute_buffers,
+                  PackedWeights, moe_prepare_weights, moe_grouped_swiglu_gemm)

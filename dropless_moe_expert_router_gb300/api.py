@@ -188,3 +188,66 @@ def moe_route_ids_bytes(T: int, K: int, id_dtype=torch.int16) -> int:
 
 def moe_route_probs_bytes(T: int, K: int) -> int:
     return int(_lib.load().moe_route_probs_bytes(T, K))
+
+
+# ------------------------------------------------------------- expert GEMMs
+def _dt_code(precision: str) -> int:
+    if precision == "bf16":
+        return MOE_BF16
+    if precision == "mxfp8":
+        return MOE_MXFP8
+    raise ValueError("precision must be 'bf16' or 'mxfp8'")
+
+
+class PackedWeights(NamedTuple):
+    precision: str
+    E: int
+    H: int
+    F: int
+    w13: torch.Tensor                 # [E, 2F, H] bf16 or uint8 (E4M3)
+    w13_scales: Optional[torch.Tensor]  # [E, 2F, H/32] uint8 (MXFP8)
+    w2: torch.Tensor                  # [E, H, F] bf16 or uint8
+    w2_scales: Optional[torch.Tensor]   # [E, H, F/32] uint8 (MXFP8)
+
+
+def moe_prepare_weights(w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, precision: str = "bf16",
+                        stream=None) -> PackedWeights:
+    """Pack logical W1, W3 [E, H, F] and W2 [E, F, H] (bf16) for the grouped GEMMs (one-time)."""
+    for t, n in ((w1, "w1"), (w3, "w3"), (w2, "w2")):
+        _want(t, n, torch.bfloat16, 3)
+    E, H, F = w1.shape
+    dev = w1.device
+    fp8 = precision == "mxfp8"
+    pdt = torch.uint8 if fp8 else torch.bfloat16
+    w13 = torch.empty((E, 2 * F, H), dtype=pdt, device=dev)
+    w2p = torch.empty((E, H, F), dtype=pdt, device=dev)
+    s13 = torch.empty((E, 2 * F, H // 32), dtype=torch.uint8, device=dev) if fp8 else None
+    s2 = torch.empty((E, H, F // 32), dtype=torch.uint8, device=dev) if fp8 else None
+    st = _lib.load().moe_prepare_weights(_ptr(w1), _ptr(w3), _ptr(w2), E, H, F, _dt_code(precision),
+                                         _ptr(w13), _ptr(s13), _ptr(w2p), _ptr(s2), _stream(stream))
+    _check("moe_prepare_weights", st)
+    return PackedWeights(precision, E, H, F, w13, s13, w2p, s2)
+
+
+def moe_grouped_swiglu_gemm(x_perm: torch.Tensor, x_scales: Optional[torch.Tensor], w: PackedWeights,
+                            group_offsets: torch.Tensor, *, h: Optional[torch.Tensor] = None,
+                            h_scales: Optional[torch.Tensor] = None, y_perm: Optional[torch.Tensor] = None,
+                            stream=None):
+    """Grouped SwiGLU MLP on permuted rows -> (y_perm [R_cap, H] bf16, h, h_scales)."""
+    fp8 = w.precision == "mxfp8"
+    _want(x_perm, "x_perm", torch.uint8 if fp8 else torch.bfloat16, 2)
+    _want(group_offsets, "group_offsets", torch.int32, 1)
+    R_cap = x_perm.shape[0]
+    dev = x_perm.device
+    if h is None:
+        h = torch.empty((R_cap, w.F), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    if fp8 and h_scales is None:
+        h_scales = torch.empty((R_cap, w.F // 32), dtype=torch.uint8, device=dev)
+    if y_perm is None:
+        y_perm = torch.empty((R_cap, w.H), dtype=torch.bfloat16, device=dev)
+    st = _lib.load().moe_grouped_swiglu_gemm(
+        _ptr(x_perm), _ptr(x_scales), _ptr(w.w13), _ptr(w.w13_scales), _ptr(w.w2), _ptr(w.w2_scales),
+        _dt_code(w.precision), _ptr(group_offsets), w.E, w.H, w.F, R_cap, _ptr(h), _ptr(h_scales),
+        _ptr(y_perm), _stream(stream))
+    _check("moe_grouped_swiglu_gemm", st)
+    return y_perm, h, h_scales

@@ -149,6 +149,56 @@ moe_status moe_quant_mxfp8_grouped(const void *x, int R_cap, int H,
                                    unsigned flags, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped SwiGLU expert MLP ([TEJAX] "Optimization 1: Grouped GEMM": one
+ * kernel covers all experts, each with its actual token count, computing only
+ * valid regions, with the counts kept on the device; MoE-layer figure: the
+ * grouped MLP is two grouped GEMMs on variable-length groups; "Transformer
+ * Engine building blocks": MXFP8 grouped GEMM on Blackwell).
+ *
+ * For each expert e and each row r in [group_offsets[e], group_offsets[e+1]):
+ *   a = x_perm[r] W1[e],  b = x_perm[r] W3[e]       (fp32 accumulation)
+ *   h[r] = silu(a) * b    rounded to bf16, or (MXFP8) quantised 1x32 along F
+ *   y_perm[r] = h[r] W2[e]  rounded to bf16
+ * Rows >= group_offsets[E] are never written. Logical weights: W1, W3 [E, H, F]
+ * and W2 [E, F, H] bf16; the GEMMs read them packed once by
+ * moe_prepare_weights (outside the hot path):
+ *   w13_packed [E][2F][H]: per 256-row tile j, rows 0..127 = columns
+ *              128j..128j+127 of W1 transposed, rows 128..255 the same of W3;
+ *   w2_packed  [E][H][F] = W2 transposed per expert;
+ * bf16, or MXFP8 (E4M3 bytes, plus E8M0 scales [E][2F][H/32] and [E][H][F/32]
+ * with blocks of 32 along the contraction dimension).
+ * Activations: x_perm [R_cap, H] bf16, or MXFP8 E4M3 with x_scales
+ * [R_cap, H/32] (as written by moe_permute with MOE_PERMUTE_FUSE_MXFP8);
+ * h [R_cap, F] (caller-allocated intermediate, kept for the backward pass)
+ * bf16, or E4M3 with h_scales [R_cap, F/32]; y_perm [R_cap, H] bf16.
+ * Requires H % 256 == 0 and F % 128 == 0, x_perm, h and the packed weights
+ * 128-byte aligned, E small enough for the group table to fit in shared
+ * memory (E <= 4096). moe_grouped_gemm_up / _down run the two halves alone.
+ * ------------------------------------------------------------------------ */
+size_t moe_packed_weights_bytes(int E, int H, int F, moe_dtype dtype, int which);
+/* which: 0 = w13 payload, 1 = w13 scales, 2 = w2 payload, 3 = w2 scales (0 bytes for bf16) */
+
+moe_status moe_prepare_weights(const void *w1, const void *w3, const void *w2, int E, int H, int F,
+                               moe_dtype dtype, void *w13_packed, uint8_t *w13_scales,
+                               void *w2_packed, uint8_t *w2_scales, moe_stream_t stream);
+
+moe_status moe_grouped_swiglu_gemm(const void *x_perm, const uint8_t *x_scales,
+                                   const void *w13_packed, const uint8_t *w13_scales,
+                                   const void *w2_packed, const uint8_t *w2_scales, moe_dtype dtype,
+                                   const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                                   void *h, uint8_t *h_scales, void *y_perm, moe_stream_t stream);
+
+moe_status moe_grouped_gemm_up(const void *x_perm, const uint8_t *x_scales, const void *w13_packed,
+                               const uint8_t *w13_scales, moe_dtype dtype,
+                               const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                               void *h, uint8_t *h_scales, moe_stream_t stream);
+
+moe_status moe_grouped_gemm_down(const void *h, const uint8_t *h_scales, const void *w2_packed,
+                                 const uint8_t *w2_scales, moe_dtype dtype,
+                                 const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                                 void *y_perm, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Unpermute / combine ([TEJAX] "Optimization 2": results are routed back and
  * accumulated; [SPARSER] "Remove work that has no selected route": combine is a
  * pull-and-reduce over each token's selected rows).
