@@ -65,6 +65,10 @@ WORKLOADS = {
                         invalid_frac=0.02),
     "heavy": Workload("heavy", T=32768, H=7168, E=32, K=8, F=2048, precision="mxfp8",
                       bias="zipf", bias_scale=1.0, zipf_s=1.5, backward=True),
+    # reduced Mixtral-like shape for profiler captures (same tile shapes and K loop,
+    # a quarter of F and half of T: about 1.5 GB on the device)
+    "mixtral_prof": Workload("mixtral_prof", T=4096, H=4096, E=8, K=2, F=3584, bias="normal",
+                             bias_scale=0.5, renorm=True),
 }
 
 
