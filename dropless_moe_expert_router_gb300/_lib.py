@@ -21,6 +21,8 @@ SIGNATURES = {
     "moe_route_topk": (I, [P, I, I, I, P, I, P, U, P]),
     "moe_permute_workspace_size": (SZ, [I, I, I]),
     "moe_permute": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, U, P, SZ, P]),
+    "moe_permute_noalloc_max_scratch": (SZ, []),
+    "moe_permute_noalloc": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, U, P]),
     "moe_quant_mxfp8_grouped": (I, [P, I, I, P, I, P, P, U, P]),
     "moe_unpermute_combine": (I, [P, P, P, I, I, I, P, P]),
     "moe_packed_weights_bytes": (SZ, [I, I, I, I, I]),

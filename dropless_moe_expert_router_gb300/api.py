@@ -131,6 +131,28 @@ def moe_permute(x: torch.Tensor, ids: torch.Tensor, E: int, *, fuse_mxfp8: bool 
     return out
 
 
+def moe_permute_noalloc(x: torch.Tensor, ids: torch.Tensor, E: int, *, fuse_mxfp8: bool = False,
+                        out: Optional[Permuted] = None, stream=None) -> Permuted:
+    """moe_permute for callers that may not allocate device memory: the library's
+    static scratch array replaces the workspace (outputs are still the caller's)."""
+    _want(x, "x", torch.bfloat16, 2)
+    _want(ids, "ids", None, 2)
+    T, H = x.shape
+    K = ids.shape[1]
+    if out is None:
+        out = permute_buffers(T, H, K, E, x.device, fuse_mxfp8)
+    st = _lib.load().moe_permute_noalloc(
+        _ptr(x), T, H, _ptr(ids), _id_code(ids.dtype), K, E, _ptr(out.x_perm), _ptr(out.x_perm_scales),
+        _ptr(out.group_sizes), _ptr(out.group_offsets), _ptr(out.row_map), _ptr(out.perm_src),
+        MOE_PERMUTE_FUSE_MXFP8 if fuse_mxfp8 else 0, _stream(stream))
+    _check("moe_permute_noalloc", st)
+    return out
+
+
+def moe_permute_noalloc_max_scratch() -> int:
+    return int(_lib.load().moe_permute_noalloc_max_scratch())
+
+
 # ---------------------------------------------------------------- quantiser
 def colwise_scale_rows(R_cap: int, E: int) -> int:
     return E + R_cap // 32 + 1

@@ -423,3 +423,59 @@ extern "C" moe_status moe_quant_mxfp8_grouped(const void* x, int R_cap, int H, c
     }
     return moe_host::launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// moe_permute_noalloc: moe_permute for callers that may not allocate device
+// memory. Its scratch (the per-expert, per-token-tile count table and the scan's
+// completion counter) lives in this file-scope array instead of a caller
+// workspace. Every GPU that loads the library holds the array until the process
+// exits; all calls on a device share it.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)4 << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_permute_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of g_permute_scratch on the current device. Host code cannot use
+// the array's name as a device address; the runtime resolves it once per device.
+moe_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_permute_noalloc_max_scratch(void) { return moe::NOALLOC_SCRATCH_BYTES; }
+
+extern "C" moe_status moe_permute_noalloc(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
+                                          int E, void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes,
+                                          int32_t* group_offsets, int32_t* row_map, int32_t* perm_src,
+                                          unsigned flags, moe_stream_t stream) {
+    const size_t need = moe_permute_workspace_size(T, K, E);
+    if (need == 0) return MOE_ERR_INVALID_ARG;
+    if (need > moe::NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    moe_status st = moe::noalloc_scratch(&scratch);
+    if (st != MOE_OK) return st;
+    // The scratch needs no clearing: the rank kernel writes every table entry it
+    // later reads and resets the completion counter before the scan kernel runs.
+    return moe_permute(x, T, H, ids, id_dtype, K, E, x_perm, x_perm_scales, group_sizes, group_offsets, row_map,
+                       perm_src, flags, scratch, moe::NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -129,6 +129,38 @@ moe_status moe_permute(const void *x, int T, int H,
                        moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_noalloc: moe_permute without a caller workspace. (The pages
+ * describe nothing like it; it exists for callers of this library.)
+ *
+ * Some callers cannot allocate device memory: a serving process that reserves
+ * all of its GPU memory at start-up and forbids any later cudaMalloc, a plug-in
+ * whose host application owns the CUDA allocator and offers C code no hook
+ * into it, or code that must not risk the implicit device synchronisation
+ * cudaMalloc / cudaFree may perform. This entry point takes the same arguments
+ * as moe_permute minus the workspace and allocates nothing: its scratch is a
+ * static device array of moe_permute_noalloc_max_scratch() bytes (4 MiB),
+ * held by every GPU that loads the library until the process exits.
+ *  - It returns MOE_ERR_WORKSPACE, without enqueuing anything, when
+ *    moe_permute_workspace_size(T, K, E) exceeds that maximum.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, once per device, with that device current); make
+ *    that first call before any stream capture.
+ *  - All calls on a device share the one array, and it keeps the last call's
+ *    contents (nothing in it needs to start at zero: each call rewrites what it
+ *    reads). Calls that overlap on the GPU (other streams, or other host threads
+ *    on the same device) race on it: serialise them.
+ * Outputs, requirements and errors are otherwise those of moe_permute.
+ * ------------------------------------------------------------------------ */
+size_t moe_permute_noalloc_max_scratch(void);
+
+moe_status moe_permute_noalloc(const void *x, int T, int H,
+                               const void *ids, moe_dtype id_dtype, int K, int E,
+                               void *x_perm, uint8_t *x_perm_scales,
+                               int32_t *group_sizes, int32_t *group_offsets,
+                               int32_t *row_map, int32_t *perm_src,
+                               unsigned flags, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Group-aware MXFP8 quantisation ([TEJAX] "Transformer Engine building
  * blocks": group-aware MXFP8 quantization feeding the MXFP8 grouped GEMM).
  *
