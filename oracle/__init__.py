@@ -73,7 +73,7 @@ def lib():
                                              i64, P, i64, i32, P, P, P, P, P, P, P, P]
             L.oracle_swiglu_dgrad_rows.restype = None
             L.oracle_swiglu_dgrad_rows.argtypes = [i32, P, P, i32, P, P, i32, i32, P, P, P, P, P,
-                                                   P, P, i32, i32, i32, i64, P, i64, P, P, P, P]
+                                                   P, P, i32, i32, i32, i64, P, i64, i32, P, P, P, P]
             L.oracle_wgrad_expert.restype = None
             L.oracle_wgrad_expert.argtypes = [i32, P, P, i64, i32, P, P, i64, P, i32, i32, i64,
                                               P, i64, P]
@@ -230,8 +230,11 @@ def swiglu_rows(x: Operand, w1: Operand, w3: Operand, w2: Operand, group_offsets
     return {k: v for k, v in outs.items() if v is not None}
 
 
+DAB_NONE, DAB_BF16, DAB_MXFP8 = 0, 1, 2
+
+
 def swiglu_dgrad_rows(dy: Operand, a: Operand, b: Operand, w1: Operand, w3: Operand,
-                      w2: Operand, group_offsets, rows, w_blk_rows=0,
+                      w2: Operand, group_offsets, rows, w_blk_rows=0, dab_mode=DAB_NONE,
                       want=("dx_bf16",)):
     off = _c(group_offsets, np.int32)
     E = off.size - 1
@@ -249,7 +252,7 @@ def swiglu_dgrad_rows(dy: Operand, a: Operand, b: Operand, w1: Operand, w3: Oper
     lib().oracle_swiglu_dgrad_rows(
         dy.kind, _p(dy.v), _p(dy.s), a.kind, _p(a.v), _p(b.v), w1.kind, int(w_blk_rows),
         _p(w1.v), _p(w1.s), _p(w3.v), _p(w3.s), _p(w2.v), _p(w2.s), _p(off), E, H, F, R_cap,
-        _p(rw), n, _p(outs["dx_bf16"]), _p(outs["dx_f64"]), _p(outs["da_f64"]),
+        _p(rw), n, int(dab_mode), _p(outs["dx_bf16"]), _p(outs["dx_f64"]), _p(outs["da_f64"]),
         _p(outs["db_f64"]))
     return {k: v for k, v in outs.items() if v is not None}
 

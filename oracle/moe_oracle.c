@@ -537,7 +537,12 @@ void oracle_swiglu_rows(int x_kind, const void *x_v, const uint8_t *x_s,
  * stored [H,F] / [F,H] matrices the 32-blocks run (the backward contracts
  * W2 over its columns and W1, W3 over their columns, so a caller quantising for
  * the backward passes column blocks, w_blk_rows = 0).
- * Outputs per listed row (each optional): dx_bf16 / dx_f64 [H], da_f64 / db_f64 [F].
+ * dab_mode says how da, db are rounded before the second product (the dx GEMM
+ * reads them as an operand): 0 = not at all, 1 = to bf16, 2 = to bf16 and then
+ * MXFP8 1x32 along F (blocks never mix da and db). Reading taken: the backward
+ * stores da, db as a bf16 operand (and quantises that operand for MXFP8).
+ * Outputs per listed row (each optional): dx_bf16 / dx_f64 [H], da_f64 / db_f64 [F]
+ * (unrounded).
  */
 void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s,
                               int ab_kind, const void *a_v, const void *b_v,
@@ -546,7 +551,7 @@ void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s
                               const void *w3_v, const uint8_t *w3_s,
                               const void *w2_v, const uint8_t *w2_s,
                               const int32_t *group_offsets, int E, int H, int F, long R_cap,
-                              const int32_t *rows, long nrows,
+                              const int32_t *rows, long nrows, int dab_mode,
                               uint16_t *dx_bf16, double *dx_f64, double *da_f64, double *db_f64)
 {
     mat DY = {dy_kind, dy_v, dy_s, R_cap, H, 0};
@@ -579,6 +584,26 @@ void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s
             da[f] = dh[f] * b[f] * (sg * (1.0 + a[f] * (1.0 - sg)));
             db[f] = dh[f] * silu(a[f]);
         }
+        if (da_f64)
+            memcpy(da_f64 + i * F, da, sizeof(double) * F);
+        if (db_f64)
+            memcpy(db_f64 + i * F, db, sizeof(double) * F);
+        if (dab_mode >= 1) {
+            for (int f = 0; f < F; f++) {
+                da[f] = oracle_bf16_to_double(oracle_double_to_bf16(da[f]));
+                db[f] = oracle_bf16_to_double(oracle_double_to_bf16(db[f]));
+            }
+        }
+        if (dab_mode == 2) {
+            double *v[2] = {da, db};
+            for (int w = 0; w < 2; w++)
+                for (int blk = 0; blk < F / 32; blk++) {
+                    uint8_t q[32];
+                    int sb = quant_block(v[w] + 32 * blk, 1, 32, q, 1);
+                    for (int j = 0; j < 32; j++)
+                        v[w][32 * blk + j] = mx_value(q[j], (uint8_t)sb);
+                }
+        }
         for (int h = 0; h < H; h++) {
             mat_row(&w1, h, wr);
             mat_row(&w3, h, wr3);
@@ -593,10 +618,6 @@ void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s
             if (dx_f64)
                 dx_f64[i * H + h] = dx[h];
         }
-        if (da_f64)
-            memcpy(da_f64 + i * F, da, sizeof(double) * F);
-        if (db_f64)
-            memcpy(db_f64 + i * F, db, sizeof(double) * F);
     }
     free(dyr); free(a); free(b); free(dh); free(da); free(db); free(dx);
     free(wr); free(wr3);

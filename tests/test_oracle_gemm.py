@@ -246,3 +246,41 @@ def test_wgrad_mxfp8_colwise_operands_decode_like_torch():
         assert np.allclose(got, ad.T @ bd, rtol=1e-12, atol=1e-12)
         # and the decoded operands approximate the bf16 ones
         assert np.allclose(ad, _f(a[r0:r1]), rtol=2 ** -3, atol=1e-3)   # saturation: <= 1/8
+
+
+def test_dgrad_dab_rounding_modes_follow_their_operands():
+    """dab_mode 1 / 2: dx equals the plain product of the bf16 (then MXFP8) da, db with
+    W1, W3, computed here with numpy on operands rounded by torch."""
+    E, H, F = 2, 32, 64
+    rng = np.random.default_rng(8)
+    off = np.array([0, 3, 7], np.int32)
+    W = lambda a: O.Operand(O.MAT_F64, a)
+    x = rng.standard_normal((7, H))
+    w1, w3 = rng.standard_normal((E, H, F)) * 0.2, rng.standard_normal((E, H, F)) * 0.2
+    w2 = rng.standard_normal((E, F, H)) * 0.2
+    dy = rng.standard_normal((7, H))
+    rows = np.arange(7, dtype=np.int32)
+    fw = O.swiglu_rows(W(x), W(w1), W(w3), W(w2), off, rows, h_mode=O.H_NONE, want=("a_f64", "b_f64"))
+    base = O.swiglu_dgrad_rows(W(dy), W(fw["a_f64"]), W(fw["b_f64"]), W(w1), W(w3), W(w2), off, rows,
+                               want=("dx_f64", "da_f64", "db_f64"))
+    tb = lambda a: torch.from_numpy(a).to(torch.float32).to(torch.bfloat16).double().numpy()
+
+    def mx(a):
+        out = np.empty_like(a)
+        for r in range(a.shape[0]):
+            for blk in range(a.shape[1] // 32):
+                v = a[r, 32 * blk:32 * blk + 32]
+                amax = np.abs(v).max()
+                e = O.e8m0_scale_byte(amax) - 127
+                q = torch.from_numpy(np.clip(v / 2.0 ** e, -448, 448)).to(torch.float32).to(
+                    torch.float8_e4m3fn).double().numpy()
+                out[r, 32 * blk:32 * blk + 32] = q * 2.0 ** e
+        return out
+    for mode, rnd in ((O.DAB_BF16, tb), (O.DAB_MXFP8, lambda a: mx(tb(a)))):
+        got = O.swiglu_dgrad_rows(W(dy), W(fw["a_f64"]), W(fw["b_f64"]), W(w1), W(w3), W(w2), off,
+                                  rows, dab_mode=mode, want=("dx_f64", "da_f64"))
+        assert np.array_equal(got["da_f64"], base["da_f64"])      # unrounded outputs unchanged
+        da, db = rnd(base["da_f64"]), rnd(base["db_f64"])
+        want = np.concatenate([da[off[e]:off[e + 1]] @ w1[e].T + db[off[e]:off[e + 1]] @ w3[e].T
+                               for e in range(E)])
+        assert np.allclose(got["dx_f64"], want, rtol=1e-12, atol=1e-12)
