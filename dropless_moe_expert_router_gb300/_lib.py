@@ -28,8 +28,14 @@ SIGNATURES = {
     "moe_packed_weights_bytes": (SZ, [I, I, I, I, I]),
     "moe_prepare_weights": (I, [P, P, P, I, I, I, I, P, P, P, P, P]),
     "moe_grouped_swiglu_gemm": (I, [P, P, P, P, P, P, I, P, I, I, I, I, P, P, P, P]),
-    "moe_grouped_gemm_up": (I, [P, P, P, P, I, P, I, I, I, I, P, P, P]),
+    "moe_grouped_gemm_up": (I, [P, P, P, P, I, P, I, I, I, I, P, P, P, P, P]),
     "moe_grouped_gemm_down": (I, [P, P, P, P, I, P, I, I, I, I, P, P]),
+    "moe_prepare_weights_bwd": (I, [P, P, P, I, I, I, I, P, P, P, P, P]),
+    "moe_grouped_swiglu_dgrad": (I, [P, P, P, P, P, I, P, I, I, I, I, P, P]),
+    "moe_grouped_gemm_dx": (I, [P, P, P, P, I, P, I, I, I, I, P, P]),
+    "moe_grouped_transpose_kpad": (SZ, [I, I]),
+    "moe_grouped_transpose": (I, [P, P, I, I, P, I, I, P, P, P]),
+    "moe_grouped_gemm_wgrad": (I, [P, P, P, P, I, P, I, I, I, I, P, P, P]),
     "moe_get_device_errors": (I, [C.POINTER(C.c_uint32), I]),
     "moe_status_string": (C.c_char_p, [I]),
     "moe_route_ids_bytes": (SZ, [I, I, I]),

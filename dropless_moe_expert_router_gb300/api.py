@@ -273,3 +273,129 @@ def moe_grouped_swiglu_gemm(x_perm: torch.Tensor, x_scales: Optional[torch.Tenso
         _ptr(y_perm), _stream(stream))
     _check("moe_grouped_swiglu_gemm", st)
     return y_perm, h, h_scales
+
+
+def moe_grouped_gemm_up(x_perm: torch.Tensor, x_scales: Optional[torch.Tensor], w: PackedWeights,
+                        group_offsets: torch.Tensor, *, h: Optional[torch.Tensor] = None,
+                        h_scales: Optional[torch.Tensor] = None, ab: Optional[torch.Tensor] = None,
+                        h_bf16: Optional[torch.Tensor] = None, stream=None):
+    """Up projection + SwiGLU; optionally saves ab [R_cap, 2F] bf16 and (MXFP8) h_bf16 [R_cap, F]."""
+    fp8 = w.precision == "mxfp8"
+    R_cap = x_perm.shape[0]
+    dev = x_perm.device
+    if h is None:
+        h = torch.empty((R_cap, w.F), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    if fp8 and h_scales is None:
+        h_scales = torch.empty((R_cap, w.F // 32), dtype=torch.uint8, device=dev)
+    st = _lib.load().moe_grouped_gemm_up(
+        _ptr(x_perm), _ptr(x_scales), _ptr(w.w13), _ptr(w.w13_scales), _dt_code(w.precision),
+        _ptr(group_offsets), w.E, w.H, w.F, R_cap, _ptr(h), _ptr(h_scales), _ptr(ab), _ptr(h_bf16),
+        _stream(stream))
+    _check("moe_grouped_gemm_up", st)
+    return h, h_scales
+
+
+class BwdWeights(NamedTuple):
+    precision: str
+    E: int
+    H: int
+    F: int
+    w2b: torch.Tensor                   # [E, F, H] bf16 or uint8
+    w2b_scales: Optional[torch.Tensor]  # [E, F, H/32]
+    w13t: torch.Tensor                  # [E, H, 2F]
+    w13t_scales: Optional[torch.Tensor]  # [E, H, 2F/32]
+
+
+def moe_prepare_weights_bwd(w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, precision: str = "bf16",
+                            stream=None) -> BwdWeights:
+    """Pack logical W1, W3 [E, H, F] and W2 [E, F, H] for the backward GEMMs (one-time)."""
+    for t, n in ((w1, "w1"), (w3, "w3"), (w2, "w2")):
+        _want(t, n, torch.bfloat16, 3)
+    E, H, F = w1.shape
+    dev = w1.device
+    fp8 = precision == "mxfp8"
+    pdt = torch.uint8 if fp8 else torch.bfloat16
+    w2b = torch.empty((E, F, H), dtype=pdt, device=dev)
+    w13t = torch.empty((E, H, 2 * F), dtype=pdt, device=dev)
+    s2 = torch.empty((E, F, H // 32), dtype=torch.uint8, device=dev) if fp8 else None
+    s13 = torch.empty((E, H, 2 * F // 32), dtype=torch.uint8, device=dev) if fp8 else None
+    st = _lib.load().moe_prepare_weights_bwd(_ptr(w1), _ptr(w3), _ptr(w2), E, H, F, _dt_code(precision),
+                                             _ptr(w2b), _ptr(s2), _ptr(w13t), _ptr(s13), _stream(stream))
+    _check("moe_prepare_weights_bwd", st)
+    return BwdWeights(precision, E, H, F, w2b, s2, w13t, s13)
+
+
+def moe_grouped_swiglu_dgrad(dy: torch.Tensor, dy_scales: Optional[torch.Tensor], bw: BwdWeights,
+                             ab: torch.Tensor, group_offsets: torch.Tensor, *, dab: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """dy [R_cap, H] (bf16 or MXFP8 codes) -> dab [R_cap, 2F] bf16 (da | db interleaved per 128)."""
+    R_cap = dy.shape[0]
+    if dab is None:
+        dab = torch.empty((R_cap, 2 * bw.F), dtype=torch.bfloat16, device=dy.device)
+    st = _lib.load().moe_grouped_swiglu_dgrad(
+        _ptr(dy), _ptr(dy_scales), _ptr(bw.w2b), _ptr(bw.w2b_scales), _ptr(ab), _dt_code(bw.precision),
+        _ptr(group_offsets), bw.E, bw.H, bw.F, R_cap, _ptr(dab), _stream(stream))
+    _check("moe_grouped_swiglu_dgrad", st)
+    return dab
+
+
+def moe_grouped_gemm_dx(dab: torch.Tensor, dab_scales: Optional[torch.Tensor], bw: BwdWeights,
+                        group_offsets: torch.Tensor, *, dx: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """dab [R_cap, 2F] (bf16 or MXFP8 codes) -> dx [R_cap, H] bf16."""
+    R_cap = dab.shape[0]
+    if dx is None:
+        dx = torch.empty((R_cap, bw.H), dtype=torch.bfloat16, device=dab.device)
+    st = _lib.load().moe_grouped_gemm_dx(
+        _ptr(dab), _ptr(dab_scales), _ptr(bw.w13t), _ptr(bw.w13t_scales), _dt_code(bw.precision),
+        _ptr(group_offsets), bw.E, bw.H, bw.F, R_cap, _ptr(dx), _stream(stream))
+    _check("moe_grouped_gemm_dx", st)
+    return dx
+
+
+def moe_grouped_transpose_kpad(R_cap: int, E: int) -> int:
+    return int(_lib.load().moe_grouped_transpose_kpad(R_cap, E))
+
+
+def moe_grouped_transpose(x: torch.Tensor, group_offsets: torch.Tensor, precision: str = "bf16", *,
+                          R_cap: Optional[int] = None, src_rows: Optional[torch.Tensor] = None,
+                          xT: Optional[torch.Tensor] = None, xT_scales: Optional[torch.Tensor] = None,
+                          stream=None):
+    """Group-padded transposed weight-gradient operand [C, Kpad] (bf16, or MXFP8 + scales)."""
+    _want(x, "x", torch.bfloat16, 2)
+    C = x.shape[1]
+    if R_cap is None:
+        R_cap = x.shape[0]
+    E = group_offsets.numel() - 1
+    kpad = moe_grouped_transpose_kpad(R_cap, E)
+    fp8 = precision == "mxfp8"
+    if xT is None:
+        xT = torch.empty((C, kpad), dtype=torch.uint8 if fp8 else torch.bfloat16, device=x.device)
+    if fp8 and xT_scales is None:
+        xT_scales = torch.empty((C, kpad // 32), dtype=torch.uint8, device=x.device)
+    st = _lib.load().moe_grouped_transpose(_ptr(x), _ptr(src_rows), R_cap, C, _ptr(group_offsets), E,
+                                           _dt_code(precision), _ptr(xT), _ptr(xT_scales), _stream(stream))
+    _check("moe_grouped_transpose", st)
+    return xT, xT_scales
+
+
+def moe_grouped_gemm_wgrad(aT: torch.Tensor, aT_scales: Optional[torch.Tensor], bT: torch.Tensor,
+                           bT_scales: Optional[torch.Tensor], precision: str, group_offsets: torch.Tensor,
+                           R_cap: int, *, split: bool = False, dw: Optional[torch.Tensor] = None,
+                           dw2: Optional[torch.Tensor] = None, stream=None):
+    """dW[e] = sum over group e's rows of a^T b, from transposed operands [M, Kpad], [N, Kpad]."""
+    M, N = aT.shape[0], bT.shape[0]
+    E = group_offsets.numel() - 1
+    dev = aT.device
+    if split:
+        if dw is None:
+            dw = torch.empty((E, M, N // 2), dtype=torch.bfloat16, device=dev)
+        if dw2 is None:
+            dw2 = torch.empty((E, M, N // 2), dtype=torch.bfloat16, device=dev)
+    elif dw is None:
+        dw = torch.empty((E, M, N), dtype=torch.bfloat16, device=dev)
+    st = _lib.load().moe_grouped_gemm_wgrad(
+        _ptr(aT), _ptr(aT_scales), _ptr(bT), _ptr(bT_scales), _dt_code(precision), _ptr(group_offsets), E, M, N,
+        R_cap, _ptr(dw), _ptr(dw2 if split else None), _stream(stream))
+    _check("moe_grouped_gemm_wgrad", st)
+    return (dw, dw2) if split else dw

@@ -1,5 +1,6 @@
-// gemm.cu -- persistent ragged grouped GEMM on tcgen05 tensor cores, with the
-// SwiGLU expert MLP built from two launches, plus one-time weight packing.
+// gemm.cu -- persistent ragged grouped GEMM on tcgen05 tensor cores: the
+// forward SwiGLU expert MLP (two launches), its activation gradient (two
+// launches) and its weight gradient.
 //
 // "Dropless MoE acceleration in JAX with NVIDIA Transformer Engine", section
 // "Optimization 1: Grouped GEMM": one kernel covers every expert with its actual
@@ -7,26 +8,41 @@
 // device (no device-to-host copy, so the call can live in a CUDA graph); on
 // Blackwell the expert matmuls can use MXFP8 block scaling. The same page's
 // MoE-layer figure: the grouped MLP is two grouped GEMMs on variable-length
-// groups.
+// groups; its "Measured training impact" is a training step, so the grouped
+// backward GEMMs run on the same ragged groups.
+//
+// One kernel template, four modes:
+//   UP     A = x_perm [R_cap, H] (rows grouped by expert), B = W13 packed
+//          [E][2F][H]; epilogue: h = silu(a) * b (bf16 or MXFP8), optionally the
+//          bf16 pre-activations (a | b) and a bf16 copy of h for the backward.
+//   DOWN   A = h or dab [R_cap, K], B = W2p [E][H][F] or W13t [E][H][2F];
+//          epilogue: plain bf16 store (y_perm, or dx).
+//   DGRAD  A = dy_perm [R_cap, H], B = W2 [E][F][H]; epilogue: SwiGLU backward
+//          da = dh * b * silu'(a), db = dh * silu(a) with the saved (a | b),
+//          stored bf16 in the same interleaved layout.
+//   WGRAD  contraction over each expert's rows: A = aT [M][Kpad], B = bT [N][Kpad]
+//          (transposed, group-padded operands, zero past each group's end);
+//          output dW[e] [M][N] bf16, or split into two [M][N/2] halves.
 //
 // Design (one CTA per SM, persistent, warp-specialised; 192 threads):
 //   warp 0     TMA producer: A tile [128 rows x 128 B] and B tile [256 rows x 128 B]
 //              per k-block into a 4-stage shared-memory ring (128-byte swizzle);
-//              MXFP8 adds the per-row E8M0 scale words of the k-block (cp.async
-//              straight into the layout tcgen05.cp expects).
+//              MXFP8 adds the E8M0 scale words of the k-block (cp.async straight
+//              into the layout tcgen05.cp expects).
 //   warp 1     allocates TMEM and issues tcgen05.mma (M=128, N=256) from one
 //              lane; each k-block's commit frees its ring stage, each tile's
 //              commit hands the accumulator to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns the
-//              32 TMEM lanes of its quarter), SwiGLU (GEMM1) or plain (GEMM2),
-//              bf16 (or MXFP8) rows stored for the rows inside the group only.
-// Tiles are scheduled on the device: every CTA reads group_offsets, counts
-// ceil(m_e / 128) row tiles per expert and walks the tile list
-// (expert-major, then output column tile, then row tile, so one weight tile is
-// consumed by all row tiles of its expert while it is hot in L2) with a static
-// stride of gridDim.x. A row tile that runs past its group reads the next
-// group's rows (or TMA zero fill past R_cap); those accumulator rows are
-// simply never stored. No padding, no dropping.
+//              32 TMEM lanes of its quarter) and the mode's store.
+// Tiles are scheduled on the device: every CTA reads group_offsets and walks
+// the tile list with a static stride of gridDim.x. Row-grouped modes count
+// ceil(m_e / 128) row tiles per expert and order tiles expert-major, then
+// output column tile, then row tile (one weight tile is consumed by all row
+// tiles of its expert while it is hot in L2); a row tile that runs past its
+// group reads the next group's rows (or TMA zero fill past R_cap) and those
+// accumulator rows are never stored. WGRAD tiles are (expert, N tile, M tile)
+// with ceil(m_e / BK) k-blocks each; an expert without rows stores zeros.
+// No padding of the data, no dropping.
 //
 // BF16: kind::f16, two TMEM accumulators (2 x 256 columns) so the epilogue of
 // tile i overlaps the main loop of tile i+1.
@@ -46,6 +62,8 @@ constexpr int STAGES = 4;        // shared-memory ring depth
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 
+enum { MODE_UP = 0, MODE_DOWN = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
+
 template <bool FP8>
 struct Cfg {
     static constexpr int BK = FP8 ? 128 : 64;       // elements per k-block (128 bytes per row)
@@ -63,15 +81,21 @@ struct Cfg {
 struct GemmArgs {
     const int* goff;             // [E+1] group offsets (device)
     int E;
-    int Kdim;                    // contraction length
-    int N;                       // B rows per expert
+    int Kdim;                    // contraction length (row-grouped modes)
+    int N;                       // B rows per expert (row-grouped) / B rows (WGRAD)
     int n_tiles;                 // N / BN
-    int R_cap;                   // rows of A
-    void* out;                   // [R_cap, ldo] bf16, or E4M3 codes (MXFP8 h)
-    int ldo;
-    uint8_t* out_scales;         // [R_cap, ldo/32] (MXFP8 h only)
-    const uint8_t* a_scales;     // [R_cap, Kdim/32] (MXFP8)
-    const uint8_t* b_scales;     // [E*N, Kdim/32] (MXFP8)
+    int R_cap;                   // rows of A (row-grouped)
+    void* out;                   // output (see the mode)
+    int ldo;                     // output row stride in elements
+    uint8_t* out_scales;         // UP + MXFP8: h scales [R_cap, ldo/32]
+    const uint8_t* a_scales;     // MXFP8 scales of A: [rows of A][sf_row_bytes]
+    const uint8_t* b_scales;     // MXFP8 scales of B
+    int sf_row_bytes;            // scale bytes per operand row (= contraction length / 32)
+    __nv_bfloat16* ab;           // UP: optional (a | b) save; DGRAD: the saved (a | b) input
+    __nv_bfloat16* h_bf16;       // UP + MXFP8: optional bf16 copy of h
+    int M;                       // WGRAD: rows of aT (multiple of BM)
+    int m_tiles;                 // WGRAD: M / BM
+    void* out2;                  // WGRAD split: second half [E][M][N/2]
 };
 
 template <bool FP8>
@@ -81,26 +105,61 @@ constexpr size_t smem_bytes_for(int E) {
 }
 
 struct TileInfo {
-    int e, m, n, row0, rows;
+    int e, m, n;
+    int row0, rows;      // row-grouped: first A row and rows inside the group
+    int a_row, b_row;    // operand rows of the tile
+    int k0, nkb;         // first contraction element and number of k-blocks
 };
 
-__device__ __forceinline__ TileInfo decode_tile(int tile, const int* s_mtp, const int* s_goff, int E, int n_tiles) {
-    const int q = tile / n_tiles;
-    int lo = 0, hi = E - 1;  // last e with s_mtp[e] <= q (never an empty expert)
+// Row-grouped modes: tile -> (expert, column tile, row tile).
+template <bool FP8>
+__device__ __forceinline__ TileInfo decode_rows(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p) {
+    const int q = tile / p.n_tiles;
+    int lo = 0, hi = p.E - 1;  // last e with s_mtp[e] <= q (never an empty expert)
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
         if (s_mtp[mid] <= q) lo = mid;
         else hi = mid - 1;
     }
     const int mt = s_mtp[lo + 1] - s_mtp[lo];
-    const int local = tile - s_mtp[lo] * n_tiles;
+    const int local = tile - s_mtp[lo] * p.n_tiles;
     TileInfo t;
     t.e = lo;
     t.n = local / mt;
     t.m = local - t.n * mt;
     t.row0 = s_goff[lo] + t.m * BM;
     t.rows = min(BM, s_goff[lo + 1] - t.row0);
+    t.a_row = t.row0;
+    t.b_row = lo * p.N + t.n * BN;
+    t.k0 = 0;
+    t.nkb = p.Kdim / Cfg<FP8>::BK;
     return t;
+}
+
+// WGRAD: tile -> (expert, N tile, M tile); the expert's rows sit at
+// [128 * (e + goff[e] / 128), + m_e) of the padded contraction axis.
+template <bool FP8>
+__device__ __forceinline__ TileInfo decode_wgrad(int tile, const int* s_goff, const GemmArgs& p) {
+    const int per = p.m_tiles * p.n_tiles;
+    TileInfo t;
+    t.e = tile / per;
+    const int local = tile - t.e * per;
+    t.n = local / p.m_tiles;
+    t.m = local - t.n * p.m_tiles;
+    const int g0 = s_goff[t.e], m_e = s_goff[t.e + 1] - g0;
+    t.row0 = t.m * BM;
+    t.rows = BM;
+    t.a_row = t.m * BM;
+    t.b_row = t.n * BN;
+    t.k0 = 128 * (t.e + g0 / 128);
+    t.nkb = (m_e + Cfg<FP8>::BK - 1) / Cfg<FP8>::BK;
+    return t;
+}
+
+template <int MODE, bool FP8>
+__device__ __forceinline__ TileInfo decode(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p) {
+    if constexpr (MODE == MODE_WGRAD) return decode_wgrad<FP8>(tile, s_goff, p);
+    else return decode_rows<FP8>(tile, s_mtp, s_goff, p);
 }
 
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -108,6 +167,22 @@ __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + _
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 32 fp32 values -> 32 bf16 stored as 4 x 16 bytes.
+__device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; i++) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; i++) bf16x8_to_f32(s[i], v + 8 * i);
 }
 
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool valid) {
@@ -118,7 +193,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
 }
 
-template <bool SWIGLU, bool FP8>
+template <int MODE, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
@@ -199,9 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
 
     const uint32_t tmem = *s_tmem;
-    const int total_tiles = s_mtp[E] * p.n_tiles;
-    const int num_kb = p.Kdim / C::BK;
-    const int kb_bytes_sf = p.Kdim / 32;  // scale bytes per row
+    const int total_tiles = MODE == MODE_WGRAD ? E * p.m_tiles * p.n_tiles : s_mtp[E] * p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -210,37 +283,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int issued = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(tile, s_mtp, s_goff, E, p.n_tiles);
-            const int a_row = ti.row0;
-            const int b_row = ti.e * p.N + ti.n * BN;
-            for (int kb = 0; kb < num_kb; kb++) {
+            const TileInfo ti = decode<MODE, FP8>(tile, s_mtp, s_goff, p);
+            for (int kb = 0; kb < ti.nkb; kb++) {
                 if (!ptx::wait_parity(&empty[stage], phase ^ 1u, s_abort)) { ok = false; break; }
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
+                const int k = ti.k0 + kb * C::BK;
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
-                    ptx::tma_load_2d(sa, &tmA, &full[stage], kb * C::BK, a_row);
-                    ptx::tma_load_2d(sb, &tmB, &full[stage], kb * C::BK, b_row);
+                    ptx::tma_load_2d(sa, &tmA, &full[stage], k, ti.a_row);
+                    ptx::tma_load_2d(sb, &tmB, &full[stage], k, ti.b_row);
                 }
                 if constexpr (FP8) {
                     // scale words of this k-block, transposed for tcgen05.cp .32x128b:
                     // word (lane*4 + j) of a 512-byte chunk holds row 32*j + lane of the chunk
                     const uint32_t sfa = ptx::smem_addr(sb + C::B_BYTES);
                     const uint32_t sfb = sfa + C::SFA_BYTES;
+                    const int kw = k / 32;  // first scale byte of the k-block (multiple of 4)
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const int r = a_row + 32 * j + lane;
-                        const bool v = r < p.R_cap;
+                        const int r = ti.a_row + 32 * j + lane;
+                        const bool v = MODE == MODE_WGRAD || r < p.R_cap;
                         cp_async_4(sfa + (lane * 4 + j) * 4,
-                                   p.a_scales + (size_t)(v ? r : 0) * kb_bytes_sf + kb * 4, v);
+                                   p.a_scales + (size_t)(v ? r : 0) * p.sf_row_bytes + kw, v);
                     }
 #pragma unroll
                     for (int c = 0; c < 2; c++)
 #pragma unroll
                         for (int j = 0; j < 4; j++) {
-                            const int r = b_row + 128 * c + 32 * j + lane;
+                            const int r = ti.b_row + 128 * c + 32 * j + lane;
                             cp_async_4(sfb + c * 512 + (lane * 4 + j) * 4,
-                                       p.b_scales + (size_t)r * kb_bytes_sf + kb * 4, true);
+                                       p.b_scales + (size_t)r * p.sf_row_bytes + kw, true);
                         }
                     cp_async_arrive_noinc(&full[stage]);
                 }
@@ -265,10 +338,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            const int nkb = MODE == MODE_WGRAD ? decode_wgrad<FP8>(tile, s_goff, p).nkb : p.Kdim / C::BK;
             if (!ptx::wait_parity(&tempty[acc], acc_phase ^ 1u, s_abort)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < num_kb; kb++) {
+            for (int kb = 0; kb < nkb; kb++) {
                 if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
                 ptx::tc_fence_after();
                 if (lane == 0) {
@@ -314,13 +388,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(tile, s_mtp, s_goff, E, p.n_tiles);
+            const TileInfo ti = decode<MODE, FP8>(tile, s_mtp, s_goff, p);
             if (!ptx::wait_parity(&tfull[acc], acc_phase, s_abort)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const bool valid = rit < ti.rows;
             const long long r = (long long)ti.row0 + rit;
-            if constexpr (SWIGLU) {
+            if constexpr (MODE == MODE_UP) {
                 const int col0 = ti.n * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; c++) {
@@ -331,6 +405,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 32; i++) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+                    if (valid && p.ab) {
+                        // saved pre-activations, same interleaved layout as W13 packed
+                        __nv_bfloat16* abrow = p.ab + r * (2 * p.ldo) + ti.n * BN + 32 * c;
+                        store_bf16x32(abrow, reinterpret_cast<const float*>(g));
+                        store_bf16x32(abrow + BN / 2, reinterpret_cast<const float*>(u));
+                    }
                     if constexpr (FP8) {
                         float amax = 0.0f;
 #pragma unroll
@@ -347,36 +427,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                             p.out_scales[r * (p.ldo / 32) + (col0 / 32) + c] = (uint8_t)sbyte;
+                            if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + col0 + 32 * c, hv);
                         }
                     } else {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; i++) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-                        if (valid) {
-                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo +
-                                                                  col0 + 32 * c);
-#pragma unroll
-                            for (int i = 0; i < 4; i++)
-                                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                        }
+                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + col0 + 32 * c, hv);
                     }
                 }
-            } else {
+            } else if constexpr (MODE == MODE_DGRAD) {
+                // dh columns f = n*256 + 32c + i; (a | b) and (da | db) interleaved per 128 columns
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c++) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_x32(tbase + 32 * c, v);
+                    ptx::tmem_wait_ld();
+                    if (valid) {
+                        const int f = ti.n * BN + 32 * c;
+                        const long long off = r * p.ldo + (long long)(f / 128) * 256 + (f % 128);
+                        float a[32], b[32], da[32], db[32];
+                        load_bf16x32(p.ab + off, a);
+                        load_bf16x32(p.ab + off + 128, b);
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            const float dh = __uint_as_float(v[i]);
+                            const float sg = __fdividef(1.0f, 1.0f + __expf(-a[i]));
+                            da[i] = dh * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
+                            db[i] = dh * a[i] * sg;
+                        }
+                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
+                        store_bf16x32(o + off, da);
+                        store_bf16x32(o + off + 128, db);
+                    }
+                }
+            } else if constexpr (MODE == MODE_WGRAD) {
+                const bool empty_expert = ti.nkb == 0;
+                const long long orow = (long long)ti.e * p.M + ti.m * BM + rit;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c++) {
+                    float v[32];
+                    if (!empty_expert) {
+                        uint32_t u[32];
+                        ptx::tmem_ld_x32(tbase + 32 * c, u);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(u[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = 0.0f;
+                    }
+                    if (p.out2) {  // split: columns [0,128) of the tile -> out, [128,256) -> out2
+                        const int half = c / 4;
+                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(half ? p.out2 : p.out);
+                        store_bf16x32(o + orow * (p.N / 2) + ti.n * (BN / 2) + 32 * (c % 4), v);
+                    } else {
+                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + orow * p.N + ti.n * BN + 32 * c, v);
+                    }
+                }
+            } else {  // MODE_DOWN
                 const int col0 = ti.n * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; c++) {
                     uint32_t v[32];
                     ptx::tmem_ld_x32(tbase + 32 * c, v);
                     ptx::tmem_wait_ld();
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i++) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    if (valid) {
-                        uint4* dst =
-                            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + col0 + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; i++) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    }
+                    if (valid)
+                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + col0 + 32 * c,
+                                      reinterpret_cast<const float*>(v));
                 }
             }
             ptx::tc_fence_before();
@@ -391,70 +506,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
-}
-
-// ---------------------------------------------------------------- weight packing
-// W1, W3 [E][H][F] -> W13 [E][2F][H] with rows grouped per 256-row tile:
-// rows [256 j, 256 j + 128) = W1^T rows f in [128 j, 128 j + 128), the next 128 = W3^T.
-// W2 [E][F][H] -> W2p [E][H][F] (= W2^T per expert).
-__device__ __forceinline__ int w13_row(int f, int half) { return (f / 128) * 256 + half * 128 + (f % 128); }
-
-// in [E][rows][cols] bf16 -> out [E][out_rows][rows] with out row = map(col).
-template <int MODE>  // 0: W13 half 0 (W1), 1: W13 half 1 (W3), 2: W2
-__global__ void pack_bf16_kernel(const __nv_bfloat16* __restrict__ in, int rows, int cols,
-                                 __nv_bfloat16* __restrict__ out) {
-    __shared__ __nv_bfloat16 tile[32][33];
-    const int e = blockIdx.z;
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-    const __nv_bfloat16* src = in + (size_t)e * rows * cols;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        int r = r0 + i, c = c0 + threadIdx.x;
-        if (r < rows && c < cols) tile[i][threadIdx.x] = src[(size_t)r * cols + c];
-    }
-    __syncthreads();
-    const int out_rows = MODE == 2 ? cols : 2 * cols;
-    __nv_bfloat16* dst = out + (size_t)e * out_rows * rows;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        int c = c0 + i, r = r0 + threadIdx.x;
-        if (r < rows && c < cols) {
-            int orow = MODE == 2 ? c : w13_row(c, MODE);
-            dst[(size_t)orow * rows + r] = tile[threadIdx.x][i];
-        }
-    }
-}
-
-// MXFP8 packing: transpose as above and quantise each packed row along its
-// contraction dimension (the source's rows) in blocks of 32. Block (32 source
-// rows x 32 source columns); thread x owns one source column.
-template <int MODE>
-__global__ void pack_mxfp8_kernel(const __nv_bfloat16* __restrict__ in, int rows, int cols,
-                                  uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
-    const int e = blockIdx.z;
-    const int r0 = blockIdx.y * 32;
-    const int c = blockIdx.x * 32 + threadIdx.x;
-    if (c >= cols) return;
-    const __nv_bfloat16* src = in + (size_t)e * rows * cols;
-    float v[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-        v[i] = __bfloat162float(src[(size_t)(r0 + i) * cols + c]);
-        amax = fmaxf(amax, fabsf(v[i]));
-    }
-    const int sb = e8m0_scale_byte(amax);
-    const float inv = e8m0_inv_scale(sb);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-        w[i] = (uint32_t)f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
-               ((uint32_t)f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
-    const int out_rows = MODE == 2 ? cols : 2 * cols;
-    const int orow = MODE == 2 ? c : w13_row(c, MODE);
-    uint8_t* qrow = q + ((size_t)e * out_rows + orow) * rows + r0;
-    uint4* d = reinterpret_cast<uint4*>(qrow);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    s[((size_t)e * out_rows + orow) * (rows / 32) + r0 / 32] = (uint8_t)sb;
 }
 
 // ---------------------------------------------------------------- host side
@@ -496,87 +547,59 @@ int device_sms() {
     return sms;
 }
 
-template <bool SWIGLU, bool FP8>
-moe_status launch_gemm(const void* A, const void* B, const GemmArgs& a, cudaStream_t s) {
+// A: [a_rows][a_inner], B: [b_rows][a_inner], both K-major.
+template <int MODE, bool FP8>
+moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
+                       const GemmArgs& a, cudaStream_t s) {
     CUtensorMap tmA, tmB;
-    if (!make_operand_map(&tmA, A, FP8, (uint64_t)a.Kdim, (uint64_t)a.R_cap, BM)) return MOE_ERR_CUDA;
-    if (!make_operand_map(&tmB, B, FP8, (uint64_t)a.Kdim, (uint64_t)a.E * a.N, BN)) return MOE_ERR_CUDA;
+    if (!make_operand_map(&tmA, A, FP8, inner, a_rows, BM)) return MOE_ERR_CUDA;
+    if (!make_operand_map(&tmB, B, FP8, inner, b_rows, BN)) return MOE_ERR_CUDA;
     const size_t smem = smem_bytes_for<FP8>(a.E);
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<SWIGLU, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
-    grouped_gemm_kernel<SWIGLU, FP8><<<device_sms(), NUM_THREADS, smem, s>>>(tmA, tmB, a);
+    grouped_gemm_kernel<MODE, FP8><<<device_sms(), NUM_THREADS, smem, s>>>(tmA, tmB, a);
     return moe_host::launch_status();
 }
 
-}  // namespace
-}  // namespace moe
-
-extern "C" size_t moe_packed_weights_bytes(int E, int H, int F, moe_dtype dtype, int which) {
-    if (E < 1 || H < 1 || F < 1) return 0;
-    const size_t n13 = (size_t)E * 2 * F * H, n2 = (size_t)E * H * F;
-    const bool fp8 = dtype == MOE_MXFP8;
-    switch (which) {
-        case 0: return n13 * (fp8 ? 1 : 2);
-        case 1: return fp8 ? n13 / 32 : 0;
-        case 2: return n2 * (fp8 ? 1 : 2);
-        case 3: return fp8 ? n2 / 32 : 0;
-    }
-    return 0;
+template <int MODE>
+moe_status launch_mode(bool fp8, const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
+                       const GemmArgs& a, cudaStream_t s) {
+    return fp8 ? launch_gemm<MODE, true>(A, a_rows, B, b_rows, inner, a, s)
+               : launch_gemm<MODE, false>(A, a_rows, B, b_rows, inner, a, s);
 }
 
-extern "C" moe_status moe_prepare_weights(const void* w1, const void* w3, const void* w2, int E, int H, int F,
-                                          moe_dtype dtype, void* w13_packed, uint8_t* w13_scales,
-                                          void* w2_packed, uint8_t* w2_scales, moe_stream_t stream) {
-    using namespace moe;
-    if (E < 1 || H < 128 || F < 128 || (H % 128) || (F % 128)) return MOE_ERR_INVALID_ARG;
-    if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
-    if (!w1 || !w3 || !w2 || !w13_packed || !w2_packed) return MOE_ERR_INVALID_ARG;
-    if (dtype == MOE_MXFP8 && (!w13_scales || !w2_scales)) return MOE_ERR_INVALID_ARG;
-    if (!moe_host::aligned(w13_packed, 16) || !moe_host::aligned(w2_packed, 16)) return MOE_ERR_ALIGNMENT;
-    cudaStream_t s = moe_host::as_stream(stream);
-    const __nv_bfloat16* W1 = (const __nv_bfloat16*)w1;
-    const __nv_bfloat16* W3 = (const __nv_bfloat16*)w3;
-    const __nv_bfloat16* W2 = (const __nv_bfloat16*)w2;
-    if (dtype == MOE_BF16) {
-        dim3 blk(32, 8);
-        dim3 g13((F + 31) / 32, (H + 31) / 32, E), g2((H + 31) / 32, (F + 31) / 32, E);
-        pack_bf16_kernel<0><<<g13, blk, 0, s>>>(W1, H, F, (__nv_bfloat16*)w13_packed);
-        pack_bf16_kernel<1><<<g13, blk, 0, s>>>(W3, H, F, (__nv_bfloat16*)w13_packed);
-        pack_bf16_kernel<2><<<g2, blk, 0, s>>>(W2, F, H, (__nv_bfloat16*)w2_packed);
-    } else {
-        dim3 g13((F + 31) / 32, H / 32, E), g2((H + 31) / 32, F / 32, E);
-        pack_mxfp8_kernel<0><<<g13, 32, 0, s>>>(W1, H, F, (uint8_t*)w13_packed, w13_scales);
-        pack_mxfp8_kernel<1><<<g13, 32, 0, s>>>(W3, H, F, (uint8_t*)w13_packed, w13_scales);
-        pack_mxfp8_kernel<2><<<g2, 32, 0, s>>>(W2, F, H, (uint8_t*)w2_packed, w2_scales);
-    }
-    return moe_host::launch_status();
-}
-
-static moe_status check_gemm_common(moe_dtype dtype, const int32_t* group_offsets, int E, int H, int F,
-                                    int R_cap) {
-    using namespace moe;
+moe_status check_common(moe_dtype dtype, const int32_t* group_offsets, int E, int H, int F, int R_cap) {
     if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
     if (E < 1 || H < 128 || F < 128 || R_cap < 0 || !group_offsets) return MOE_ERR_INVALID_ARG;
     if ((H % 256) || (F % 128)) return MOE_ERR_UNSUPPORTED;
     if (smem_bytes_for<true>(E) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
     if ((long long)E * 2 * F > 0x7fffffffLL || (long long)E * H > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+    if ((long long)R_cap * 2 * F > 0x7fffffffffffLL) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
+
+bool al(const void* p, size_t a) { return p == nullptr || moe_host::aligned(p, a); }
+
+}  // namespace
+}  // namespace moe
+
+using moe::GemmArgs;
 
 extern "C" moe_status moe_grouped_gemm_up(const void* x_perm, const uint8_t* x_scales, const void* w13_packed,
                                           const uint8_t* w13_scales, moe_dtype dtype,
                                           const int32_t* group_offsets, int E, int H, int F, int R_cap, void* h,
-                                          uint8_t* h_scales, moe_stream_t stream) {
+                                          uint8_t* h_scales, void* ab_save, void* h_bf16_save,
+                                          moe_stream_t stream) {
     using namespace moe;
-    moe_status st = check_gemm_common(dtype, group_offsets, E, H, F, R_cap);
+    moe_status st = check_common(dtype, group_offsets, E, H, F, R_cap);
     if (st != MOE_OK) return st;
     if (R_cap == 0) return MOE_OK;
     const bool fp8 = dtype == MOE_MXFP8;
-    if (!x_perm || !w13_packed || !h || (fp8 && (!x_scales || !w13_scales || !h_scales)))
-        return MOE_ERR_INVALID_ARG;
-    if (!moe_host::aligned(x_perm, 128) || !moe_host::aligned(w13_packed, 128) || !moe_host::aligned(h, 16) ||
-        (fp8 && (!moe_host::aligned(x_scales, 4) || !moe_host::aligned(w13_scales, 4))))
+    if (!x_perm || !w13_packed || !h || (fp8 && (!x_scales || !w13_scales || !h_scales))) return MOE_ERR_INVALID_ARG;
+    if (h_bf16_save && !fp8) return MOE_ERR_INVALID_ARG;
+    if (!al(x_perm, 128) || !al(w13_packed, 128) || !al(h, 16) || !al(ab_save, 16) || !al(h_bf16_save, 16) ||
+        (fp8 && (!al(x_scales, 4) || !al(w13_scales, 4))))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;
@@ -590,38 +613,47 @@ extern "C" moe_status moe_grouped_gemm_up(const void* x_perm, const uint8_t* x_s
     a.out_scales = h_scales;
     a.a_scales = x_scales;
     a.b_scales = w13_scales;
-    cudaStream_t s = moe_host::as_stream(stream);
-    return fp8 ? launch_gemm<true, true>(x_perm, w13_packed, a, s)
-               : launch_gemm<true, false>(x_perm, w13_packed, a, s);
+    a.sf_row_bytes = H / 32;
+    a.ab = static_cast<__nv_bfloat16*>(ab_save);
+    a.h_bf16 = static_cast<__nv_bfloat16*>(h_bf16_save);
+    return launch_mode<MODE_UP>(fp8, x_perm, (uint64_t)R_cap, w13_packed, (uint64_t)E * 2 * F, (uint64_t)H, a,
+                                moe_host::as_stream(stream));
+}
+
+// Shared by the forward down projection (A = h, B = W2p, K = F) and the dx
+// product of the backward (A = dab, B = W13t, K = 2F): y[r] = A[r] B[e]^T.
+static moe_status grouped_down(const void* A, const uint8_t* a_scales, const void* B, const uint8_t* b_scales,
+                               moe_dtype dtype, const int32_t* group_offsets, int E, int H, int Kc, int R_cap,
+                               void* out, moe_stream_t stream) {
+    using namespace moe;
+    if (R_cap == 0) return MOE_OK;
+    const bool fp8 = dtype == MOE_MXFP8;
+    if (!A || !B || !out || (fp8 && (!a_scales || !b_scales))) return MOE_ERR_INVALID_ARG;
+    if (!al(A, 128) || !al(B, 128) || !al(out, 16) || (fp8 && (!al(a_scales, 4) || !al(b_scales, 4))))
+        return MOE_ERR_ALIGNMENT;
+    GemmArgs a{};
+    a.goff = group_offsets;
+    a.E = E;
+    a.Kdim = Kc;
+    a.N = H;
+    a.n_tiles = H / BN;
+    a.R_cap = R_cap;
+    a.out = out;
+    a.ldo = H;
+    a.a_scales = a_scales;
+    a.b_scales = b_scales;
+    a.sf_row_bytes = Kc / 32;
+    return launch_mode<MODE_DOWN>(fp8, A, (uint64_t)R_cap, B, (uint64_t)E * H, (uint64_t)Kc, a,
+                                  moe_host::as_stream(stream));
 }
 
 extern "C" moe_status moe_grouped_gemm_down(const void* h, const uint8_t* h_scales, const void* w2_packed,
                                             const uint8_t* w2_scales, moe_dtype dtype,
                                             const int32_t* group_offsets, int E, int H, int F, int R_cap,
                                             void* y_perm, moe_stream_t stream) {
-    using namespace moe;
-    moe_status st = check_gemm_common(dtype, group_offsets, E, H, F, R_cap);
+    moe_status st = moe::check_common(dtype, group_offsets, E, H, F, R_cap);
     if (st != MOE_OK) return st;
-    if ((H % BN) != 0) return MOE_ERR_UNSUPPORTED;
-    if (R_cap == 0) return MOE_OK;
-    const bool fp8 = dtype == MOE_MXFP8;
-    if (!h || !w2_packed || !y_perm || (fp8 && (!h_scales || !w2_scales))) return MOE_ERR_INVALID_ARG;
-    if (!moe_host::aligned(h, 128) || !moe_host::aligned(w2_packed, 128) || !moe_host::aligned(y_perm, 16) ||
-        (fp8 && (!moe_host::aligned(h_scales, 4) || !moe_host::aligned(w2_scales, 4))))
-        return MOE_ERR_ALIGNMENT;
-    GemmArgs a{};
-    a.goff = group_offsets;
-    a.E = E;
-    a.Kdim = F;
-    a.N = H;
-    a.n_tiles = H / BN;
-    a.R_cap = R_cap;
-    a.out = y_perm;
-    a.ldo = H;
-    a.a_scales = h_scales;
-    a.b_scales = w2_scales;
-    cudaStream_t s = moe_host::as_stream(stream);
-    return fp8 ? launch_gemm<false, true>(h, w2_packed, a, s) : launch_gemm<false, false>(h, w2_packed, a, s);
+    return grouped_down(h, h_scales, w2_packed, w2_scales, dtype, group_offsets, E, H, F, R_cap, y_perm, stream);
 }
 
 extern "C" moe_status moe_grouped_swiglu_gemm(const void* x_perm, const uint8_t* x_scales,
@@ -630,8 +662,84 @@ extern "C" moe_status moe_grouped_swiglu_gemm(const void* x_perm, const uint8_t*
                                               const int32_t* group_offsets, int E, int H, int F, int R_cap,
                                               void* h, uint8_t* h_scales, void* y_perm, moe_stream_t stream) {
     moe_status st = moe_grouped_gemm_up(x_perm, x_scales, w13_packed, w13_scales, dtype, group_offsets, E, H, F,
-                                        R_cap, h, h_scales, stream);
+                                        R_cap, h, h_scales, nullptr, nullptr, stream);
     if (st != MOE_OK) return st;
     return moe_grouped_gemm_down(h, h_scales, w2_packed, w2_scales, dtype, group_offsets, E, H, F, R_cap, y_perm,
                                  stream);
+}
+
+extern "C" moe_status moe_grouped_swiglu_dgrad(const void* dy, const uint8_t* dy_scales, const void* w2_bwd,
+                                               const uint8_t* w2_bwd_scales, const void* ab, moe_dtype dtype,
+                                               const int32_t* group_offsets, int E, int H, int F, int R_cap,
+                                               void* dab, moe_stream_t stream) {
+    using namespace moe;
+    moe_status st = check_common(dtype, group_offsets, E, H, F, R_cap);
+    if (st != MOE_OK) return st;
+    if ((F % BN) != 0) return MOE_ERR_UNSUPPORTED;
+    if (R_cap == 0) return MOE_OK;
+    const bool fp8 = dtype == MOE_MXFP8;
+    if (!dy || !w2_bwd || !ab || !dab || (fp8 && (!dy_scales || !w2_bwd_scales))) return MOE_ERR_INVALID_ARG;
+    if (!al(dy, 128) || !al(w2_bwd, 128) || !al(ab, 16) || !al(dab, 16) ||
+        (fp8 && (!al(dy_scales, 4) || !al(w2_bwd_scales, 4))))
+        return MOE_ERR_ALIGNMENT;
+    GemmArgs a{};
+    a.goff = group_offsets;
+    a.E = E;
+    a.Kdim = H;
+    a.N = F;
+    a.n_tiles = F / BN;
+    a.R_cap = R_cap;
+    a.out = dab;
+    a.ldo = 2 * F;
+    a.a_scales = dy_scales;
+    a.b_scales = w2_bwd_scales;
+    a.sf_row_bytes = H / 32;
+    a.ab = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ab));
+    return launch_mode<MODE_DGRAD>(fp8, dy, (uint64_t)R_cap, w2_bwd, (uint64_t)E * F, (uint64_t)H, a,
+                                   moe_host::as_stream(stream));
+}
+
+extern "C" moe_status moe_grouped_gemm_dx(const void* dab, const uint8_t* dab_scales, const void* w13t,
+                                          const uint8_t* w13t_scales, moe_dtype dtype, const int32_t* group_offsets,
+                                          int E, int H, int F, int R_cap, void* dx, moe_stream_t stream) {
+    moe_status st = moe::check_common(dtype, group_offsets, E, H, F, R_cap);
+    if (st != MOE_OK) return st;
+    return grouped_down(dab, dab_scales, w13t, w13t_scales, dtype, group_offsets, E, H, 2 * F, R_cap, dx, stream);
+}
+
+extern "C" size_t moe_grouped_transpose_kpad(int R_cap, int E) {
+    if (R_cap < 0 || E < 1) return 0;
+    return (size_t)128 * ((size_t)E + ((size_t)R_cap + 127) / 128 + 1);
+}
+
+extern "C" moe_status moe_grouped_gemm_wgrad(const void* aT, const uint8_t* aT_scales, const void* bT,
+                                             const uint8_t* bT_scales, moe_dtype dtype,
+                                             const int32_t* group_offsets, int E, int M, int N, int R_cap,
+                                             void* dw, void* dw2, moe_stream_t stream) {
+    using namespace moe;
+    if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || M < BM || N < BN || R_cap < 0 || !group_offsets) return MOE_ERR_INVALID_ARG;
+    if ((M % BM) || (N % BN)) return MOE_ERR_UNSUPPORTED;
+    if (smem_bytes_for<true>(E) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    const size_t kpad = moe_grouped_transpose_kpad(R_cap, E);
+    if (kpad > 0x7fffffffULL || (long long)E * M > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+    const bool fp8 = dtype == MOE_MXFP8;
+    if (!aT || !bT || !dw || (fp8 && (!aT_scales || !bT_scales))) return MOE_ERR_INVALID_ARG;
+    if (!al(aT, 128) || !al(bT, 128) || !al(dw, 16) || !al(dw2, 16) ||
+        (fp8 && (!al(aT_scales, 4) || !al(bT_scales, 4))))
+        return MOE_ERR_ALIGNMENT;
+    GemmArgs a{};
+    a.goff = group_offsets;
+    a.E = E;
+    a.N = N;
+    a.n_tiles = N / BN;
+    a.M = M;
+    a.m_tiles = M / BM;
+    a.out = dw;
+    a.out2 = dw2;
+    a.a_scales = aT_scales;
+    a.b_scales = bT_scales;
+    a.sf_row_bytes = (int)(kpad / 32);
+    return launch_mode<MODE_WGRAD>(fp8, aT, (uint64_t)M, bT, (uint64_t)N, (uint64_t)kpad, a,
+                                   moe_host::as_stream(stream));
 }

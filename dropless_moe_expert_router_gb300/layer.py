@@ -56,7 +56,7 @@ class MoELayer:
         st = self._lib.moe_grouped_gemm_up(
             api._ptr(self.perm.x_perm), api._ptr(self.perm.x_perm_scales), api._ptr(w.w13),
             api._ptr(w.w13_scales), api._dt_code(w.precision), api._ptr(self.perm.group_offsets), w.E, w.H,
-            w.F, self.R_cap, api._ptr(self.h), api._ptr(self.h_scales), api._stream(stream))
+            w.F, self.R_cap, api._ptr(self.h), api._ptr(self.h_scales), None, None, api._stream(stream))
         api._check("moe_grouped_gemm_up", st)
 
     def stage_gemm_down(self, stream=None):

@@ -220,15 +220,80 @@ moe_status moe_grouped_swiglu_gemm(const void *x_perm, const uint8_t *x_scales,
                                    const int32_t *group_offsets, int E, int H, int F, int R_cap,
                                    void *h, uint8_t *h_scales, void *y_perm, moe_stream_t stream);
 
+/* moe_grouped_gemm_up also saves, when the pointers are not NULL, what the
+ * backward pass needs: ab_save [R_cap, 2F] bf16, the pre-activations a and b in
+ * the interleaved layout of w13_packed (per 256 columns: 128 of a, then the
+ * same 128 columns of b); h_bf16_save [R_cap, F] bf16, a bf16 copy of h (MXFP8
+ * only, for the column-wise quantisation of the weight gradient). */
 moe_status moe_grouped_gemm_up(const void *x_perm, const uint8_t *x_scales, const void *w13_packed,
                                const uint8_t *w13_scales, moe_dtype dtype,
                                const int32_t *group_offsets, int E, int H, int F, int R_cap,
-                               void *h, uint8_t *h_scales, moe_stream_t stream);
+                               void *h, uint8_t *h_scales, void *ab_save, void *h_bf16_save,
+                               moe_stream_t stream);
 
 moe_status moe_grouped_gemm_down(const void *h, const uint8_t *h_scales, const void *w2_packed,
                                  const uint8_t *w2_scales, moe_dtype dtype,
                                  const int32_t *group_offsets, int E, int H, int F, int R_cap,
                                  void *y_perm, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped backward of the SwiGLU expert MLP (the training step of [TEJAX]
+ * "Measured training impact", on the same ragged groups as the forward).
+ *
+ * For each expert e and row r of its group, with a, b the saved bf16
+ * pre-activations (ab_save of moe_grouped_gemm_up) and dy the gradient of y_perm:
+ *   dh = dy W2[e]^T;  da = dh * b * silu'(a);  db = dh * silu(a)
+ *       (silu'(a) = s(a) (1 + a (1 - s(a))), s the logistic function)
+ *   dx = da W1[e]^T + db W3[e]^T
+ *   dW2[e] = h_e^T dy_e;  dW1[e] = x_e^T da_e;  dW3[e] = x_e^T db_e
+ * (fp32 accumulation, bf16 outputs). Backward weights, packed once by
+ * moe_prepare_weights_bwd: w2_bwd [E][F][H] (= W2) and w13t [E][H][2F] (row h =
+ * W1[e][h] and W3[e][h] interleaved per 128 columns), bf16 or MXFP8 with blocks
+ * along H and along 2F respectively.
+ *
+ * moe_grouped_swiglu_dgrad: dy [R_cap, H] (bf16, or MXFP8 row-wise: E4M3 +
+ *   dy_scales [R_cap, H/32]) -> dab [R_cap, 2F] bf16 = (da | db) interleaved per
+ *   128 columns like ab. Requires F % 256 == 0.
+ * moe_grouped_gemm_dx: dab (bf16, or MXFP8 row-wise along 2F) -> dx [R_cap, H] bf16.
+ * moe_grouped_transpose: makes a weight-gradient operand: for x [R_cap, C] bf16
+ *   (or, with src_rows != NULL, x [*, C] read at row src_rows[r], e.g. the
+ *   tokens through perm_src), xT[c][P_e + i] = x[off[e] + i][c] for i < m_e, with
+ *   P_e = 128 * (e + off[e] / 128) and zeros up to P_e + 128 * ceil(m_e / 128);
+ *   xT is [C][Kpad], Kpad = moe_grouped_transpose_kpad(R_cap, E). MXFP8 output:
+ *   group-aware 32-row blocks (starting at each group's first row, a partial
+ *   block taking its amax over valid rows), E4M3 payload in xT and E8M0 scales
+ *   xT_scales[c][P_e / 32 + b] ([C][Kpad/32]). Requires C % 64 == 0.
+ * moe_grouped_gemm_wgrad: aT [M][Kpad], bT [N][Kpad] from moe_grouped_transpose
+ *   -> dw [E][M][N] bf16 with dw[e] = sum over group e's rows of a^T b; with dw2
+ *   != NULL the output is split: columns [256j, 256j+128) of each row go to
+ *   dw [E][M][N/2] and [256j+128, 256j+256) to dw2 (so bT = transposed dab gives
+ *   dW1 and dW3 in their logical layouts). An expert with no rows gets zeros.
+ *   Requires M % 128 == 0, N % 256 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_prepare_weights_bwd(const void *w1, const void *w3, const void *w2, int E, int H, int F,
+                                   moe_dtype dtype, void *w2_bwd, uint8_t *w2_bwd_scales,
+                                   void *w13t, uint8_t *w13t_scales, moe_stream_t stream);
+
+moe_status moe_grouped_swiglu_dgrad(const void *dy, const uint8_t *dy_scales, const void *w2_bwd,
+                                    const uint8_t *w2_bwd_scales, const void *ab, moe_dtype dtype,
+                                    const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                                    void *dab, moe_stream_t stream);
+
+moe_status moe_grouped_gemm_dx(const void *dab, const uint8_t *dab_scales, const void *w13t,
+                               const uint8_t *w13t_scales, moe_dtype dtype,
+                               const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                               void *dx, moe_stream_t stream);
+
+size_t moe_grouped_transpose_kpad(int R_cap, int E);
+
+moe_status moe_grouped_transpose(const void *x, const int32_t *src_rows, int R_cap, int C,
+                                 const int32_t *group_offsets, int E, moe_dtype out_dtype,
+                                 void *xT, uint8_t *xT_scales, moe_stream_t stream);
+
+moe_status moe_grouped_gemm_wgrad(const void *aT, const uint8_t *aT_scales, const void *bT,
+                                  const uint8_t *bT_scales, moe_dtype dtype,
+                                  const int32_t *group_offsets, int E, int M, int N, int R_cap,
+                                  void *dw, void *dw2, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Unpermute / combine ([TEJAX] "Optimization 2": results are routed back and
