@@ -41,6 +41,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s; grouped-GEMM TFLOPS and permute/combine GB/s vs peak"
+KERNEL_NAMES = {"gemm_up": "grouped_gemm_kernel<UP> (GEMM up + SwiGLU)",
+                "gemm_down": "grouped_gemm_kernel<DOWN> (GEMM down)",
+                "dgrad_dh": "grouped_gemm_kernel<DGRAD> (dh + SwiGLU backward)"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from an ncu capture,
@@ -173,29 +176,42 @@ def oracle_inputs(wl):
 def run_ours(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
+    from dropless_moe_expert_router_gb300 import api
     from dropless_moe_expert_router_gb300 import workloads as W
     from dropless_moe_expert_router_gb300.layer import MoELayer
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    torch.backends.cuda.matmul.allow_tf32 = False
     w1, w3, w2 = W.weights(wl, seed=0)                      # replicas hold the same layer
     x = W.x(wl, seed=rank).to(dev)                          # each rank its own batch
     logits = W.logits(wl, seed=rank).to(dev)
     layer = MoELayer(w1.to(dev), w3.to(dev), w2.to(dev), T=wl.T, K=wl.K, precision=wl.precision,
-                     renorm=wl.renorm, id_dtype=torch.int16 if wl.id_bits == 16 else torch.int32)
+                     renorm=wl.renorm, id_dtype=torch.int16 if wl.id_bits == 16 else torch.int32,
+                     training=wl.backward)
     del w1, w3, w2
+    dy = W.dy_perm(wl, seed=rank).to(dev) if wl.backward else None
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    stages = [("route", lambda: layer.stage_route(logits)), ("permute", lambda: layer.stage_permute(x)),
+              ("gemm_up", layer.stage_gemm_up), ("gemm_down", layer.stage_gemm_down),
+              ("combine", layer.stage_combine)]
+    if wl.backward:
+        stages += [("dgrad_dh", lambda: layer.stage_dgrad_dh(dy)), ("dgrad_dx", layer.stage_dgrad_dx),
+                   ("wgrad_transpose", lambda: layer.stage_transposes(x, dy)), ("wgrad_gemm", layer.stage_wgrad_gemm)]
+
+    def step():
+        for _, fn in stages:
+            fn()
+
     for _ in range(args.warmup):
-        layer.forward(x, logits)
+        step()
     torch.cuda.synchronize()
-    from dropless_moe_expert_router_gb300 import api
     assert api.moe_get_device_errors() == 0, "device error during warm-up"
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    ns = len(stages)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(local_rank))
     sampler.start()
     time.sleep(0.2)
@@ -206,29 +222,30 @@ def run_ours(args, wl, rank, world, local_rank):
         flush.zero_()                                       # L2 flush, outside the timed interval
         e = ev[i]
         e[0].record(stream)
-        layer.stage_route(logits)
-        e[1].record(stream)
-        layer.stage_permute(x)
-        e[2].record(stream)
-        layer.stage_gemm_up()
-        e[3].record(stream)
-        layer.stage_gemm_down()
-        e[4].record(stream)
-        layer.stage_combine()
-        e[5].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            e[j + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][5]) for i in range(K)]
-    stage_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(5)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][ns]) for i in range(K)]
+    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+                for j, (name, _) in enumerate(stages)}
     total_ms = sum(step_ms)
 
-    # end to end through the host-memory call
+    # end to end through the host-memory call: x and logits in, y out (for the training
+    # workload dy_perm stays on the device, where the next layer's backward produces it)
     x_host = W.x(wl, seed=rank).pin_memory()
     lg_host = W.logits(wl, seed=rank).pin_memory()
     y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    for _ in range(max(2, args.warmup // 2)):
+
+    def e2e_step():
         layer.forward_host(x_host, lg_host, y_host)
+        if wl.backward:
+            layer.backward(layer.x_dev, dy)
+
+    for _ in range(max(2, args.warmup // 2)):
+        e2e_step()
     torch.cuda.synchronize()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
@@ -237,49 +254,47 @@ def run_ours(args, wl, rank, world, local_rank):
     for i in range(K):
         flush.zero_()
         e2e_ev[i][0].record(stream)
-        layer.forward_host(x_host, lg_host, y_host)
+        e2e_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     errs = api.moe_get_device_errors()
     R = int(layer.perm.group_offsets[-1].item())
+    launches = MoELayer.LAUNCHES_PER_FORWARD + (layer.launches_per_backward if wl.backward else 0)
 
     if world > 1:
         t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms, e2e_ms = float(t[0]), float(t[1])
     return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, clocks=clocks, R=R, errs=errs,
-                h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2,
-                launches=K * layer.LAUNCHES_PER_FORWARD)
+                h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2, launches=K * launches)
 
 
 def stage_report(wl, R, stage_ms):
     """Algorithmic bytes / FLOPs of each stage (minimum traffic, not counters)."""
     T, H, E, K, F = wl.T, wl.H, wl.E, wl.K, wl.F
     idb = 2 if wl.id_bits == 16 else 4
-    b_out = 1 if wl.precision == "mxfp8" else 2
-    route_b = T * E * 4 + T * K * (idb + 4)
-    perm_b = T * H * 2 + R * H * b_out + (R * H // 32 if wl.precision == "mxfp8" else 0) + T * K * (idb + 4) + R * 4
-    comb_b = R * H * 2 + T * K * 8 + T * H * 2
-    up_f = 4.0 * R * H * F
-    down_f = 2.0 * R * H * F
-    names = ["route", "permute", "gemm_up", "gemm_down", "combine"]
+    fp8 = wl.precision == "mxfp8"
+    b_out = 1 if fp8 else 2
+    bytes_ = {
+        "route": T * E * 4 + T * K * (idb + 4),
+        "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
+        "combine": R * H * 2 + T * K * 8 + T * H * 2,
+        # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands
+        "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
+    }
+    flops = {"gemm_up": 4.0 * R * H * F, "gemm_down": 2.0 * R * H * F, "dgrad_dh": 2.0 * R * H * F,
+             "dgrad_dx": 4.0 * R * H * F, "wgrad_gemm": 6.0 * R * H * F}
     out = {}
-    for n, ms in zip(names, stage_ms):
+    for n, ms in stage_ms.items():
         d = {"us": round(ms * 1e3, 2)}
-        if n == "route":
-            d["GB/s"] = round(route_b / (ms * 1e-3) / 1e9, 1)
-        elif n == "permute":
-            d["GB/s"] = round(perm_b / (ms * 1e-3) / 1e9, 1)
-        elif n == "combine":
-            d["GB/s"] = round(comb_b / (ms * 1e-3) / 1e9, 1)
-        elif n == "gemm_up":
-            d["TFLOP/s"] = round(up_f / (ms * 1e-3) / 1e12, 1)
-        else:
-            d["TFLOP/s"] = round(down_f / (ms * 1e-3) / 1e12, 1)
+        if n in bytes_:
+            d["GB/s"] = round(bytes_[n] / (ms * 1e-3) / 1e9, 1)
+        if n in flops:
+            d["TFLOP/s"] = round(flops[n] / (ms * 1e-3) / 1e12, 1)
         out[n] = d
-    return out, up_f
+    return out, flops
 
 
 def main():
@@ -340,16 +355,18 @@ def main():
 
     r = run_ours(args, wl, rank, world, local_rank)
     peaks, peak_kind = load_peaks()
-    stages, up_flops = stage_report(wl, r["R"], r["stage_ms"])
-    up_ms = r["stage_ms"][2]
-    achieved = up_flops / (up_ms * 1e-3) / 1e12
+    stages, flops = stage_report(wl, r["R"], r["stage_ms"])
+    # dominant kernel: the GEMM stage with the largest time (one kernel launch per stage)
+    dom = max((n for n in flops if n in r["stage_ms"] and n != "wgrad_gemm" and n != "dgrad_dx"),
+              key=lambda n: r["stage_ms"][n])
+    achieved = flops[dom] / (r["stage_ms"][dom] * 1e-3) / 1e12
     fp8_ratio = 2.0 if wl.precision == "mxfp8" else 1.0
     # The timed loop is well under a second and the SM clock stays at its maximum
     # (see "clocks"), the conditions of the burst measurement: report against the
     # burst peak, and the sustained figure beside it.
     peak = peaks["bf16_tflops"] * fp8_ratio
     peak_sustained = peaks["bf16_tflops_sustained"] * fp8_ratio
-    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash())
+    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash()) if (wl.name == "mixtral" and dom == "gemm_up") else None
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -364,7 +381,7 @@ def main():
         "e2e": {"value": world * wl.T * args.steps / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
-        "roofline": {"kernel": "grouped_gemm_kernel<swiglu> (GEMM up + SwiGLU)", "bound": "tensor",
+        "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "tensor",
                      "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,

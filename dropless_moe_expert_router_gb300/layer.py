@@ -19,14 +19,17 @@ from . import _lib, api
 
 class MoELayer:
     def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, *, T: int, K: int,
-                 precision: str = "bf16", renorm: bool = False, id_dtype=torch.int32, stream=None):
+                 precision: str = "bf16", renorm: bool = False, id_dtype=torch.int32, training: bool = False,
+                 stream=None):
         E, H, F = w1.shape
         self.E, self.H, self.F, self.T, self.K = E, H, F, T, K
         self.precision = precision
         self.renorm = renorm
         self.fp8 = precision == "mxfp8"
+        self.training = training
         dev = w1.device
         self.weights = api.moe_prepare_weights(w1, w3, w2, precision, stream=stream)
+        self.bwd_weights = api.moe_prepare_weights_bwd(w1, w3, w2, precision, stream=stream) if training else None
         R_cap = T * K
         self.R_cap = R_cap
         self.ids = torch.empty((T, K), dtype=id_dtype, device=dev)
@@ -40,6 +43,27 @@ class MoELayer:
         self.x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.logits_dev = torch.empty((T, E), dtype=torch.float32, device=dev)
         self._lib = _lib.load()
+        if training:
+            bf = torch.bfloat16
+            kpad = api.moe_grouped_transpose_kpad(R_cap, E)
+            self.ab = torch.empty((R_cap, 2 * F), dtype=bf, device=dev)
+            self.h_bf16 = torch.empty((R_cap, F), dtype=bf, device=dev) if self.fp8 else None
+            self.dab = torch.empty((R_cap, 2 * F), dtype=bf, device=dev)
+            self.dx = torch.empty((R_cap, H), dtype=bf, device=dev)
+            u8 = torch.uint8
+            self.dy_q = torch.empty((R_cap, H), dtype=u8, device=dev) if self.fp8 else None
+            self.dy_s = torch.empty((R_cap, H // 32), dtype=u8, device=dev) if self.fp8 else None
+            self.dab_q = torch.empty((R_cap, 2 * F), dtype=u8, device=dev) if self.fp8 else None
+            self.dab_s = torch.empty((R_cap, 2 * F // 32), dtype=u8, device=dev) if self.fp8 else None
+            tdt = u8 if self.fp8 else bf
+
+            def tbuf(C):
+                return (torch.empty((C, kpad), dtype=tdt, device=dev),
+                        torch.empty((C, kpad // 32), dtype=u8, device=dev) if self.fp8 else None)
+            self.hT, self.dyT, self.xT, self.dabT = tbuf(F), tbuf(H), tbuf(H), tbuf(2 * F)
+            self.dW1 = torch.empty((E, H, F), dtype=bf, device=dev)
+            self.dW3 = torch.empty((E, H, F), dtype=bf, device=dev)
+            self.dW2 = torch.empty((E, F, H), dtype=bf, device=dev)
 
     # number of library kernel launches one forward enqueues
     LAUNCHES_PER_FORWARD = 7   # router 1, permute 3 (rank, scan, scatter), GEMM 2, combine 1
@@ -53,10 +77,13 @@ class MoELayer:
 
     def stage_gemm_up(self, stream=None):
         w = self.weights
+        ab = self.ab if self.training else None
+        hb = self.h_bf16 if self.training else None
         st = self._lib.moe_grouped_gemm_up(
             api._ptr(self.perm.x_perm), api._ptr(self.perm.x_perm_scales), api._ptr(w.w13),
             api._ptr(w.w13_scales), api._dt_code(w.precision), api._ptr(self.perm.group_offsets), w.E, w.H,
-            w.F, self.R_cap, api._ptr(self.h), api._ptr(self.h_scales), None, None, api._stream(stream))
+            w.F, self.R_cap, api._ptr(self.h), api._ptr(self.h_scales), api._ptr(ab), api._ptr(hb),
+            api._stream(stream))
         api._check("moe_grouped_gemm_up", st)
 
     def stage_gemm_down(self, stream=None):
@@ -78,6 +105,62 @@ class MoELayer:
         self.stage_gemm_down(stream)
         self.stage_combine(stream)
         return self.y
+
+    # ------------------------------------------------------------ backward
+    # library launches of one backward: dgrad 1, dx 1, transposes 4, wgrad 2 (+ 2 quantisations for MXFP8)
+    @property
+    def launches_per_backward(self) -> int:
+        return 8 + (2 if self.fp8 else 0)
+
+    def stage_dgrad_dh(self, dy_perm: torch.Tensor, stream=None):
+        """dy_perm [R_cap, H] bf16 -> dab = SwiGLU backward of dh = dy W2^T (bf16)."""
+        goff = self.perm.group_offsets
+        bw = self.bwd_weights
+        if self.fp8:
+            api.moe_quant_mxfp8_grouped(dy_perm, goff, q=self.dy_q, scales=self.dy_s, stream=stream)
+            api.moe_grouped_swiglu_dgrad(self.dy_q, self.dy_s, bw, self.ab, goff, dab=self.dab, stream=stream)
+        else:
+            api.moe_grouped_swiglu_dgrad(dy_perm, None, bw, self.ab, goff, dab=self.dab, stream=stream)
+
+    def stage_dgrad_dx(self, stream=None):
+        """dab -> dx = da W1^T + db W3^T [R_cap, H] bf16."""
+        goff = self.perm.group_offsets
+        bw = self.bwd_weights
+        if self.fp8:
+            api.moe_quant_mxfp8_grouped(self.dab, goff, q=self.dab_q, scales=self.dab_s, stream=stream)
+            api.moe_grouped_gemm_dx(self.dab_q, self.dab_s, bw, goff, dx=self.dx, stream=stream)
+        else:
+            api.moe_grouped_gemm_dx(self.dab, None, bw, goff, dx=self.dx, stream=stream)
+        return self.dx
+
+    def stage_transposes(self, x: torch.Tensor, dy_perm: torch.Tensor, stream=None):
+        """Group-padded transposed (and, for MXFP8, column-quantised) weight-gradient operands."""
+        goff = self.perm.group_offsets
+        prec = self.precision
+        h_src = self.h_bf16 if self.fp8 else self.h
+        api.moe_grouped_transpose(h_src, goff, prec, xT=self.hT[0], xT_scales=self.hT[1], stream=stream)
+        api.moe_grouped_transpose(dy_perm, goff, prec, xT=self.dyT[0], xT_scales=self.dyT[1], stream=stream)
+        api.moe_grouped_transpose(x, goff, prec, R_cap=self.R_cap, src_rows=self.perm.perm_src, xT=self.xT[0],
+                                  xT_scales=self.xT[1], stream=stream)
+        api.moe_grouped_transpose(self.dab, goff, prec, xT=self.dabT[0], xT_scales=self.dabT[1], stream=stream)
+
+    def stage_wgrad_gemm(self, stream=None):
+        """dW2 = h^T dy, dW1 = x^T da, dW3 = x^T db per expert."""
+        goff = self.perm.group_offsets
+        prec = self.precision
+        api.moe_grouped_gemm_wgrad(self.hT[0], self.hT[1], self.dyT[0], self.dyT[1], prec, goff, self.R_cap,
+                                   dw=self.dW2, stream=stream)
+        api.moe_grouped_gemm_wgrad(self.xT[0], self.xT[1], self.dabT[0], self.dabT[1], prec, goff, self.R_cap,
+                                   split=True, dw=self.dW1, dw2=self.dW3, stream=stream)
+        return self.dW1, self.dW3, self.dW2
+
+    def backward(self, x: torch.Tensor, dy_perm: torch.Tensor, stream=None):
+        """Grouped backward of the expert MLP after a training forward (x: the forward's tokens,
+        dy_perm: gradient of y_perm) -> (dx_perm, dW1, dW3, dW2)."""
+        self.stage_dgrad_dh(dy_perm, stream)
+        dx = self.stage_dgrad_dx(stream)
+        self.stage_transposes(x, dy_perm, stream)
+        return (dx,) + tuple(self.stage_wgrad_gemm(stream))
 
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor,
                      stream=None) -> torch.Tensor:
