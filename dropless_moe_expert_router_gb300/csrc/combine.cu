@@ -14,9 +14,8 @@
 namespace moe {
 namespace {
 
-constexpr int CHUNKS = 2;  // 16-byte chunks in flight per lane and route
-
-template <int KC>
+// KC * 32 route slots per token, CHUNKS 16-byte chunks in flight per lane and route
+template <int KC, int CHUNKS>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
                                                       const int* __restrict__ row_map,
                                                       const float* __restrict__ probs, int T, int K, int H,
@@ -99,11 +98,18 @@ extern "C" moe_status moe_unpermute_combine(const void* y_perm, const int32_t* r
     if (blocks > cap) blocks = cap;
     cudaStream_t s = moe_host::as_stream(stream);
     const int KC = (K + 31) / 32;
-    if (KC == 1)
-        combine_kernel<1><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
-    else if (KC == 2)
-        combine_kernel<2><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
-    else
-        combine_kernel<4><<<(int)blocks, 256, 0, s>>>((const uint4*)y_perm, row_map, probs, T, K, H, (uint4*)y);
+    const int H8 = H / 8;
+    const int CH = H8 >= 128 ? 4 : (H8 >= 64 ? 2 : 1);  // no more chunks than a row has per lane
+    const uint4* yp = (const uint4*)y_perm;
+    uint4* yo = (uint4*)y;
+#define MOE_COMBINE(kc, ch) combine_kernel<kc, ch><<<(int)blocks, 256, 0, s>>>(yp, row_map, probs, T, K, H, yo)
+    if (KC == 1) {
+        if (CH == 4) MOE_COMBINE(1, 4); else if (CH == 2) MOE_COMBINE(1, 2); else MOE_COMBINE(1, 1);
+    } else if (KC == 2) {
+        if (CH == 4) MOE_COMBINE(2, 4); else if (CH == 2) MOE_COMBINE(2, 2); else MOE_COMBINE(2, 1);
+    } else {
+        if (CH == 4) MOE_COMBINE(4, 4); else if (CH == 2) MOE_COMBINE(4, 2); else MOE_COMBINE(4, 1);
+    }
+#undef MOE_COMBINE
     return moe_host::launch_status();
 }

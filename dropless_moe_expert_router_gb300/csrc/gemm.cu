@@ -27,11 +27,12 @@
 // Design (one CTA per SM, persistent, warp-specialised; 192 threads):
 //   warp 0     TMA producer: A tile [128 rows x 128 B] and B tile [256 rows x 128 B]
 //              per k-block into a 4-stage shared-memory ring (128-byte swizzle);
-//              MXFP8 adds the E8M0 scale words of the k-block (cp.async straight
-//              into the layout tcgen05.cp expects).
+//              MXFP8 adds one TMA box of 16 E8M0 scale bytes per A and B row.
 //   warp 1     allocates TMEM and issues tcgen05.mma (M=128, N=256) from one
 //              lane; each k-block's commit frees its ring stage, each tile's
-//              commit hands the accumulator to the epilogue.
+//              commit hands the accumulator to the epilogue. For MXFP8 the warp
+//              first rearranges the k-block's scale words into the layout
+//              tcgen05.cp expects and copies them to TMEM.
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns the
 //              32 TMEM lanes of its quarter) and the mode's store.
 // Tiles are scheduled on the device: every CTA reads group_offsets and walks
@@ -71,8 +72,10 @@ struct Cfg {
     static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per k-block (4)
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN * 128;
-    static constexpr int SFA_BYTES = FP8 ? BM * 4 : 0;   // one 32-bit word (4 scales) per row
-    static constexpr int SFB_BYTES = FP8 ? BN * 4 : 0;
+    // scale landing zones: a TMA box of 16 scale bytes (four k-blocks) per operand row;
+    // the k-block's 32-bit word is then rearranged in place for tcgen05.cp
+    static constexpr int SFA_BYTES = FP8 ? BM * 16 : 0;
+    static constexpr int SFB_BYTES = FP8 ? BN * 16 : 0;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int ACC_STAGES = FP8 ? 1 : 2;
     static constexpr int SF_COLS = 12;              // TMEM columns of one stage's scales (4 A + 8 B)
@@ -162,6 +165,18 @@ __device__ __forceinline__ TileInfo decode(int tile, const int* s_mtp, const int
     else return decode_rows<FP8>(tile, s_mtp, s_goff, p);
 }
 
+// First contraction element of a tile, in units of 128 elements (WGRAD: the
+// expert's padded start; row-grouped modes: 0).
+template <int MODE>
+__device__ __forceinline__ int tile_k0_div128(const GemmArgs& p, int tile, const int* s_goff) {
+    if constexpr (MODE == MODE_WGRAD) {
+        const int e = tile / (p.m_tiles * p.n_tiles);
+        return e + s_goff[e] / 128;
+    } else {
+        return 0;
+    }
+}
+
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -185,17 +200,10 @@ __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
     for (int i = 0; i < 4; i++) bf16x8_to_f32(s[i], v + 8 * i);
 }
 
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
-}
-
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs p) {
     using C = Cfg<FP8>;
     extern __shared__ uint8_t smem_raw[];
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
-            ptx::mbar_init(&full[s], FP8 ? 1 + 32 : 1);
+            ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; a++) {
@@ -232,6 +240,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if constexpr (FP8) {
+            ptx::prefetch_tmap(&tmSA);
+            ptx::prefetch_tmap(&tmSB);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(s_tmem, TMEM_COLS);
@@ -290,32 +302,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint8_t* sb = sa + C::A_BYTES;
                 const int k = ti.k0 + kb * C::BK;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+                    ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     ptx::tma_load_2d(sa, &tmA, &full[stage], k, ti.a_row);
                     ptx::tma_load_2d(sb, &tmB, &full[stage], k, ti.b_row);
-                }
-                if constexpr (FP8) {
-                    // scale words of this k-block, transposed for tcgen05.cp .32x128b:
-                    // word (lane*4 + j) of a 512-byte chunk holds row 32*j + lane of the chunk
-                    const uint32_t sfa = ptx::smem_addr(sb + C::B_BYTES);
-                    const uint32_t sfb = sfa + C::SFA_BYTES;
-                    const int kw = k / 32;  // first scale byte of the k-block (multiple of 4)
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const int r = ti.a_row + 32 * j + lane;
-                        const bool v = MODE == MODE_WGRAD || r < p.R_cap;
-                        cp_async_4(sfa + (lane * 4 + j) * 4,
-                                   p.a_scales + (size_t)(v ? r : 0) * p.sf_row_bytes + kw, v);
+                    if constexpr (FP8) {
+                        // 16 scale bytes per row (the 16-byte aligned group of four k-blocks holding this one)
+                        const int kx = (k / 32) & ~15;
+                        ptx::tma_load_2d(sb + C::B_BYTES, &tmSA, &full[stage], kx, ti.a_row);
+                        ptx::tma_load_2d(sb + C::B_BYTES + C::SFA_BYTES, &tmSB, &full[stage], kx, ti.b_row);
                     }
-#pragma unroll
-                    for (int c = 0; c < 2; c++)
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const int r = ti.b_row + 128 * c + 32 * j + lane;
-                            cp_async_4(sfb + c * 512 + (lane * 4 + j) * 4,
-                                       p.b_scales + (size_t)r * p.sf_row_bytes + kw, true);
-                        }
-                    cp_async_arrive_noinc(&full[stage]);
                 }
                 __syncwarp();
                 issued++;
@@ -345,12 +340,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < nkb; kb++) {
                 if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
                 ptx::tc_fence_after();
+                uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
+                uint8_t* sb = sa + C::A_BYTES;
+                if constexpr (FP8) {
+                    // Rearrange this k-block's scale words for tcgen05.cp .32x128b: word (lane*4 + j)
+                    // of a 512-byte chunk must hold row 32*j + lane of that chunk. The landing zone
+                    // holds 16 bytes (four k-blocks) per row; read everything, then write in place.
+                    const int w = ((tile_k0_div128<MODE>(p, tile, s_goff) + kb) & 3);
+                    const uint32_t* la = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES);
+                    const uint32_t* lb = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES + C::SFA_BYTES);
+                    uint32_t va[4], vb0[4], vb1[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        va[j] = la[(32 * j + lane) * 4 + w];
+                        vb0[j] = lb[(32 * j + lane) * 4 + w];
+                        vb1[j] = lb[(128 + 32 * j + lane) * 4 + w];
+                    }
+                    __syncwarp();
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES)[lane] = make_uint4(va[0], va[1], va[2], va[3]);
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES)[lane] =
+                        make_uint4(vb0[0], vb0[1], vb0[2], vb0[3]);
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES + 512)[lane] =
+                        make_uint4(vb1[0], vb1[1], vb1[2], vb1[3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 if (lane == 0) {
-                    uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
-                    uint8_t* sb = sa + C::A_BYTES;
                     const uint32_t a0 = ptx::smem_addr(sa), b0 = ptx::smem_addr(sb);
                     if constexpr (FP8) {
-                        ptx::fence_proxy_async_smem();
                         const uint32_t sf_t = tmem + (uint32_t)(BN + stage * C::SF_COLS);
                         const uint32_t sfa_s = ptx::smem_addr(sb + C::B_BYTES);
                         ptx::tc_cp_32x128b_warpx4(sf_t, ptx::sdesc_plain(sfa_s));
@@ -547,18 +564,39 @@ int device_sms() {
     return sms;
 }
 
+// MXFP8 scales [rows][row_bytes] (bytes), box {16 bytes, box_rows}, no swizzle.
+bool make_scale_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {16u, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // A: [a_rows][a_inner], B: [b_rows][a_inner], both K-major.
 template <int MODE, bool FP8>
 moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
                        const GemmArgs& a, cudaStream_t s) {
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmSA, tmSB;
     if (!make_operand_map(&tmA, A, FP8, inner, a_rows, BM)) return MOE_ERR_CUDA;
     if (!make_operand_map(&tmB, B, FP8, inner, b_rows, BN)) return MOE_ERR_CUDA;
+    if (FP8) {
+        if (!make_scale_map(&tmSA, a.a_scales, (uint64_t)a.sf_row_bytes, a_rows, BM)) return MOE_ERR_CUDA;
+        if (!make_scale_map(&tmSB, a.b_scales, (uint64_t)a.sf_row_bytes, b_rows, BN)) return MOE_ERR_CUDA;
+    } else {
+        tmSA = tmA;
+        tmSB = tmB;
+    }
     const size_t smem = smem_bytes_for<FP8>(a.E);
     if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
-    grouped_gemm_kernel<MODE, FP8><<<device_sms(), NUM_THREADS, smem, s>>>(tmA, tmB, a);
+    grouped_gemm_kernel<MODE, FP8><<<device_sms(), NUM_THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);
     return moe_host::launch_status();
 }
 
@@ -573,7 +611,10 @@ moe_status check_common(moe_dtype dtype, const int32_t* group_offsets, int E, in
     if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
     if (E < 1 || H < 128 || F < 128 || R_cap < 0 || !group_offsets) return MOE_ERR_INVALID_ARG;
     if ((H % 256) || (F % 128)) return MOE_ERR_UNSUPPORTED;
-    if (smem_bytes_for<true>(E) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    // MXFP8: a row of scales of every contraction (H, F, 2F) is a whole number of 16-byte TMA boxes
+    if (dtype == MOE_MXFP8 && ((H % 512) || (F % 512))) return MOE_ERR_UNSUPPORTED;
+    if ((dtype == MOE_MXFP8 ? smem_bytes_for<true>(E) : smem_bytes_for<false>(E)) > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
     if ((long long)E * 2 * F > 0x7fffffffLL || (long long)E * H > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
     if ((long long)R_cap * 2 * F > 0x7fffffffffffLL) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
@@ -599,7 +640,7 @@ extern "C" moe_status moe_grouped_gemm_up(const void* x_perm, const uint8_t* x_s
     if (!x_perm || !w13_packed || !h || (fp8 && (!x_scales || !w13_scales || !h_scales))) return MOE_ERR_INVALID_ARG;
     if (h_bf16_save && !fp8) return MOE_ERR_INVALID_ARG;
     if (!al(x_perm, 128) || !al(w13_packed, 128) || !al(h, 16) || !al(ab_save, 16) || !al(h_bf16_save, 16) ||
-        (fp8 && (!al(x_scales, 4) || !al(w13_scales, 4))))
+        (fp8 && (!al(x_scales, 16) || !al(w13_scales, 16))))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;
@@ -629,7 +670,7 @@ static moe_status grouped_down(const void* A, const uint8_t* a_scales, const voi
     if (R_cap == 0) return MOE_OK;
     const bool fp8 = dtype == MOE_MXFP8;
     if (!A || !B || !out || (fp8 && (!a_scales || !b_scales))) return MOE_ERR_INVALID_ARG;
-    if (!al(A, 128) || !al(B, 128) || !al(out, 16) || (fp8 && (!al(a_scales, 4) || !al(b_scales, 4))))
+    if (!al(A, 128) || !al(B, 128) || !al(out, 16) || (fp8 && (!al(a_scales, 16) || !al(b_scales, 16))))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;
@@ -680,7 +721,7 @@ extern "C" moe_status moe_grouped_swiglu_dgrad(const void* dy, const uint8_t* dy
     const bool fp8 = dtype == MOE_MXFP8;
     if (!dy || !w2_bwd || !ab || !dab || (fp8 && (!dy_scales || !w2_bwd_scales))) return MOE_ERR_INVALID_ARG;
     if (!al(dy, 128) || !al(w2_bwd, 128) || !al(ab, 16) || !al(dab, 16) ||
-        (fp8 && (!al(dy_scales, 4) || !al(w2_bwd_scales, 4))))
+        (fp8 && (!al(dy_scales, 16) || !al(w2_bwd_scales, 16))))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;
@@ -709,7 +750,8 @@ extern "C" moe_status moe_grouped_gemm_dx(const void* dab, const uint8_t* dab_sc
 
 extern "C" size_t moe_grouped_transpose_kpad(int R_cap, int E) {
     if (R_cap < 0 || E < 1) return 0;
-    return (size_t)128 * ((size_t)E + ((size_t)R_cap + 127) / 128 + 1);
+    const size_t k = (size_t)128 * ((size_t)E + ((size_t)R_cap + 127) / 128 + 1);
+    return (k + 511) / 512 * 512;  // MXFP8 scale rows of whole 16-byte TMA boxes
 }
 
 extern "C" moe_status moe_grouped_gemm_wgrad(const void* aT, const uint8_t* aT_scales, const void* bT,
@@ -720,13 +762,14 @@ extern "C" moe_status moe_grouped_gemm_wgrad(const void* aT, const uint8_t* aT_s
     if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
     if (E < 1 || M < BM || N < BN || R_cap < 0 || !group_offsets) return MOE_ERR_INVALID_ARG;
     if ((M % BM) || (N % BN)) return MOE_ERR_UNSUPPORTED;
-    if (smem_bytes_for<true>(E) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    if ((dtype == MOE_MXFP8 ? smem_bytes_for<true>(E) : smem_bytes_for<false>(E)) > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
     const size_t kpad = moe_grouped_transpose_kpad(R_cap, E);
     if (kpad > 0x7fffffffULL || (long long)E * M > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
     const bool fp8 = dtype == MOE_MXFP8;
     if (!aT || !bT || !dw || (fp8 && (!aT_scales || !bT_scales))) return MOE_ERR_INVALID_ARG;
     if (!al(aT, 128) || !al(bT, 128) || !al(dw, 16) || !al(dw2, 16) ||
-        (fp8 && (!al(aT_scales, 4) || !al(bT_scales, 4))))
+        (fp8 && (!al(aT_scales, 16) || !al(bT_scales, 16))))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;

@@ -192,36 +192,56 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
             mask[c] = __ballot_sync(FULL, r >= 0);
         }
         const uint4* src = x + t * H8;
-        for (int it = 0; it < iters; it++) {
-            const int j = it * 32 + lane;
-            const bool in = j < H8;
-            uint4 v = in ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+        // U 16-byte chunks per lane in flight before the stores (memory-level parallelism)
+        constexpr int U = 4;
+        for (int it0 = 0; it0 < iters; it0 += U) {
+            uint4 v[U];
+            bool in[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int j = (it0 + u) * 32 + lane;
+                in[u] = (it0 + u < iters) && j < H8;
+                v[u] = in[u] ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+            }
             if (!FUSE) {
 #pragma unroll
                 for (int c = 0; c < KC; c++) {
                     unsigned m = mask[c];
                     while (m) {
-                        int b = __ffs(m) - 1;
+                        const int b = __ffs(m) - 1;
                         m &= m - 1;
-                        int r = __shfl_sync(FULL, rows[c], b);
-                        if (in) reinterpret_cast<uint4*>(x_perm)[(long long)r * H8 + j] = v;
+                        const int r = __shfl_sync(FULL, rows[c], b);
+                        uint4* dst = reinterpret_cast<uint4*>(x_perm) + (long long)r * H8 + lane;
+#pragma unroll
+                        for (int u = 0; u < U; u++)
+                            if (in[u]) dst[(it0 + u) * 32] = v[u];
                     }
                 }
             } else {
-                float f[8];
-                bf16x8_to_f32(v, f);
-                int sb;
-                uint2 qv = quant8_in_quad(f, &sb);
+                uint2 qv[U];
+                int sb[U];
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    if (it0 + u < iters) {  // warp-uniform: the quad shuffles see every lane
+                        float f[8];
+                        bf16x8_to_f32(v[u], f);
+                        qv[u] = quant8_in_quad(f, &sb[u]);
+                    }
+                }
 #pragma unroll
                 for (int c = 0; c < KC; c++) {
                     unsigned m = mask[c];
                     while (m) {
-                        int b = __ffs(m) - 1;
+                        const int b = __ffs(m) - 1;
                         m &= m - 1;
-                        int r = __shfl_sync(FULL, rows[c], b);
-                        if (in) {
-                            reinterpret_cast<uint2*>(x_perm)[(long long)r * H8 + j] = qv;
-                            if ((lane & 3) == 0) scales[(long long)r * (H >> 5) + (j >> 2)] = (uint8_t)sb;
+                        const int r = __shfl_sync(FULL, rows[c], b);
+#pragma unroll
+                        for (int u = 0; u < U; u++) {
+                            if (in[u]) {
+                                const int j = (it0 + u) * 32 + lane;
+                                reinterpret_cast<uint2*>(x_perm)[(long long)r * H8 + j] = qv[u];
+                                if ((lane & 3) == 0) scales[(long long)r * (H >> 5) + (j >> 2)] = (uint8_t)sb[u];
+                            }
                         }
                     }
                 }

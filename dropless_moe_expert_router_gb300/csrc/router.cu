@@ -3,11 +3,12 @@
 // Two paths ("Sparser MoE end-to-end", section "Preserve a compact route"):
 //  * small E and K: a warp (or a group of G lanes of a warp) per row keeps the
 //    logits in registers and runs K rounds of a segmented arg-max;
-//  * large E and K (e.g. 2,304 experts, top-36): radix select -- three bounded
-//    histogram passes (11/11/10-bit digits of an order-preserving key) find the
-//    exact K-th largest key, only candidates matching the narrowed prefix are
-//    counted after the first pass, and the K winners are ranked in a final
-//    O(K^2 / 32) step instead of K full-row scans.
+//  * large E and K (e.g. 2,304 experts, top-36): radix/threshold select -- a
+//    bounded histogram pass over the top 11 bits of an order-preserving key
+//    finds the bin of the K-th largest key, the candidates in that bin are
+//    ranked directly (further 11- and 10-bit passes narrow the range only when
+//    the bin is crowded), and the K winners are ranked in a final step; no
+//    full-row scan per selected expert.
 // Output: ids [T, K] (selection order: descending logit, lower index on ties),
 // probs [T, K] fp32 (softmax over all E logits at the selected ids, or over the
 // K selected logits with MOE_ROUTE_RENORM).
@@ -18,7 +19,6 @@
 namespace moe {
 namespace {
 
-constexpr int RADIX_WARPS = 4;    // warps (rows in flight) per block of the radix kernel
 constexpr int KMAX = 128;         // largest K of the radix kernel (list in shared memory)
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -117,11 +117,6 @@ __global__ void __launch_bounds__(256) route_small_kernel(const float* __restric
     }
 }
 
-// ---------------------------------------------------------------------------
-// Radix path: one warp per row, V = ceil(E/32) logits per lane in registers
-// (expert index = i * 32 + lane, so every load is a coalesced 128-byte line).
-// ---------------------------------------------------------------------------
-
 // Order-preserving key: larger float -> larger unsigned; -0 and +0 map to one key.
 __device__ __forceinline__ unsigned f2key(float f) {
     unsigned u = __float_as_uint(f);
@@ -142,139 +137,215 @@ __device__ __forceinline__ unsigned suffix_sum(unsigned v, int lane) {
     return v;
 }
 
-// Find the bin holding the rem-th largest element of a histogram of nb bins
-// (nb = 2048 or 1024) in shared memory. Returns the bin; *above = number of
-// elements in higher bins.
-__device__ __forceinline__ int find_bin(const unsigned* hist, int nb, unsigned rem, int lane,
-                                        unsigned* above) {
-    const int per = nb / 32;                    // bins per lane at the first level
+// ---------------------------------------------------------------------------
+// Radix path, one CTA (256 threads) per row: V logits per thread, expert index
+// e = i * 256 + tid (coalesced loads). The first histogram pass (top 11 bits of
+// the key) finds the bin that holds the K-th largest key; the keys in that bin
+// (normally a few dozen) are compacted and ranked directly. Only if that bin
+// holds more than CAND_MAX keys do the next passes (11 and 10 bits) narrow it
+// further, down to the exact K-th key.
+// ---------------------------------------------------------------------------
+constexpr int RT = 256;           // threads per row
+constexpr int RW = RT / 32;       // warps per row
+constexpr int CAND_MAX = 256;     // candidates ranked directly
+
+struct RadixSmem {
+    unsigned hist[2048];          // skewed: bin d at (d % 8) * 256 + d / 8
+    unsigned cand_key[CAND_MAX];
+    int cand_idx[CAND_MAX];
+    unsigned list_key[KMAX];
+    int list_idx[KMAX];
+    float red[RW];
+    unsigned ured[RW];
+    int n_cand, n_list;
+    unsigned bin, above;
+};
+
+__device__ __forceinline__ float block_max(float v, RadixSmem& sm) {
+    v = warp_max(v);
+    __syncthreads();
+    if (lane_id() == 0) sm.red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = sm.red[0];
+#pragma unroll
+    for (int w = 1; w < RW; w++) r = fmaxf(r, sm.red[w]);
+    return r;
+}
+__device__ __forceinline__ float block_sum(float v, RadixSmem& sm) {
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane_id() == 0) sm.red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.0f;
+#pragma unroll
+    for (int w = 0; w < RW; w++) r += sm.red[w];
+    return r;
+}
+
+// One histogram pass over keys matching (key & pmask) == prefix, on the digit
+// (key >> sh) & (nb - 1); nb = 2048 or 1024. Sets sm.bin to the digit holding
+// the rem-th largest matching key and sm.above to the matching keys in higher
+// digits. Each thread owns nb / 256 consecutive digits.
+template <int V>
+__device__ void radix_pass(const unsigned (&key)[V], unsigned prefix, unsigned pmask, int sh, int nb,
+                           unsigned rem, RadixSmem& sm) {
+    const int tid = threadIdx.x, lane = (int)lane_id(), warp = tid >> 5;
+    const int per = nb / RT;                       // 8 or 4 digits per thread
+    const int pshift = per == 8 ? 3 : 2;
+    for (int b = tid; b < nb; b += RT) sm.hist[b] = 0u;
+    __syncthreads();
+    const unsigned dmask = (unsigned)nb - 1u;
+#pragma unroll
+    for (int i = 0; i < V; i++)
+        if (key[i] != 0u && (key[i] & pmask) == prefix) {
+            const int d = (int)((key[i] >> sh) & dmask);
+            atomicAdd(&sm.hist[((d & (per - 1)) << 8) + (d >> pshift)], 1u);
+        }
+    __syncthreads();
     unsigned s = 0;
-    for (int j = 0; j < per; j++) s += hist[lane * per + j];
+    for (int j = 0; j < per; j++) s += sm.hist[j * RT + tid];
+    // block suffix sum over threads (thread t: sum of threads >= t)
     unsigned suf = suffix_sum(s, lane);
-    unsigned nxt = __shfl_down_sync(FULL, suf, 1);
-    if (lane == 31) nxt = 0;
-    int L = __ffs(__ballot_sync(FULL, suf >= rem && nxt < rem)) - 1;
-    unsigned aboveL = __shfl_sync(FULL, nxt, L);
-    // second level: lane L's `per` bins, per/32 to a lane
-    const int q = per / 32;
-    unsigned s2 = 0;
-    for (int j = 0; j < q; j++) s2 += hist[L * per + lane * q + j];
-    unsigned suf2 = suffix_sum(s2, lane);
-    unsigned nxt2 = __shfl_down_sync(FULL, suf2, 1);
-    if (lane == 31) nxt2 = 0;
-    int L2 = __ffs(__ballot_sync(FULL, aboveL + suf2 >= rem && aboveL + nxt2 < rem)) - 1;
-    unsigned acc = aboveL + __shfl_sync(FULL, nxt2, L2);
-    int base = L * per + L2 * q;
-    int bin = base;
-    for (int j = q - 1; j >= 0; j--) {
-        unsigned c = hist[base + j];
-        if (acc + c >= rem) { bin = base + j; break; }
-        acc += c;
+    if (lane == 0) sm.ured[warp] = suf;             // warp total
+    __syncthreads();
+    unsigned later = 0;
+    for (int w = warp + 1; w < RW; w++) later += sm.ured[w];
+    suf += later;
+    const unsigned nxt = suf - s;                   // sum of threads > t
+    if (suf >= rem && nxt < rem) {                  // exactly one thread
+        unsigned acc = nxt;
+        int d = tid * per;
+        for (int j = per - 1; j >= 0; j--) {
+            const unsigned c = sm.hist[j * RT + tid];
+            if (acc + c >= rem) { d = tid * per + j; break; }
+            acc += c;
+        }
+        sm.bin = (unsigned)d;
+        sm.above = acc;
     }
-    *above = acc;
-    return bin;
+    __syncthreads();
 }
 
 template <int V>
-__global__ void __launch_bounds__(RADIX_WARPS * 32) route_radix_kernel(const float* __restrict__ logits,
-                                                                       int T, int E, int K, void* ids,
-                                                                       bool i16, float* __restrict__ probs,
-                                                                       bool renorm) {
-    __shared__ unsigned s_hist[RADIX_WARPS][2048];
-    __shared__ unsigned s_key[RADIX_WARPS][KMAX];
-    __shared__ int s_idx[RADIX_WARPS][KMAX];
-    const int warp = threadIdx.x >> 5;
-    const int lane = (int)lane_id();
-    unsigned* hist = s_hist[warp];
-    unsigned* lkey = s_key[warp];
-    int* lidx = s_idx[warp];
-
-    for (long long t = (long long)blockIdx.x * RADIX_WARPS + warp; t < T;
-         t += (long long)gridDim.x * RADIX_WARPS) {
+__global__ void __launch_bounds__(RT) route_radix_kernel(const float* __restrict__ logits, int T, int E, int K,
+                                                         void* ids, bool i16, float* __restrict__ probs,
+                                                         bool renorm) {
+    __shared__ RadixSmem sm;
+    const int tid = threadIdx.x, lane = (int)lane_id(), warp = tid >> 5;
+    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
         const float* row = logits + t * E;
         unsigned key[V];
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < V; i++) {
-            int e = i * 32 + lane;
-            float x = (e < E) ? __ldg(row + e) : -INFINITY;
+            const int e = i * RT + tid;
+            const float x = (e < E) ? __ldg(row + e) : -INFINITY;
             key[i] = (e < E) ? f2key(x) : 0u;   // absent slots: key 0, below every real key
             m = fmaxf(m, x);
         }
-        m = warp_max(m);
+        m = block_max(m, sm);
         float den = 0.0f;
         if (!renorm) {
 #pragma unroll
             for (int i = 0; i < V; i++)
-                if (i * 32 + lane < E) den += expf(key2f(key[i]) - m);
-            den = warp_sum(den);
+                if (key[i] != 0u) den += expf(key2f(key[i]) - m);
+            den = block_sum(den, sm);
         }
-
-        // three histogram passes over 11/11/10-bit digits, each restricted to the
-        // keys that match the prefix found so far
+        if (tid == 0) { sm.n_cand = 0; sm.n_list = 0; }
+        // narrow the K-th key until its bin is small enough to rank directly
         unsigned prefix = 0, pmask = 0, rem = (unsigned)K;
+        bool exact = false;
 #pragma unroll 1
         for (int p = 0; p < 3; p++) {
             const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
-            const int nbits = p == 2 ? 10 : 11;
-            const int nb = 1 << nbits;
-            const unsigned dmask = (unsigned)nb - 1u;
-            for (int b = lane; b < nb; b += 32) hist[b] = 0u;
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < V; i++)
-                if (key[i] != 0u && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> sh) & dmask], 1u);
-            __syncwarp();
-            unsigned above;
-            int bin = find_bin(hist, nb, rem, lane, &above);
-            rem -= above;
-            prefix |= (unsigned)bin << sh;
-            pmask |= dmask << sh;
-            __syncwarp();
+            const int nb = p == 2 ? 1024 : 2048;
+            radix_pass<V>(key, prefix, pmask, sh, nb, rem, sm);
+            rem -= sm.above;
+            prefix |= sm.bin << sh;
+            pmask |= ((unsigned)nb - 1u) << sh;
+            const unsigned cnt = sm.hist[((sm.bin & (nb / RT - 1)) << 8) + (sm.bin >> (nb == 2048 ? 3 : 2))];
+            if (p == 2) exact = true;
+            else if (cnt <= CAND_MAX) break;
+            __syncthreads();   // sm.bin / sm.hist reused by the next pass
         }
-        // prefix is now the exact K-th largest key; take every key above it and
-        // the `rem` lowest-index keys equal to it
-        const unsigned tau = prefix;
-        unsigned tie_left = rem;
-        int base = 0;
+        // keys above the prefix go straight to the list; keys matching it are candidates
 #pragma unroll
         for (int i = 0; i < V; i++) {
-            int e = i * 32 + lane;
-            bool real = e < E;
-            bool gt = real && key[i] > tau;
-            bool eq = real && key[i] == tau;
-            unsigned meq = __ballot_sync(FULL, eq);
-            unsigned r = (unsigned)__popc(meq & lanemask_lt());
-            bool take = gt || (eq && r < tie_left);
-            unsigned ne = (unsigned)__popc(meq);
-            tie_left -= ne < tie_left ? ne : tie_left;
-            unsigned mt = __ballot_sync(FULL, take);
-            if (take) {
-                int pos = base + __popc(mt & lanemask_lt());
-                lkey[pos] = key[i];
-                lidx[pos] = e;
+            const unsigned k = key[i];
+            if (k == 0u) continue;
+            const unsigned km = k & pmask;
+            if (km > prefix) {
+                const int pos = atomicAdd(&sm.n_list, 1);
+                sm.list_key[pos] = k;
+                sm.list_idx[pos] = i * RT + tid;
+            } else if (km == prefix && !exact) {
+                const int pos = atomicAdd(&sm.n_cand, 1);
+                sm.cand_key[pos] = k;
+                sm.cand_idx[pos] = i * RT + tid;
             }
-            base += __popc(mt);
         }
-        __syncwarp();
+        if (exact) {
+            // prefix is the K-th key itself: take the `rem` lowest-index keys equal to it, in index order
+            unsigned taken = 0;
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const bool eq = key[i] == prefix && key[i] != 0u;
+                const unsigned bal = __ballot_sync(FULL, eq);
+                __syncthreads();
+                if (lane == 0) sm.ured[warp] = __popc(bal);
+                __syncthreads();
+                unsigned before = taken;
+                for (int w = 0; w < warp; w++) before += sm.ured[w];
+                unsigned tot = taken;
+                for (int w = 0; w < RW; w++) tot += sm.ured[w];
+                const unsigned r = before + __popc(bal & lanemask_lt());
+                if (eq && r < rem) {
+                    const int pos = atomicAdd(&sm.n_list, 1);
+                    sm.list_key[pos] = key[i];
+                    sm.list_idx[pos] = i * RT + tid;
+                }
+                taken = tot;
+            }
+        }
+        __syncthreads();
+        if (!exact) {
+            // rank the candidates (descending key, ascending index); the first rem join the list
+            const int nc = sm.n_cand;
+            for (int c = tid; c < nc; c += RT) {
+                const unsigned kc = sm.cand_key[c];
+                const int ic = sm.cand_idx[c];
+                unsigned r = 0;
+                for (int j = 0; j < nc; j++) {
+                    const unsigned kj = sm.cand_key[j];
+                    r += (kj > kc) || (kj == kc && sm.cand_idx[j] < ic);
+                }
+                if (r < rem) {
+                    const int pos = atomicAdd(&sm.n_list, 1);
+                    sm.list_key[pos] = kc;
+                    sm.list_idx[pos] = ic;
+                }
+            }
+            __syncthreads();
+        }
+        // the list holds exactly K keys: rank them and write ids / probs in order
         if (renorm) {
-            for (int j = lane; j < K; j += 32) den += expf(key2f(lkey[j]) - m);
-            den = warp_sum(den);
+            float d = 0.0f;
+            for (int j = tid; j < K; j += RT) d += expf(key2f(sm.list_key[j]) - m);
+            den = block_sum(d, sm);
         }
-        // rank the K winners: descending key, ascending index
-        for (int j = lane; j < K; j += 32) {
-            unsigned kj = lkey[j];
-            int ij = lidx[j];
+        for (int j = tid; j < K; j += RT) {
+            const unsigned kj = sm.list_key[j];
+            const int ij = sm.list_idx[j];
             int rk = 0;
             for (int j2 = 0; j2 < K; j2++) {
-                unsigned k2 = lkey[j2];
-                rk += (k2 > kj) || (k2 == kj && lidx[j2] < ij);
+                const unsigned k2 = sm.list_key[j2];
+                rk += (k2 > kj) || (k2 == kj && sm.list_idx[j2] < ij);
             }
-            long long o = t * K + rk;
+            const long long o = t * K + rk;
             store_route(ids, i16, o, ij);
             probs[o] = expf(key2f(kj) - m) / den;
         }
-        __syncwarp();
+        __syncthreads();   // shared state is reused by the next row
     }
 }
 
@@ -293,10 +364,9 @@ cudaError_t launch_radix(const float* logits, int T, int E, int K, void* ids, bo
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    long long need = ((long long)T + RADIX_WARPS - 1) / RADIX_WARPS;
-    long long cap = (long long)sms * 8;
-    int blocks = (int)(need < cap ? need : cap);
-    route_radix_kernel<V><<<blocks, RADIX_WARPS * 32, 0, s>>>(logits, T, E, K, ids, i16, probs, renorm);
+    const long long cap = (long long)sms * 8;
+    const int blocks = (int)(T < cap ? T : cap);
+    route_radix_kernel<V><<<blocks, RT, 0, s>>>(logits, T, E, K, ids, i16, probs, renorm);
     return cudaGetLastError();
 }
 
@@ -331,12 +401,13 @@ extern "C" moe_status moe_route_topk(const float* logits, int T, int E, int K, v
         else if (E <= 128) err = launch_small<32, 4>(logits, T, E, K, ids, i16, probs, renorm, s);
         else err = launch_small<32, 8>(logits, T, E, K, ids, i16, probs, renorm, s);
     } else {
-        if (K > KMAX || E > 4096) return MOE_ERR_UNSUPPORTED;
-        if (E <= 256) err = launch_radix<8>(logits, T, E, K, ids, i16, probs, renorm, s);
-        else if (E <= 512) err = launch_radix<16>(logits, T, E, K, ids, i16, probs, renorm, s);
-        else if (E <= 1024) err = launch_radix<32>(logits, T, E, K, ids, i16, probs, renorm, s);
-        else if (E <= 2304) err = launch_radix<72>(logits, T, E, K, ids, i16, probs, renorm, s);
-        else err = launch_radix<128>(logits, T, E, K, ids, i16, probs, renorm, s);
+        if (K > KMAX || E > 8192) return MOE_ERR_UNSUPPORTED;
+        if (E <= 256) err = launch_radix<1>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 512) err = launch_radix<2>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 1024) err = launch_radix<4>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 2304) err = launch_radix<9>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 4096) err = launch_radix<16>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else err = launch_radix<32>(logits, T, E, K, ids, i16, probs, renorm, s);
     }
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -69,6 +69,10 @@ WORKLOADS = {
     # a quarter of F and half of T: about 1.5 GB on the device)
     "mixtral_prof": Workload("mixtral_prof", T=4096, H=4096, E=8, K=2, F=3584, bias="normal",
                              bias_scale=0.5, renorm=True),
+    # reduced MXFP8 training shape for profiler captures (H, F of the DeepSeek-V3-like
+    # slice, 8 experts, about 2 GB on the device)
+    "dsv3_prof": Workload("dsv3_prof", T=4096, H=7168, E=8, K=2, F=2048, precision="mxfp8",
+                          backward=True),
 }
 
 

@@ -85,9 +85,9 @@ typedef enum {
  * in that order (int16 or int32 per id_dtype); probs[T, K] fp32 is the softmax
  * over all E logits taken at the selected expert, or, with MOE_ROUTE_RENORM,
  * the softmax over the K selected logits. The router never emits -1.
- * Requires 1 <= K <= E, K <= 128, E <= 4096 (E <= 32767 for int16 ids), no NaN
+ * Requires 1 <= K <= E, K <= 128, E <= 8192, no NaN
  * logits (NaN rows give unspecified ids). Small E (<= 256) and K (<= 16) use a
- * warp-per-row arg-max path; the rest use the radix-select path.
+ * warp-per-row arg-max path; the rest use the radix-select path (a CTA per row).
  * ------------------------------------------------------------------------ */
 moe_status moe_route_topk(const float *logits, int T, int E, int K,
                           void *ids, moe_dtype id_dtype, float *probs,
@@ -203,9 +203,10 @@ moe_status moe_quant_mxfp8_grouped(const void *x, int R_cap, int H,
  * [R_cap, H/32] (as written by moe_permute with MOE_PERMUTE_FUSE_MXFP8);
  * h [R_cap, F] (caller-allocated intermediate, kept for the backward pass)
  * bf16, or E4M3 with h_scales [R_cap, F/32]; y_perm [R_cap, H] bf16.
- * Requires H % 256 == 0 and F % 128 == 0, x_perm, h and the packed weights
- * 128-byte aligned, E small enough for the group table to fit in shared
- * memory (E <= 4096). moe_grouped_gemm_up / _down run the two halves alone.
+ * Requires H % 256 == 0 and F % 128 == 0 (MXFP8: H % 512 == 0 and F % 512 == 0),
+ * x_perm, h and the packed weights 128-byte aligned, scales 16-byte aligned,
+ * E small enough for the group table to fit in shared memory (bf16: E <= 4200,
+ * MXFP8: E <= 1150). moe_grouped_gemm_up / _down run the two halves alone.
  * ------------------------------------------------------------------------ */
 size_t moe_packed_weights_bytes(int E, int H, int F, moe_dtype dtype, int which);
 /* which: 0 = w13 payload, 1 = w13 scales, 2 = w2 payload, 3 = w2 scales (0 bytes for bf16) */
@@ -259,7 +260,8 @@ moe_status moe_grouped_gemm_down(const void *h, const uint8_t *h_scales, const v
  *   (or, with src_rows != NULL, x [*, C] read at row src_rows[r], e.g. the
  *   tokens through perm_src), xT[c][P_e + i] = x[off[e] + i][c] for i < m_e, with
  *   P_e = 128 * (e + off[e] / 128) and zeros up to P_e + 128 * ceil(m_e / 128);
- *   xT is [C][Kpad], Kpad = moe_grouped_transpose_kpad(R_cap, E). MXFP8 output:
+ *   xT is [C][Kpad], Kpad = moe_grouped_transpose_kpad(R_cap, E) (a multiple of
+ *   512 at least 128 * (E + ceil(R_cap / 128) + 1)). MXFP8 output:
  *   group-aware 32-row blocks (starting at each group's first row, a partial
  *   block taking its amax over valid rows), E4M3 payload in xT and E8M0 scales
  *   xT_scales[c][P_e / 32 + b] ([C][Kpad/32]). Requires C % 64 == 0.

@@ -187,7 +187,8 @@ def _ids_from_sizes(T, K, sizes):
 def test_backward_small_ragged(precision):
     sizes = (0, 37, 130, 200, 1)
     T = sum(sizes) + 3
-    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=256, F=256, precision=precision, act_std=0.3)
+    HF = 512 if precision == "mxfp8" else 256   # MXFP8 contractions are whole 512-element scale boxes
+    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=HF, F=HF, precision=precision, act_std=0.3)
     _check_small(wl, _ids_from_sizes(T, 1, sizes), precision)
 
 

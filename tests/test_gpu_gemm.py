@@ -182,7 +182,7 @@ def test_gemm_mxfp8_tiny_all_rows():
 @pytest.mark.parametrize("sizes", [(0, 1, 127, 129, 300, 0, 3), (1, 1, 1, 1)])
 def test_gemm_mxfp8_ragged_groups(sizes):
     T = int(sum(sizes)) + 5
-    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=512, F=256, precision="mxfp8")
+    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=512, F=512, precision="mxfp8")
     _check_mxfp8(_run(wl, "mxfp8", sizes=list(sizes)))
 
 
