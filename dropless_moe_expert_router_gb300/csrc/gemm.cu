@@ -46,7 +46,11 @@
 // No padding of the data, no dropping.
 //
 // BF16: kind::f16, two TMEM accumulators (2 x 256 columns) so the epilogue of
-// tile i overlaps the main loop of tile i+1.
+// tile i overlaps the main loop of tile i+1. When groups are large, a tile is
+// 256 rows computed by a cluster of two CTAs (tcgen05 cta_group::2): each CTA
+// loads its 128 A rows and half of the B tile, the even CTA issues the MMAs
+// into both CTAs' TMEM and its barriers collect both CTAs' loads and
+// epilogues; the smaller stage (32 KB) allows a 6-deep ring.
 // MXFP8: kind::mxf8f6f4.block_scale (E4M3 x E4M3, UE8M0 scale per 32
 // elements); one accumulator plus per-stage scale-factor columns in TMEM.
 #include "common.cuh"
@@ -57,26 +61,32 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;          // rows per tile (MMA M)
+constexpr int BM = 128;          // rows per tile and CTA (MMA M per CTA)
 constexpr int BN = 256;          // output columns per tile (MMA N)
-constexpr int STAGES = 4;        // shared-memory ring depth
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 
 enum { MODE_UP = 0, MODE_DOWN = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
 
-template <bool FP8>
+// PAIR: a tile is computed by a cluster of two CTAs with tcgen05 cta_group::2 --
+// M = 256 rows (128 per CTA), and each CTA loads only its half of the B tile,
+// so a stage is 32 KB and the ring is 6 stages deep.
+template <bool FP8, bool PAIR = false>
 struct Cfg {
+    static_assert(!(FP8 && PAIR), "MXFP8 uses single-CTA tiles");
     static constexpr int BK = FP8 ? 128 : 64;       // elements per k-block (128 bytes per row)
     static constexpr int UMMA_K = FP8 ? 32 : 16;    // elements per MMA instruction
     static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per k-block (4)
+    static constexpr int TM = PAIR ? 2 * BM : BM;   // rows of a tile (both CTAs of a pair)
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows this CTA loads
     static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = BN * 128;
+    static constexpr int B_BYTES = B_ROWS * 128;
     // scale landing zones: a TMA box of 16 scale bytes (four k-blocks) per operand row;
     // the k-block's 32-bit word is then rearranged in place for tcgen05.cp
     static constexpr int SFA_BYTES = FP8 ? BM * 16 : 0;
     static constexpr int SFB_BYTES = FP8 ? BN * 16 : 0;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int ACC_STAGES = FP8 ? 1 : 2;
     static constexpr int SF_COLS = 12;              // TMEM columns of one stage's scales (4 A + 8 B)
 };
@@ -101,22 +111,25 @@ struct GemmArgs {
     void* out2;                  // WGRAD split: second half [E][M][N/2]
 };
 
-template <bool FP8>
+template <bool FP8, bool PAIR = false>
 constexpr size_t smem_bytes_for(int E) {
-    return 1024 /* alignment slack */ + (size_t)STAGES * Cfg<FP8>::STAGE_BYTES + 256 /* barriers, flags */ +
+    using C = Cfg<FP8, PAIR>;
+    return 1024 /* alignment slack */ + (size_t)C::STAGES * C::STAGE_BYTES + 256 /* barriers, flags */ +
            (size_t)NUM_THREADS * 4 + (size_t)2 * (E + 1) * 4;
 }
 
 struct TileInfo {
     int e, m, n;
-    int row0, rows;      // row-grouped: first A row and rows inside the group
-    int a_row, b_row;    // operand rows of the tile
+    int row0, rows;      // this CTA's first output row and its rows inside the group (may be <= 0)
+    int a_row, b_row;    // operand rows this CTA loads
     int k0, nkb;         // first contraction element and number of k-blocks
 };
 
-// Row-grouped modes: tile -> (expert, column tile, row tile).
-template <bool FP8>
-__device__ __forceinline__ TileInfo decode_rows(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p) {
+// Row-grouped modes: tile -> (expert, column tile, row tile of C::TM rows).
+template <bool FP8, bool PAIR>
+__device__ __forceinline__ TileInfo decode_rows(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p,
+                                                int rank) {
+    using C = Cfg<FP8, PAIR>;
     const int q = tile / p.n_tiles;
     int lo = 0, hi = p.E - 1;  // last e with s_mtp[e] <= q (never an empty expert)
     while (lo < hi) {
@@ -130,19 +143,20 @@ __device__ __forceinline__ TileInfo decode_rows(int tile, const int* s_mtp, cons
     t.e = lo;
     t.n = local / mt;
     t.m = local - t.n * mt;
-    t.row0 = s_goff[lo] + t.m * BM;
+    t.row0 = s_goff[lo] + t.m * C::TM + BM * rank;
     t.rows = min(BM, s_goff[lo + 1] - t.row0);
     t.a_row = t.row0;
-    t.b_row = lo * p.N + t.n * BN;
+    t.b_row = lo * p.N + t.n * BN + C::B_ROWS * rank;
     t.k0 = 0;
-    t.nkb = p.Kdim / Cfg<FP8>::BK;
+    t.nkb = p.Kdim / C::BK;
     return t;
 }
 
 // WGRAD: tile -> (expert, N tile, M tile); the expert's rows sit at
 // [128 * (e + goff[e] / 128), + m_e) of the padded contraction axis.
-template <bool FP8>
-__device__ __forceinline__ TileInfo decode_wgrad(int tile, const int* s_goff, const GemmArgs& p) {
+template <bool FP8, bool PAIR>
+__device__ __forceinline__ TileInfo decode_wgrad(int tile, const int* s_goff, const GemmArgs& p, int rank) {
+    using C = Cfg<FP8, PAIR>;
     const int per = p.m_tiles * p.n_tiles;
     TileInfo t;
     t.e = tile / per;
@@ -150,19 +164,20 @@ __device__ __forceinline__ TileInfo decode_wgrad(int tile, const int* s_goff, co
     t.n = local / p.m_tiles;
     t.m = local - t.n * p.m_tiles;
     const int g0 = s_goff[t.e], m_e = s_goff[t.e + 1] - g0;
-    t.row0 = t.m * BM;
+    t.row0 = t.m * C::TM + BM * rank;
     t.rows = BM;
-    t.a_row = t.m * BM;
-    t.b_row = t.n * BN;
+    t.a_row = t.row0;
+    t.b_row = t.n * BN + C::B_ROWS * rank;
     t.k0 = 128 * (t.e + g0 / 128);
-    t.nkb = (m_e + Cfg<FP8>::BK - 1) / Cfg<FP8>::BK;
+    t.nkb = (m_e + C::BK - 1) / C::BK;
     return t;
 }
 
-template <int MODE, bool FP8>
-__device__ __forceinline__ TileInfo decode(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p) {
-    if constexpr (MODE == MODE_WGRAD) return decode_wgrad<FP8>(tile, s_goff, p);
-    else return decode_rows<FP8>(tile, s_mtp, s_goff, p);
+template <int MODE, bool FP8, bool PAIR>
+__device__ __forceinline__ TileInfo decode(int tile, const int* s_mtp, const int* s_goff, const GemmArgs& p,
+                                           int rank) {
+    if constexpr (MODE == MODE_WGRAD) return decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank);
+    else return decode_rows<FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
 }
 
 // First contraction element of a tile, in units of 128 elements (WGRAD: the
@@ -200,12 +215,13 @@ __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
     for (int i = 0; i < 4; i++) bf16x8_to_f32(s[i], v + 8 * i);
 }
 
-template <int MODE, bool FP8>
+template <int MODE, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs p) {
-    using C = Cfg<FP8>;
+    using C = Cfg<FP8, PAIR>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;  // STAGES x [A | B | SFA | SFB]
@@ -223,6 +239,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int E = p.E;
+    // CTA pairs: rank within the pair; the even CTA (rank 0) issues the MMAs and owns
+    // the barriers both CTAs' loads and epilogues signal
+    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
@@ -231,7 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; a++) {
             ptx::mbar_init(&tfull[a], 1);
-            ptx::mbar_init(&tempty[a], 128);
+            ptx::mbar_init(&tempty[a], PAIR ? 8 : 128);  // pair: one arrival per epilogue warp of both CTAs
         }
         ptx::mbar_init(done, 1);
         *s_abort = 0u;
@@ -245,11 +267,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::prefetch_tmap(&tmSB);
         }
     }
+    if constexpr (PAIR) ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     if (warp == 1) {
-        ptx::tmem_alloc(s_tmem, TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(s_tmem, TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(s_tmem, TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
-    // group table: offsets, and the exclusive scan of row tiles per expert
+    // group table: offsets, and the exclusive scan of row tiles (C::TM rows) per expert
     for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_goff[e] = __ldg(p.goff + e);
     __syncthreads();
     {
@@ -258,7 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int local = 0;
         for (int j = 0; j < per; j++) {
             int e = b0 + j;
-            if (e < E) local += (s_goff[e + 1] - s_goff[e] + BM - 1) / BM;
+            if (e < E) local += (s_goff[e + 1] - s_goff[e] + C::TM - 1) / C::TM;
         }
         s_part[threadIdx.x] = local;
         __syncthreads();
@@ -277,12 +305,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int e = b0 + j;
             if (e < E) {
                 s_mtp[e] = run;
-                run += (s_goff[e + 1] - s_goff[e] + BM - 1) / BM;
+                run += (s_goff[e + 1] - s_goff[e] + C::TM - 1) / C::TM;
             }
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // both CTAs' TMEM is allocated
     ptx::tc_fence_after();
 
     const uint32_t tmem = *s_tmem;
@@ -294,22 +323,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const TileInfo ti = decode<MODE, FP8>(tile, s_mtp, s_goff, p);
+        for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
+            const TileInfo ti = decode<MODE, FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
             for (int kb = 0; kb < ti.nkb; kb++) {
                 if (!ptx::wait_parity(&empty[stage], phase ^ 1u, s_abort)) { ok = false; break; }
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
                 const int k = ti.k0 + kb * C::BK;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    ptx::tma_load_2d(sa, &tmA, &full[stage], k, ti.a_row);
-                    ptx::tma_load_2d(sb, &tmB, &full[stage], k, ti.b_row);
-                    if constexpr (FP8) {
-                        // 16 scale bytes per row (the 16-byte aligned group of four k-blocks holding this one)
-                        const int kx = (k / 32) & ~15;
-                        ptx::tma_load_2d(sb + C::B_BYTES, &tmSA, &full[stage], kx, ti.a_row);
-                        ptx::tma_load_2d(sb + C::B_BYTES + C::SFA_BYTES, &tmSB, &full[stage], kx, ti.b_row);
+                    if constexpr (PAIR) {
+                        // the even CTA's full barrier counts both CTAs' bytes
+                        if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                        const uint32_t bar = ptx::mapa_rank(&full[stage], 0);
+                        ptx::tma_load_2d_pair(sa, &tmA, bar, k, ti.a_row);
+                        ptx::tma_load_2d_pair(sb, &tmB, bar, k, ti.b_row);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        ptx::tma_load_2d(sa, &tmA, &full[stage], k, ti.a_row);
+                        ptx::tma_load_2d(sb, &tmB, &full[stage], k, ti.b_row);
+                        if constexpr (FP8) {
+                            // 16 scale bytes per row (the 16-byte aligned group of four k-blocks holding this one)
+                            const int kx = (k / 32) & ~15;
+                            ptx::tma_load_2d(sb + C::B_BYTES, &tmSA, &full[stage], kx, ti.a_row);
+                            ptx::tma_load_2d(sb + C::B_BYTES + C::SFA_BYTES, &tmSB, &full[stage], kx, ti.b_row);
+                        }
                     }
                 }
                 __syncwarp();
@@ -317,7 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (!ok) {
+        if (!ok && !PAIR) {
             // give the loads already issued a bounded chance to land before the CTA exits
             for (int i = 0; i < STAGES && i < issued; i++) {
                 if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
@@ -326,14 +363,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer (even CTA of a pair)
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const int nkb = MODE == MODE_WGRAD ? decode_wgrad<FP8>(tile, s_goff, p).nkb : p.Kdim / C::BK;
+        bool ok = leader;
+        for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
+            const int nkb =
+                MODE == MODE_WGRAD ? decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank).nkb : p.Kdim / C::BK;
             if (!ptx::wait_parity(&tempty[acc], acc_phase ^ 1u, s_abort)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
@@ -377,35 +415,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int k = 0; k < C::KSTEPS; k++)
                             ptx::mma_mxf8(d_tmem, ptx::sdesc_k_sw128(a0 + k * 32), ptx::sdesc_k_sw128(b0 + k * 32),
                                           ptx::idesc_mxf8(BM, BN, k, k), sf_t, sf_t + 4, (kb | k) != 0);
+                        ptx::tc_commit(&empty[stage]);
+                    } else if constexpr (PAIR) {
+#pragma unroll
+                        for (int k = 0; k < C::KSTEPS; k++)
+                            ptx::mma_f16_pair(d_tmem, ptx::sdesc_k_sw128(a0 + k * 32),
+                                              ptx::sdesc_k_sw128(b0 + k * 32), ptx::idesc_bf16(2 * BM, BN),
+                                              (kb | k) != 0);
+                        ptx::tc_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
                     } else {
 #pragma unroll
                         for (int k = 0; k < C::KSTEPS; k++)
                             ptx::mma_f16(d_tmem, ptx::sdesc_k_sw128(a0 + k * 32), ptx::sdesc_k_sw128(b0 + k * 32),
                                          ptx::idesc_bf16(BM, BN), (kb | k) != 0);
+                        ptx::tc_commit(&empty[stage]);
                     }
-                    ptx::tc_commit(&empty[stage]);
                 }
                 __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) ptx::tc_commit(&tfull[acc]);
+            if (lane == 0) {
+                if constexpr (PAIR) ptx::tc_commit_pair(&tfull[acc], 0x3);
+                else ptx::tc_commit(&tfull[acc]);
+            }
             __syncwarp();
             if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
         }
-        // make sure every MMA issued by this CTA has completed before TMEM is released
-        if (lane == 0) ptx::tc_commit(done);
-        __syncwarp();
-        volatile uint32_t never = 0u;
-        ptx::wait_parity(done, 0u, &never, 100000000ull);
+        if (leader) {
+            // make sure every MMA issued by this CTA has completed before TMEM is released
+            if (lane == 0) {
+                if constexpr (PAIR) ptx::tc_commit_pair(done, 0x1);
+                else ptx::tc_commit(done);
+            }
+            __syncwarp();
+            volatile uint32_t never = 0u;
+            ptx::wait_parity(done, 0u, &never, 100000000ull);
+        }
     } else {
-        // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int rit = q * 32 + lane;          // row within the tile
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode<MODE, FP8>(tile, s_mtp, s_goff, p);
+        for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+            const TileInfo ti = decode<MODE, FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
             if (!ptx::wait_parity(&tfull[acc], acc_phase, s_abort)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -477,7 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             } else if constexpr (MODE == MODE_WGRAD) {
                 const bool empty_expert = ti.nkb == 0;
-                const long long orow = (long long)ti.e * p.M + ti.m * BM + rit;
+                const long long orow = (long long)ti.e * p.M + ti.row0 + rit;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; c++) {
                     float v[32];
@@ -512,16 +565,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&tempty[acc]);
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_rank(&tempty[acc], 0));  // the even CTA's barrier
+            } else {
+                ptx::mbar_arrive(&tempty[acc]);
+            }
             if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+        else ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -579,12 +639,13 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64
 }
 
 // A: [a_rows][a_inner], B: [b_rows][a_inner], both K-major.
-template <int MODE, bool FP8>
+template <int MODE, bool FP8, bool PAIR>
 moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
-                       const GemmArgs& a, cudaStream_t s) {
+                       GemmArgs a, cudaStream_t s) {
+    using C = Cfg<FP8, PAIR>;
     CUtensorMap tmA, tmB, tmSA, tmSB;
     if (!make_operand_map(&tmA, A, FP8, inner, a_rows, BM)) return MOE_ERR_CUDA;
-    if (!make_operand_map(&tmB, B, FP8, inner, b_rows, BN)) return MOE_ERR_CUDA;
+    if (!make_operand_map(&tmB, B, FP8, inner, b_rows, C::B_ROWS)) return MOE_ERR_CUDA;
     if (FP8) {
         if (!make_scale_map(&tmSA, a.a_scales, (uint64_t)a.sf_row_bytes, a_rows, BM)) return MOE_ERR_CUDA;
         if (!make_scale_map(&tmSB, a.b_scales, (uint64_t)a.sf_row_bytes, b_rows, BN)) return MOE_ERR_CUDA;
@@ -592,19 +653,43 @@ moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b
         tmSA = tmA;
         tmSB = tmB;
     }
-    const size_t smem = smem_bytes_for<FP8>(a.E);
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (MODE == MODE_WGRAD) a.m_tiles = a.M / C::TM;
+    const size_t smem = smem_bytes_for<FP8, PAIR>(a.E);
+    auto kern = grouped_gemm_kernel<MODE, FP8, PAIR>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
-    grouped_gemm_kernel<MODE, FP8><<<device_sms(), NUM_THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);
+    const int sms = device_sms();
+    if (!PAIR) {
+        kern<<<sms, NUM_THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);
+        return moe_host::launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms / 2 * 2));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmSB, a) != cudaSuccess) return MOE_ERR_CUDA;
     return moe_host::launch_status();
 }
 
+// bf16 tiles are computed by CTA pairs (M = 256) when the groups can fill them:
+// row-grouped GEMMs when the mean group (R_cap / E, an upper bound) has at least
+// 512 rows, and weight gradients whose M is a multiple of 256; otherwise, and
+// for MXFP8, by single CTAs (M = 128).
 template <int MODE>
 moe_status launch_mode(bool fp8, const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
                        const GemmArgs& a, cudaStream_t s) {
-    return fp8 ? launch_gemm<MODE, true>(A, a_rows, B, b_rows, inner, a, s)
-               : launch_gemm<MODE, false>(A, a_rows, B, b_rows, inner, a, s);
+    if (fp8) return launch_gemm<MODE, true, false>(A, a_rows, B, b_rows, inner, a, s);
+    const bool pair = MODE == MODE_WGRAD ? (a.M % (2 * BM)) == 0 : (long long)a.R_cap >= 512LL * a.E;
+    return pair ? launch_gemm<MODE, false, true>(A, a_rows, B, b_rows, inner, a, s)
+                : launch_gemm<MODE, false, false>(A, a_rows, B, b_rows, inner, a, s);
 }
 
 moe_status check_common(moe_dtype dtype, const int32_t* group_offsets, int E, int H, int F, int R_cap) {
@@ -777,7 +862,7 @@ extern "C" moe_status moe_grouped_gemm_wgrad(const void* aT, const uint8_t* aT_s
     a.N = N;
     a.n_tiles = N / BN;
     a.M = M;
-    a.m_tiles = M / BM;
+    a.m_tiles = M / BM;  // reset per tile height at launch
     a.out = dw;
     a.out2 = dw2;
     a.a_scales = aT_scales;

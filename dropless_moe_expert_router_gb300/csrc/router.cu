@@ -227,21 +227,36 @@ __device__ void radix_pass(const unsigned (&key)[V], unsigned prefix, unsigned p
 }
 
 template <int V>
-__global__ void __launch_bounds__(RT) route_radix_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                         void* ids, bool i16, float* __restrict__ probs,
-                                                         bool renorm) {
+__global__ void __launch_bounds__(RT, 5) route_radix_kernel(const float* __restrict__ logits, int T, int E,
+                                                            int K, void* ids, bool i16, float* __restrict__ probs,
+                                                            bool renorm) {
     __shared__ RadixSmem sm;
     const int tid = threadIdx.x, lane = (int)lane_id(), warp = tid >> 5;
+    // the next row's logits are loaded while the current row is processed
+    float xn[V];
+    if (blockIdx.x < T) {
+#pragma unroll
+        for (int i = 0; i < V; i++) {
+            const int e = i * RT + tid;
+            xn[i] = (e < E) ? __ldg(logits + (long long)blockIdx.x * E + e) : -INFINITY;
+        }
+    }
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-        const float* row = logits + t * E;
         unsigned key[V];
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < V; i++) {
             const int e = i * RT + tid;
-            const float x = (e < E) ? __ldg(row + e) : -INFINITY;
-            key[i] = (e < E) ? f2key(x) : 0u;   // absent slots: key 0, below every real key
-            m = fmaxf(m, x);
+            key[i] = (e < E) ? f2key(xn[i]) : 0u;   // absent slots: key 0, below every real key
+            m = fmaxf(m, xn[i]);
+        }
+        const long long tn = t + gridDim.x;
+        if (tn < T) {
+#pragma unroll
+            for (int i = 0; i < V; i++) {
+                const int e = i * RT + tid;
+                xn[i] = (e < E) ? __ldg(logits + tn * E + e) : -INFINITY;
+            }
         }
         m = block_max(m, sm);
         float den = 0.0f;
@@ -364,7 +379,7 @@ cudaError_t launch_radix(const float* logits, int T, int E, int K, void* ids, bo
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long cap = (long long)sms * 8;
+    const long long cap = (long long)sms * 5;   // resident CTAs per SM at 48 registers: one wave
     const int blocks = (int)(T < cap ? T : cap);
     route_radix_kernel<V><<<blocks, RT, 0, s>>>(logits, T, E, K, ids, i16, probs, renorm);
     return cudaGetLastError();

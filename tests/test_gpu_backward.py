@@ -192,6 +192,14 @@ def test_backward_small_ragged(precision):
     _check_small(wl, _ids_from_sizes(T, 1, sizes), precision)
 
 
+def test_backward_bf16_pair_tiles_ragged():
+    """bf16 backward with groups large enough for 256-row CTA-pair tiles (dgrad, dx, wgrad)."""
+    sizes = (300, 0, 1100, 513)
+    T = 2100
+    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=256, F=256, act_std=0.3)
+    _check_small(wl, _ids_from_sizes(T, 1, sizes), "bf16")
+
+
 @pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
 def test_backward_small_routed(precision):
     wl = W.get("tiny", T=384, E=6, K=2, H=512, F=512, precision=precision, act_std=0.1)

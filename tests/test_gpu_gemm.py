@@ -166,6 +166,14 @@ def test_gemm_bf16_ragged_groups(sizes):
     _check_bf16(_run(wl, "bf16", sizes=list(sizes)))
 
 
+def test_gemm_bf16_pair_tiles_ragged():
+    """Enough rows per expert for 256-row CTA-pair tiles: empty, 1-row and ragged groups,
+    pair tiles whose second CTA has no valid row."""
+    sizes = (0, 700, 1, 513, 0, 1024)
+    wl = W.get("tiny", T=3200, E=len(sizes), K=1, H=256, F=256)
+    _check_bf16(_run(wl, "bf16", sizes=list(sizes)))
+
+
 def test_gemm_bf16_mixtral_sampled():
     _check_bf16(_run(W.get("mixtral"), "bf16", n_random=16))
 
