@@ -264,11 +264,23 @@ def run_ours(args, wl, rank, world, local_rank):
     launches = MoELayer.LAUNCHES_PER_FORWARD + (layer.launches_per_backward if wl.backward else 0)
 
     if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+        total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)
     return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, clocks=clocks, R=R, errs=errs,
                 h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2, launches=K * launches)
+
+
+def reduce_max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over all ranks of the process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, max_total_ms: float) -> float:
+    """Tokens of all ranks over the slowest rank's timed interval."""
+    return world * tokens_per_rank_step * steps / (max_total_ms / 1e3)
 
 
 def stage_report(wl, R, stage_ms):
@@ -372,13 +384,12 @@ def main():
     if rank != 0:
         return 0
 
-    total_s = r["total_ms"] / 1e3
-    value = world * wl.T * args.steps / total_s
+    value = whole_job_tokens_per_s(world, wl.T, args.steps, r["total_ms"])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.precision, "data": "synthetic", "config": config,
-        "e2e": {"value": world * wl.T * args.steps / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "tensor",

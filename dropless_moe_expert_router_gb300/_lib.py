@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_grouped_transpose": (I, [P, P, I, I, P, I, I, P, P, P]),
     "moe_grouped_gemm_wgrad": (I, [P, P, P, P, I, P, I, I, I, I, P, P, P]),
     "moe_get_device_errors": (I, [C.POINTER(C.c_uint32), I]),
+    "moe_debug_bounded_wait_selftest": (I, [C.c_uint32, P]),
     "moe_status_string": (C.c_char_p, [I]),
     "moe_route_ids_bytes": (SZ, [I, I, I]),
     "moe_route_probs_bytes": (SZ, [I, I]),

@@ -204,6 +204,12 @@ def moe_get_device_errors(clear: bool = True) -> int:
     return int(v.value)
 
 
+def moe_debug_bounded_wait_selftest(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (sets MOE_DEVERR_TIMEOUT after limit_us)."""
+    _check("moe_debug_bounded_wait_selftest",
+           _lib.load().moe_debug_bounded_wait_selftest(int(limit_us), _stream(stream)))
+
+
 def moe_route_ids_bytes(T: int, K: int, id_dtype=torch.int16) -> int:
     return int(_lib.load().moe_route_ids_bytes(T, K, _id_code(id_dtype)))
 

@@ -1,5 +1,6 @@
-// api.cu -- device error word and status helpers of the C ABI.
+// api.cu -- device error word, status helpers and the bounded-wait self-test of the C ABI.
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 __device__ unsigned int g_device_errors = 0u;
@@ -28,4 +29,29 @@ extern "C" const char* moe_status_string(moe_status status) {
         case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
     }
     return "MOE_ERR_UNKNOWN";
+}
+
+namespace moe {
+namespace {
+// One warp waits on an mbarrier that nothing ever arrives on, with the same
+// bounded wait the grouped GEMM uses; the wait gives up after limit_ns, sets
+// MOE_DEVERR_TIMEOUT and the kernel returns normally.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    ptx::wait_parity(&bar, 0u, &abort_flag, limit_ns);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_debug_bounded_wait_selftest(uint32_t limit_us, moe_stream_t stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_ARG;
+    moe::bounded_wait_selftest_kernel<<<1, 32, 0, moe_host::as_stream(stream)>>>((uint64_t)limit_us * 1000ull);
+    return moe_host::launch_status();
 }

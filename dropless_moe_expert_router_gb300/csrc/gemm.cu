@@ -656,8 +656,14 @@ moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b
     if (MODE == MODE_WGRAD) a.m_tiles = a.M / C::TM;
     const size_t smem = smem_bytes_for<FP8, PAIR>(a.E);
     auto kern = grouped_gemm_kernel<MODE, FP8, PAIR>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    // raise the kernel's dynamic shared-memory limit once per process and size (not a stream operation,
+    // but keeping it out of repeated calls keeps captured launches free of other API calls)
+    static int configured_smem = 0;
+    if ((int)smem > configured_smem) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured_smem = (int)smem;
+    }
     const int sms = device_sms();
     if (!PAIR) {
         kern<<<sms, NUM_THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);

@@ -319,6 +319,12 @@ moe_status moe_unpermute_combine(const void *y_perm, const int32_t *row_map,
  * ------------------------------------------------------------------------ */
 moe_status moe_get_device_errors(uint32_t *flags_out, int clear);
 
+/* Self-test of the bounded waits the grouped GEMM uses for its pipeline barriers:
+ * launches one warp that waits on a barrier nothing arrives on; after limit_us
+ * microseconds (1 .. 1,000,000) the wait gives up, sets MOE_DEVERR_TIMEOUT in the
+ * device error word and the kernel returns, leaving the context usable. */
+moe_status moe_debug_bounded_wait_selftest(uint32_t limit_us, moe_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *moe_status_string(moe_status status);
 

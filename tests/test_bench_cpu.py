@@ -1,0 +1,81 @@
+"""Host-side logic of bench.py, on the CPU: the reference arm's JSON line, rank
+handling under torchrun, and the max-over-ranks reduction of the timed
+intervals with world_size 2 over gloo."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                          env=env, timeout=600)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"]["workload"].startswith("tiny")
+    assert d["steps"] == 2 and d["warmup"] == 3
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_rejected():
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "2"])
+    assert r.returncode != 0
+
+
+def test_whole_job_throughput():
+    import bench
+    # 2 ranks x 8192 tokens x 10 steps over a slowest-rank interval of 40 ms
+    assert bench.whole_job_tokens_per_s(2, 8192, 10, 40.0) == pytest.approx(2 * 8192 * 10 / 0.040)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    mine = [10.0 + rank * 5.0, 30.0 - rank * 7.0]       # rank 0: (10, 30); rank 1: (15, 23)
+    got = bench.reduce_max_over_ranks(mine, "cpu")
+    out[rank] = got
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_gloo_world_size_2():
+    world = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
+    for r in range(world):
+        assert out[r] == [15.0, 30.0]
