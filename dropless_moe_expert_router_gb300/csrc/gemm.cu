@@ -24,7 +24,7 @@
 //          (transposed, group-padded operands, zero past each group's end);
 //          output dW[e] [M][N] bf16, or split into two [M][N/2] halves.
 //
-// Design (one CTA per SM, persistent, warp-specialised; 192 threads):
+// Design (one CTA per SM, persistent, warp-specialised; 320 threads):
 //   warp 0     TMA producer: A tile [128 rows x 128 B] and B tile [256 rows x 128 B]
 //              per k-block into a 4-stage shared-memory ring (128-byte swizzle);
 //              MXFP8 adds one TMA box of 16 E8M0 scale bytes per A and B row.
@@ -33,8 +33,11 @@
 //              commit hands the accumulator to the epilogue. For MXFP8 the warp
 //              first rearranges the k-block's scale words into the layout
 //              tcgen05.cp expects and copies them to TMEM.
-//   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns the
-//              32 TMEM lanes of its quarter) and the mode's store.
+//   warp 10    (MXFP8) rearranges each landed stage's scale words for tcgen05.cp.
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, each copying its half of
+//              the fp32 accumulator columns to registers with tcgen05.ld and
+//              handing TMEM back before the mode's math and stores (so with one
+//              accumulator, as for MXFP8, the next tile's MMAs start at once).
 // Tiles are scheduled on the device: every CTA reads group_offsets and walks
 // the tile list with a static stride of gridDim.x. Row-grouped modes count
 // ceil(m_e / 128) row tiles per expert and order tiles expert-major, then
@@ -63,7 +66,7 @@ namespace {
 
 constexpr int BM = 128;          // rows per tile and CTA (MMA M per CTA)
 constexpr int BN = 256;          // output columns per tile (MMA N)
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 352;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 scales (MXFP8)
 constexpr int TMEM_COLS = 512;
 
 enum { MODE_UP = 0, MODE_DOWN = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
@@ -89,6 +92,7 @@ struct Cfg {
     static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int ACC_STAGES = FP8 ? 1 : 2;
     static constexpr int SF_COLS = 12;              // TMEM columns of one stage's scales (4 A + 8 B)
+    static constexpr int THREADS = FP8 ? NUM_THREADS : NUM_THREADS - 32;  // the scale warp exists for MXFP8 only
 };
 
 struct GemmArgs {
@@ -115,7 +119,7 @@ template <bool FP8, bool PAIR = false>
 constexpr size_t smem_bytes_for(int E) {
     using C = Cfg<FP8, PAIR>;
     return 1024 /* alignment slack */ + (size_t)C::STAGES * C::STAGE_BYTES + 256 /* barriers, flags */ +
-           (size_t)NUM_THREADS * 4 + (size_t)2 * (E + 1) * 4;
+           (size_t)C::THREADS * 4 + (size_t)2 * (E + 1) * 4;
 }
 
 struct TileInfo {
@@ -216,7 +220,7 @@ __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
 }
 
 template <int MODE, bool FP8, bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs p) {
@@ -230,10 +234,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* sfready = done + 1;   // MXFP8: a stage's scale words are rearranged for tcgen05.cp
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sfready + STAGES);
     volatile uint32_t* s_abort = s_tmem + 1;
     int* s_part = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
-    int* s_goff = s_part + NUM_THREADS;
+    int* s_goff = s_part + C::THREADS;
     int* s_mtp = s_goff + (p.E + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -250,10 +255,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; s++) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&sfready[s], 1);
         }
         for (int a = 0; a < 2; a++) {
             ptx::mbar_init(&tfull[a], 1);
-            ptx::mbar_init(&tempty[a], PAIR ? 8 : 128);  // pair: one arrival per epilogue warp of both CTAs
+            ptx::mbar_init(&tempty[a], PAIR ? 16 : 8);  // one arrival per epilogue warp (of both CTAs of a pair)
         }
         ptx::mbar_init(done, 1);
         *s_abort = 0u;
@@ -278,10 +284,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
     // group table: offsets, and the exclusive scan of row tiles (C::TM rows) per expert
-    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_goff[e] = __ldg(p.goff + e);
+    for (int e = threadIdx.x; e <= E; e += C::THREADS) s_goff[e] = __ldg(p.goff + e);
     __syncthreads();
     {
-        const int per = (E + NUM_THREADS - 1) / NUM_THREADS;
+        const int per = (E + C::THREADS - 1) / C::THREADS;
         const int b0 = threadIdx.x * per;
         int local = 0;
         for (int j = 0; j < per; j++) {
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncthreads();
         if (threadIdx.x == 0) {
             int run = 0;
-            for (int i = 0; i < NUM_THREADS; i++) {
+            for (int i = 0; i < C::THREADS; i++) {
                 int v = s_part[i];
                 s_part[i] = run;
                 run += v;
@@ -376,33 +382,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
             for (int kb = 0; kb < nkb; kb++) {
-                if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
+                // MXFP8: the scale warp signals once the stage has landed and its scales are rearranged
+                if (!ptx::wait_parity(FP8 ? &sfready[stage] : &full[stage], phase, s_abort)) { ok = false; break; }
                 ptx::tc_fence_after();
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
-                if constexpr (FP8) {
-                    // Rearrange this k-block's scale words for tcgen05.cp .32x128b: word (lane*4 + j)
-                    // of a 512-byte chunk must hold row 32*j + lane of that chunk. The landing zone
-                    // holds 16 bytes (four k-blocks) per row; read everything, then write in place.
-                    const int w = ((tile_k0_div128<MODE>(p, tile, s_goff) + kb) & 3);
-                    const uint32_t* la = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES);
-                    const uint32_t* lb = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES + C::SFA_BYTES);
-                    uint32_t va[4], vb0[4], vb1[4];
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        va[j] = la[(32 * j + lane) * 4 + w];
-                        vb0[j] = lb[(32 * j + lane) * 4 + w];
-                        vb1[j] = lb[(128 + 32 * j + lane) * 4 + w];
-                    }
-                    __syncwarp();
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES)[lane] = make_uint4(va[0], va[1], va[2], va[3]);
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES)[lane] =
-                        make_uint4(vb0[0], vb0[1], vb0[2], vb0[3]);
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES + 512)[lane] =
-                        make_uint4(vb1[0], vb1[1], vb1[2], vb1[3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                }
                 if (lane == 0) {
                     const uint32_t a0 = ptx::smem_addr(sa), b0 = ptx::smem_addr(sb);
                     if constexpr (FP8) {
@@ -452,9 +436,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             volatile uint32_t never = 0u;
             ptx::wait_parity(done, 0u, &never, 100000000ull);
         }
+    } else if (FP8 && warp == 10) {
+        // ------------------------------------------------------------ scale warp (MXFP8)
+        // Rearranges each landed stage's scale words for tcgen05.cp .32x128b -- word
+        // (lane*4 + j) of a 512-byte chunk must hold row 32*j + lane of that chunk -- in
+        // place (the landing zone holds 16 bytes, four k-blocks, per row), then releases
+        // the stage to the MMA warp. Runs ahead of the MMA issue, off its critical path.
+        if constexpr (FP8) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
+                const int nkb = MODE == MODE_WGRAD ? decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank).nkb : p.Kdim / C::BK;
+                const int k0b = tile_k0_div128<MODE>(p, tile, s_goff);
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
+                    uint8_t* sb = ring + (size_t)stage * C::STAGE_BYTES + C::A_BYTES;
+                    const int w = (k0b + kb) & 3;
+                    const uint32_t* la = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES);
+                    const uint32_t* lb = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES + C::SFA_BYTES);
+                    uint32_t va[4], vb0[4], vb1[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        va[j] = la[(32 * j + lane) * 4 + w];
+                        vb0[j] = lb[(32 * j + lane) * 4 + w];
+                        vb1[j] = lb[(128 + 32 * j + lane) * 4 + w];
+                    }
+                    __syncwarp();
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES)[lane] = make_uint4(va[0], va[1], va[2], va[3]);
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES)[lane] =
+                        make_uint4(vb0[0], vb0[1], vb0[2], vb0[3]);
+                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES + 512)[lane] =
+                        make_uint4(vb1[0], vb1[1], vb1[2], vb1[3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&sfready[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
     } else {
-        const int q = warp & 3;                 // TMEM lane quarter of this warp
-        const int rit = q * 32 + lane;          // row within the tile
+        // ------------------------------------------------------------ epilogue (8 warps)
+        // Two warps per TMEM lane quarter, each owning half of the tile's columns. A warp
+        // first copies its 128 accumulator columns to registers and hands TMEM back (so the
+        // next tile's MMAs can start), then does the math and the stores.
+        const int q = warp & 3;                  // TMEM lane quarter of this warp
+        const int hf = (warp - 2) >> 2;          // column half of this warp
+        const int rit = q * 32 + lane;           // row within this CTA's tile
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = tile0; tile < total_tiles; tile += tile_step) {
@@ -464,23 +492,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const bool valid = rit < ti.rows;
             const long long r = (long long)ti.row0 + rit;
-            if constexpr (MODE == MODE_UP) {
-                const int col0 = ti.n * (BN / 2);
-#pragma unroll 1
-                for (int c = 0; c < BN / 64; c++) {
-                    uint32_t g[32], u[32];
-                    ptx::tmem_ld_x32(tbase + 32 * c, g);
-                    ptx::tmem_ld_x32(tbase + BN / 2 + 32 * c, u);
-                    ptx::tmem_wait_ld();
-                    float hv[32];
+            const bool has_acc = !(MODE == MODE_WGRAD && ti.nkb == 0);  // an expert without rows: zeros
+            uint32_t v[128];
+            if (has_acc) {
+                if constexpr (MODE == MODE_UP) {
+                    // gate columns [64 hf, 64 hf + 64) and the matching up columns
+                    ptx::tmem_ld_x32(tbase + 64 * hf, v);
+                    ptx::tmem_ld_x32(tbase + 64 * hf + 32, v + 32);
+                    ptx::tmem_ld_x32(tbase + BN / 2 + 64 * hf, v + 64);
+                    ptx::tmem_ld_x32(tbase + BN / 2 + 64 * hf + 32, v + 96);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+                    for (int c = 0; c < 4; c++) ptx::tmem_ld_x32(tbase + 128 * hf + 32 * c, v + 32 * c);
+                }
+                ptx::tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; i++) v[i] = 0u;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_rank(&tempty[acc], 0));  // even CTA's barrier
+                else ptx::mbar_arrive(&tempty[acc]);
+            }
+            if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+            const float* f = reinterpret_cast<const float*>(v);
+
+            if constexpr (MODE == MODE_UP) {
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    const int hcol = ti.n * (BN / 2) + 64 * hf + 32 * c;   // h column
                     if (valid && p.ab) {
                         // saved pre-activations, same interleaved layout as W13 packed
-                        __nv_bfloat16* abrow = p.ab + r * (2 * p.ldo) + ti.n * BN + 32 * c;
-                        store_bf16x32(abrow, reinterpret_cast<const float*>(g));
-                        store_bf16x32(abrow + BN / 2, reinterpret_cast<const float*>(u));
+                        __nv_bfloat16* abrow = p.ab + r * (2 * p.ldo) + ti.n * BN + 64 * hf + 32 * c;
+                        store_bf16x32(abrow, f + 32 * c);
+                        store_bf16x32(abrow + BN / 2, f + 64 + 32 * c);
                     }
+                    // h = silu(a) * b, written over the gate values it no longer needs
+                    float* hv = reinterpret_cast<float*>(v) + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; i++) hv[i] = silu_f(hv[i]) * f[64 + 32 * c + i];
                     if constexpr (FP8) {
                         float amax = 0.0f;
 #pragma unroll
@@ -493,85 +545,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             w[i] = (uint32_t)f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
                                    ((uint32_t)f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
                         if (valid) {
-                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + r * p.ldo + col0 + 32 * c);
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + r * p.ldo + hcol);
                             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                            p.out_scales[r * (p.ldo / 32) + (col0 / 32) + c] = (uint8_t)sbyte;
-                            if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + col0 + 32 * c, hv);
+                            p.out_scales[r * (p.ldo / 32) + hcol / 32] = (uint8_t)sbyte;
+                            if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + hcol, hv);
                         }
                     } else {
-                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + col0 + 32 * c, hv);
+                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + hcol, hv);
                     }
                 }
             } else if constexpr (MODE == MODE_DGRAD) {
-                // dh columns f = n*256 + 32c + i; (a | b) and (da | db) interleaved per 128 columns
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c++) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_x32(tbase + 32 * c, v);
-                    ptx::tmem_wait_ld();
-                    if (valid) {
-                        const int f = ti.n * BN + 32 * c;
-                        const long long off = r * p.ldo + (long long)(f / 128) * 256 + (f % 128);
-                        float a[32], b[32], da[32], db[32];
-                        load_bf16x32(p.ab + off, a);
-                        load_bf16x32(p.ab + off + 128, b);
+                // dh columns fc = n*256 + 128 hf + 32c + i; (a | b) and (da | db) interleaved per 128
+                if (valid) {
+                    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            const float dh = __uint_as_float(v[i]);
-                            const float sg = __fdividef(1.0f, 1.0f + __expf(-a[i]));
-                            da[i] = dh * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
-                            db[i] = dh * a[i] * sg;
+                    for (int c = 0; c < 4; c++) {
+                        const int fc = ti.n * BN + 128 * hf + 32 * c;
+                        const long long off = r * p.ldo + (long long)(fc / 128) * 256 + (fc % 128);
+#pragma unroll
+                        for (int sbk = 0; sbk < 4; sbk++) {
+                            const uint4 av = *reinterpret_cast<const uint4*>(p.ab + off + 8 * sbk);
+                            const uint4 bv = *reinterpret_cast<const uint4*>(p.ab + off + 128 + 8 * sbk);
+                            float a[8], b[8], da[8], db[8];
+                            bf16x8_to_f32(av, a);
+                            bf16x8_to_f32(bv, b);
+#pragma unroll
+                            for (int i = 0; i < 8; i++) {
+                                const float dh = f[32 * c + 8 * sbk + i];
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-a[i]));
+                                da[i] = dh * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
+                                db[i] = dh * a[i] * sg;
+                            }
+                            *reinterpret_cast<uint4*>(o + off + 8 * sbk) = f32_to_bf16x8(da);
+                            *reinterpret_cast<uint4*>(o + off + 128 + 8 * sbk) = f32_to_bf16x8(db);
                         }
-                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
-                        store_bf16x32(o + off, da);
-                        store_bf16x32(o + off + 128, db);
                     }
                 }
             } else if constexpr (MODE == MODE_WGRAD) {
-                const bool empty_expert = ti.nkb == 0;
                 const long long orow = (long long)ti.e * p.M + ti.row0 + rit;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c++) {
-                    float v[32];
-                    if (!empty_expert) {
-                        uint32_t u[32];
-                        ptx::tmem_ld_x32(tbase + 32 * c, u);
-                        ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(u[i]);
+                for (int c = 0; c < 4; c++) {
+                    if (p.out2) {  // split: column half 0 of the tile -> out, half 1 -> out2
+                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(hf ? p.out2 : p.out);
+                        store_bf16x32(o + orow * (p.N / 2) + ti.n * (BN / 2) + 32 * c, f + 32 * c);
                     } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = 0.0f;
-                    }
-                    if (p.out2) {  // split: columns [0,128) of the tile -> out, [128,256) -> out2
-                        const int half = c / 4;
-                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(half ? p.out2 : p.out);
-                        store_bf16x32(o + orow * (p.N / 2) + ti.n * (BN / 2) + 32 * (c % 4), v);
-                    } else {
-                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + orow * p.N + ti.n * BN + 32 * c, v);
+                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + orow * p.N + ti.n * BN + 128 * hf + 32 * c,
+                                      f + 32 * c);
                     }
                 }
             } else {  // MODE_DOWN
-                const int col0 = ti.n * BN;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c++) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_x32(tbase + 32 * c, v);
-                    ptx::tmem_wait_ld();
-                    if (valid)
-                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + col0 + 32 * c,
-                                      reinterpret_cast<const float*>(v));
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++)
+                        store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + ti.n * BN + 128 * hf + 32 * c,
+                                      f + 32 * c);
                 }
             }
-            ptx::tc_fence_before();
-            if constexpr (PAIR) {
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_rank(&tempty[acc], 0));  // the even CTA's barrier
-            } else {
-                ptx::mbar_arrive(&tempty[acc]);
-            }
-            if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
@@ -666,12 +696,12 @@ moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b
     }
     const int sms = device_sms();
     if (!PAIR) {
-        kern<<<sms, NUM_THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);
+        kern<<<sms, C::THREADS, smem, s>>>(tmA, tmB, tmSA, tmSB, a);
         return moe_host::launch_status();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(sms / 2 * 2));
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
