@@ -1,18 +1,24 @@
 // router.cu -- router top-K kernels and the moe_route_topk entry point.
 //
-// Two paths ("Sparser MoE end-to-end", section "Preserve a compact route"):
+// Three paths ("Sparser MoE end-to-end", section "Preserve a compact route"):
 //  * small E and K: a warp (or a group of G lanes of a warp) per row keeps the
 //    logits in registers and runs K rounds of a segmented arg-max;
-//  * large E and K (e.g. 2,304 experts, top-36): radix/threshold select -- a
-//    bounded histogram pass over the top 11 bits of an order-preserving key
-//    finds the bin of the K-th largest key, the candidates in that bin are
-//    ranked directly (further 11- and 10-bit passes narrow the range only when
-//    the bin is crowded), and the K winners are ranked in a final step; no
-//    full-row scan per selected expert.
+//  * large E and K with E % 4 == 0, E <= 2,304 (e.g. 2,304 experts, top-36):
+//    threshold select, one warp per row -- a threshold from the lanes' own top
+//    values bounds the K-th largest logit from below, the few logits above it
+//    are ranked directly, and a warp-level exact search takes over for rows
+//    with heavy ties;
+//  * other large shapes: radix/threshold select, one CTA per row -- a bounded
+//    histogram pass over the top 11 bits of an order-preserving key finds the
+//    bin of the K-th largest key, the candidates in that bin are ranked
+//    directly (further 11- and 10-bit passes narrow the range only when the
+//    bin is crowded), and the K winners are ranked in a final step.
+// No path scans the full row once per selected expert.
 // Output: ids [T, K] (selection order: descending logit, lower index on ties),
 // probs [T, K] fp32 (softmax over all E logits at the selected ids, or over the
 // K selected logits with MOE_ROUTE_RENORM).
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 #include <math.h>
 
@@ -364,6 +370,378 @@ __global__ void __launch_bounds__(RT, 5) route_radix_kernel(const float* __restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Filter path, one warp per row (rows 16-byte aligned, E % 4 == 0, E <= 128 NV4):
+// lane l holds the float4s q = j*32 + l of its row (expert e = 4 q + c) and keeps
+// its P largest logits. A 16-step search over the top 16 bits of the order-
+// preserving key of those 32 P values gives a threshold tau with at least K
+// logits >= tau (the K-th largest of a subset of the row is a lower bound of the
+// row's K-th largest) and, normally, only a few more. The logits >= tau are
+// compacted to shared memory and ranked directly; a winner's rank is its output
+// slot. A row with more than FCAND logits >= tau (heavy ties) takes the exact
+// path instead: a 32-step search for the K-th largest key, the larger logits
+// ranked, and the logits equal to it taken in expert order.
+// ---------------------------------------------------------------------------
+constexpr int FW = 8;             // warps (rows in flight) per CTA
+constexpr int FCAND = 256;        // candidates per warp ranked directly
+
+// Shared memory of one CTA: per warp a row buffer (4 * 128 * NV4 bytes, filled by
+// a bulk copy one row ahead), the candidate list and its ranks, a counter and an
+// mbarrier.
+struct FilterWarp {
+    unsigned long long cand[FCAND];   // (logit, expert) as a pair, then as a 64-bit rank key
+    int rank[FCAND];
+    uint64_t bar;
+    int n;
+    uint32_t abort_flag;
+};
+template <int NV4>
+constexpr size_t filter_smem_bytes() {
+    return (size_t)FW * (512 * NV4 + sizeof(FilterWarp));
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// 2^y by the hardware approximation (relative error about 2^-22); exp(x - m) is
+// taken as 2^(x log2(e) - m log2(e)) with one rounding for the exponent.
+__device__ __forceinline__ float ex2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed pair arithmetic (two fp32 lanes in one 64-bit register).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// A candidate as a unique 64-bit key: order-preserving logit key above, the
+// complement of the expert index below, so that a larger key is a better route
+// (larger logit, then lower index).
+__device__ __forceinline__ unsigned long long cand_pack(float x, int e) {
+    return ((unsigned long long)__float_as_uint(x) << 32) | (unsigned)e;
+}
+__device__ __forceinline__ unsigned long long cand_key(unsigned long long pair) {
+    const unsigned k = f2key(__uint_as_float((unsigned)(pair >> 32)));
+    return ((unsigned long long)k << 32) | (0xffffffffu - (unsigned)pair);
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) { return key2f((unsigned)(key >> 32)); }
+__device__ __forceinline__ int key_expert(unsigned long long key) { return (int)(0xffffffffu - (unsigned)key); }
+
+// Turns the warp's n (logit, expert) pairs into rank keys and ranks them, two per
+// lane per sweep over the list; returns this lane's share of sum exp(logit - m)
+// over the candidates ranked below `limit` (mb = m log2(e)).
+__device__ __forceinline__ float rank_candidates(unsigned long long* cand, int* rk, int n, int limit, float mb) {
+    for (int c = (int)lane_id(); c < n; c += 32) cand[c] = cand_key(cand[c]);
+    __syncwarp();
+    float d = 0.0f;
+    for (int c0 = (int)lane_id(); c0 < n; c0 += 64) {
+        const int c1 = c0 + 32;
+        const unsigned long long ka = cand[c0];
+        const unsigned long long kb = c1 < n ? cand[c1] : ~0ull;
+        int ra = 0, rb = 0;
+#pragma unroll 4
+        for (int q = 0; q < n; q++) {
+            const unsigned long long o = cand[q];
+            ra += o > ka;
+            rb += o > kb;
+        }
+        rk[c0] = ra;
+        if (ra < limit) d += ex2_approx(fmaf(key_logit(ka), LOG2E, -mb));
+        if (c1 < n) {
+            rk[c1] = rb;
+            if (rb < limit) d += ex2_approx(fmaf(key_logit(kb), LOG2E, -mb));
+        }
+    }
+    return d;
+}
+
+__device__ __forceinline__ void write_ranked(const unsigned long long* cand, const int* rk, int n, int limit,
+                                             long long t, int K, void* ids, bool i16, float* probs, float mb,
+                                             float inv_den) {
+    for (int c = (int)lane_id(); c < n; c += 32) {
+        const int r = rk[c];
+        if (r < limit) {
+            const long long o = t * K + r;
+            store_route(ids, i16, o, key_expert(cand[c]));
+            probs[o] = ex2_approx(fmaf(key_logit(cand[c]), LOG2E, -mb)) * inv_den;
+        }
+    }
+}
+
+// G: group maxima per lane for the threshold (32 G >= K); element (j, c) of a lane
+// belongs to group (4 j + c) mod G.
+template <int NV4, int G>
+__global__ void __launch_bounds__(FW * 32, 2) route_filter_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int K, void* ids, bool i16,
+                                                                  float* __restrict__ probs, bool renorm) {
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int lane = (int)lane_id(), w = (int)(threadIdx.x >> 5);
+    float* rowbuf = reinterpret_cast<float*>(fsm) + (size_t)w * 128 * NV4;
+    FilterWarp& fw = reinterpret_cast<FilterWarp*>(fsm + (size_t)FW * 512 * NV4)[w];
+    unsigned long long* cand = fw.cand;
+    int* rk = fw.rank;
+    const int E4 = E >> 2;
+    const uint32_t row_bytes = 4u * (uint32_t)E;
+    const int nq = E4 > lane ? (E4 - lane + 31) / 32 : 0;   // float4s of the row this lane holds
+    const long long nwarps = (long long)gridDim.x * FW;
+    long long t = (long long)blockIdx.x * FW + w;
+    if (lane == 0) {
+        ptx::mbar_init(&fw.bar, 1);
+        fw.abort_flag = 0u;
+        ptx::fence_mbar_init();
+        if (t < T) {
+            ptx::mbar_arrive_expect_tx(&fw.bar, row_bytes);
+            ptx::bulk_load(rowbuf, logits + t * E, row_bytes, &fw.bar);
+        }
+    }
+    __syncwarp();
+    uint32_t phase = 0;
+    for (; t < T; t += nwarps) {
+        if (!ptx::wait_parity(&fw.bar, phase, &fw.abort_flag)) break;
+        phase ^= 1u;
+        // absent slots (past E) hold -inf: no group maximum, exp or threshold test is changed by them
+        float x[NV4][4];
+        const float4* rb = reinterpret_cast<const float4*>(rowbuf);
+#pragma unroll
+        for (int j = 0; j < NV4; j++) {
+            const float4 f = j < nq ? rb[j * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            x[j][0] = f.x;
+            x[j][1] = f.y;
+            x[j][2] = f.z;
+            x[j][3] = f.w;
+        }
+        float gm[G];
+#pragma unroll
+        for (int g = 0; g < G; g++) gm[g] = -INFINITY;
+        constexpr int GS = G / 4;                 // slot j + GS is in the same group as slot j
+#pragma unroll
+        for (int j0 = 0; j0 < NV4; j0 += 2 * GS)
+#pragma unroll
+            for (int j = j0; j < j0 + GS && j < NV4; j++)
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int g = (4 * j + c) % G;
+                    gm[g] = j + GS < NV4 ? max3f(gm[g], x[j][c], x[j + GS][c]) : fmaxf(gm[g], x[j][c]);
+                }
+        float m = gm[0];
+#pragma unroll
+        for (int g = 1; g < G; g++) m = fmaxf(m, gm[g]);
+        m = warp_max(m);
+        const float mb = m * LOG2E;
+        float den = 0.0f;
+        if (!renorm) {
+            // sum of 2^(x log2 e - m log2 e), the exponent arguments and sums formed in pairs
+            const unsigned long long l2 = f2_pack(LOG2E, LOG2E), nm = f2_pack(-mb, -mb);
+            unsigned long long d01 = 0ull, d23 = 0ull;
+#pragma unroll
+            for (int j = 0; j < NV4; j++) {
+                float y0, y1, y2, y3;
+                f2_unpack(f2_fma(f2_pack(x[j][0], x[j][1]), l2, nm), y0, y1);
+                f2_unpack(f2_fma(f2_pack(x[j][2], x[j][3]), l2, nm), y2, y3);
+                d01 = f2_add(d01, f2_pack(ex2_approx(y0), ex2_approx(y1)));
+                d23 = f2_add(d23, f2_pack(ex2_approx(y2), ex2_approx(y3)));
+            }
+            float a0, a1, a2, a3;
+            f2_unpack(d01, a0, a1);
+            f2_unpack(d23, a2, a3);
+            den = warp_sum((a0 + a1) + (a2 + a3));
+        }
+        // threshold: the largest 16-bit key prefix that at least K of the 32 G group maxima reach
+        // (the K-th largest of a subset of the row is at most the row's K-th largest)
+        unsigned ck[G];
+#pragma unroll
+        for (int g = 0; g < G; g++) ck[g] = f2key(gm[g]);
+        // key bits shared by every group maximum are bits of the answer: start below them
+        unsigned kmin = ck[0], kmax = ck[0];
+#pragma unroll
+        for (int g = 1; g < G; g++) {
+            kmin = min(kmin, ck[g]);
+            kmax = max(kmax, ck[g]);
+        }
+        kmin = __reduce_min_sync(FULL, kmin);
+        kmax = __reduce_max_sync(FULL, kmax);
+        const unsigned diff16 = (kmin ^ kmax) >> 16;
+        unsigned pre = kmin >> 16;
+        int b0 = -2;                              // lower bit of the first two-bit step
+        if (diff16) {
+            b0 = (31 - __clz(diff16)) & ~1;
+            pre &= ~((2u << b0) - 1u);            // bits b0 .. 0 are searched (b0 + 1 is kept or found again)
+        }
+#pragma unroll 1
+        for (int b = b0; b >= 0; b -= 2) {       // two bits a step: three independent counts
+            const unsigned t1 = (pre | (1u << b)) << 16, t2 = (pre | (2u << b)) << 16,
+                           t3 = (pre | (3u << b)) << 16;
+            unsigned c1 = 0, c2 = 0, c3 = 0;
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                c1 += ck[g] >= t1;
+                c2 += ck[g] >= t2;
+                c3 += ck[g] >= t3;
+            }
+            c1 = __reduce_add_sync(FULL, c1);
+            c2 = __reduce_add_sync(FULL, c2);
+            c3 = __reduce_add_sync(FULL, c3);
+            const unsigned uk = (unsigned)K;
+            pre |= (c3 >= uk ? 3u : c2 >= uk ? 2u : c1 >= uk ? 1u : 0u) << b;
+        }
+        // at or below the key of -inf the test would admit -inf (and absent) slots: exact path
+        const bool low = pre < 0x80u;
+        const float tau = low ? INFINITY : key2f(pre << 16);
+        // this lane's logits >= tau as a bit mask over its slots (bit 4 j + c), and their count
+        constexpr int NW = (4 * NV4 + 31) / 32;
+        unsigned mk[NW];
+#pragma unroll
+        for (int i = 0; i < NW; i++) mk[i] = 0u;
+#pragma unroll
+        for (int j = 0; j < NV4; j++)
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                if (x[j][c] >= tau) mk[(4 * j + c) >> 5] |= 1u << ((4 * j + c) & 31);
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < NW; i++) cnt += __popc(mk[i]);
+        int incl = cnt;
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            const int o = __shfl_up_sync(FULL, incl, dd);
+            if (lane >= dd) incl += o;
+        }
+        const int n = __shfl_sync(FULL, incl, 31);
+        const bool direct = !low && n <= FCAND;
+        int a = 0;                                        // exact path: logits above the K-th
+        if (direct) {
+            // the candidates, read back from the row buffer at the set bits
+            int pos = incl - cnt;
+#pragma unroll
+            for (int i = 0; i < NW; i++) {
+                unsigned bits = mk[i];
+                while (bits) {
+                    const int bslot = 32 * i + __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    const int e = 128 * (bslot >> 2) + 4 * lane + (bslot & 3);
+                    cand[pos++] = cand_pack(rowbuf[e], e);
+                }
+            }
+        } else {
+            // exact path over the row buffer: the K-th largest key by a search over all 32 key bits
+            unsigned kk = 0;
+#pragma unroll 1
+            for (int b = 31; b >= 0; b--) {
+                const unsigned trial = kk | (1u << b);
+                unsigned c = 0;
+                if (trial <= 0x007fffffu) {
+                    c = (unsigned)K;                      // at or below the key of -inf: every logit
+                } else {
+                    const float f = key2f(trial);         // above the key of +inf: NaN, no logit
+#pragma unroll 4
+                    for (int e = lane; e < E; e += 32) c += rowbuf[e] >= f;
+                    c = __reduce_add_sync(FULL, c);
+                }
+                if (c >= (unsigned)K) kk = trial;
+            }
+            const float fk = key2f(kk);                   // the K-th largest logit
+            const float ek = ex2_approx(fmaf(fk, LOG2E, -mb));
+            if (lane == 0) fw.n = 0;
+            __syncwarp();
+            float d = 0.0f;
+            for (int e = lane; e < E; e += 32) {
+                const float v = rowbuf[e];
+                if (v > fk) {                             // fewer than K such logits
+                    cand[atomicAdd(&fw.n, 1)] = cand_pack(v, e);
+                    d += ex2_approx(fmaf(v, LOG2E, -mb));
+                }
+            }
+            __syncwarp();
+            a = fw.n;
+            const int rem = K - a;                        // logits equal to fk that are taken, in expert order
+            if (renorm) den = warp_sum(d) + (float)rem * ek;
+            const float pk = ek / den;
+            int taken = 0;
+            for (int e0 = 0; e0 < E && taken < rem; e0 += 32) {
+                const int e = e0 + lane;
+                const bool eq = e < E && rowbuf[e] == fk;
+                const unsigned bal = __ballot_sync(FULL, eq);
+                const int ord = taken + __popc(bal & lanemask_lt());
+                if (eq && ord < rem) {
+                    const long long o = t * K + a + ord;
+                    store_route(ids, i16, o, e);
+                    probs[o] = pk;
+                }
+                taken += __popc(bal);
+            }
+        }
+        // the row buffer is free: start the copy of this warp's next row
+        __syncwarp();
+        if (lane == 0 && t + nwarps < T) {
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive_expect_tx(&fw.bar, row_bytes);
+            ptx::bulk_load(rowbuf, logits + (t + nwarps) * E, row_bytes, &fw.bar);
+        }
+        if (direct) {
+            const float d = rank_candidates(cand, rk, n, K, mb);
+            if (renorm) den = warp_sum(d);
+            __syncwarp();
+            write_ranked(cand, rk, n, K, t, K, ids, i16, probs, mb, 1.0f / den);
+        } else {
+            rank_candidates(cand, rk, a, K, mb);
+            __syncwarp();
+            write_ranked(cand, rk, a, K, t, K, ids, i16, probs, mb, 1.0f / den);
+        }
+        __syncwarp();   // the warp's shared lists are reused by its next row
+    }
+}
+
+template <int NV4, int G>
+cudaError_t launch_filter(const float* logits, int T, int E, int K, void* ids, bool i16, float* probs,
+                          bool renorm, cudaStream_t s) {
+    constexpr size_t smem = filter_smem_bytes<NV4>();
+    static int resident = 0;                      // one wave of CTAs: SMs x resident CTAs per SM
+    if (!resident) {
+        int dev = 0, sms = 0, per = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaError_t e = cudaFuncSetAttribute(route_filter_kernel<NV4, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_filter_kernel<NV4, G>, FW * 32, smem);
+        resident = sms * (per > 0 ? per : 1);
+    }
+    const long long need = ((long long)T + FW - 1) / FW;
+    const int blocks = (int)(need < resident ? need : resident);
+    route_filter_kernel<NV4, G><<<blocks, FW * 32, smem, s>>>(logits, T, E, K, ids, i16, probs, renorm);
+    return cudaGetLastError();
+}
+
+template <int NV4>
+cudaError_t launch_filter_k(const float* logits, int T, int E, int K, void* ids, bool i16, float* probs,
+                            bool renorm, cudaStream_t s) {
+    if (K <= 128 && K > 64) return launch_filter<NV4, 8>(logits, T, E, K, ids, i16, probs, renorm, s);
+    return launch_filter<NV4, 4>(logits, T, E, K, ids, i16, probs, renorm, s);
+}
+
 template <int G, int V>
 cudaError_t launch_small(const float* logits, int T, int E, int K, void* ids, bool i16, float* probs,
                          bool renorm, cudaStream_t s) {
@@ -415,6 +793,11 @@ extern "C" moe_status moe_route_topk(const float* logits, int T, int E, int K, v
         else if (E <= 64) err = launch_small<32, 2>(logits, T, E, K, ids, i16, probs, renorm, s);
         else if (E <= 128) err = launch_small<32, 4>(logits, T, E, K, ids, i16, probs, renorm, s);
         else err = launch_small<32, 8>(logits, T, E, K, ids, i16, probs, renorm, s);
+    } else if (E % 4 == 0 && E <= 2304 && K <= KMAX && moe_host::aligned(logits, 16)) {
+        if (E <= 256) err = launch_filter_k<2>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 512) err = launch_filter_k<4>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else if (E <= 1024) err = launch_filter_k<8>(logits, T, E, K, ids, i16, probs, renorm, s);
+        else err = launch_filter_k<18>(logits, T, E, K, ids, i16, probs, renorm, s);
     } else {
         if (K > KMAX || E > 8192) return MOE_ERR_UNSUPPORTED;
         if (E <= 256) err = launch_radix<1>(logits, T, E, K, ids, i16, probs, renorm, s);

@@ -87,7 +87,10 @@ typedef enum {
  * the softmax over the K selected logits. The router never emits -1.
  * Requires 1 <= K <= E, K <= 128, E <= 8192, no NaN
  * logits (NaN rows give unspecified ids). Small E (<= 256) and K (<= 16) use a
- * warp-per-row arg-max path; the rest use the radix-select path (a CTA per row).
+ * warp-per-row arg-max path; E % 4 == 0, E <= 2304 with 16-byte aligned logits
+ * use a warp-per-row threshold select; the rest use the radix-select path (a
+ * CTA per row). All paths give the same ids and the same probs up to fp32
+ * rounding order.
  * ------------------------------------------------------------------------ */
 moe_status moe_route_topk(const float *logits, int T, int E, int K,
                           void *ids, moe_dtype id_dtype, float *probs,

@@ -52,7 +52,9 @@ def test_router_matches_oracle(name):
 @pytest.mark.parametrize("T,E,K,renorm", [(1, 1, 1, False), (3, 2, 2, True), (37, 5, 5, False),
                                           (100, 32, 1, False), (64, 64, 16, True), (50, 200, 7, False),
                                           (50, 256, 32, False), (33, 300, 36, True), (20, 1000, 128, False),
-                                          (10, 2304, 36, False), (9, 4096, 100, True)])
+                                          (10, 2304, 36, False), (9, 4096, 100, True),
+                                          (16, 512, 64, True), (12, 2304, 128, False), (40, 2300, 36, True),
+                                          (24, 2302, 36, False), (20, 1028, 65, False)])
 def test_router_edge_shapes_and_ties(T, E, K, renorm):
     g = torch.Generator().manual_seed(T * 7919 + E)
     # a coarse value pool forces many exact ties, plus +-0 and -inf
