@@ -113,6 +113,7 @@ struct GemmArgs {
     int M;                       // WGRAD: rows of aT (multiple of BM)
     int m_tiles;                 // WGRAD: M / BM
     void* out2;                  // WGRAD split: second half [E][M][N/2]
+    int st32;                    // every output row segment is 32-byte aligned: 32-byte stores
 };
 
 template <bool FP8, bool PAIR = false>
@@ -203,14 +204,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 32 fp32 values -> 32 bf16 stored as 4 x 16 bytes.
-__device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
+// One 32-byte global store (dst 32-byte aligned): a whole sector per thread.
+__device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// 32 bytes from w[0..8) at dst: one 32-byte store when st32, else two 16-byte stores.
+__device__ __forceinline__ void store_32B(void* dst, const uint32_t* w, bool st32) {
+    if (st32) {
+        st_global_32B(dst, w);
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// 32 fp32 values -> 32 bf16 (64 bytes).
+__device__ __forceinline__ void store_bf16x32(void* dst, const float* v, bool st32) {
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; i++) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    store_32B(dst, w, st32);
+    store_32B(static_cast<uint8_t*>(dst) + 32, w + 8, st32);
 }
 
 __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
@@ -526,8 +544,8 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                     if (valid && p.ab) {
                         // saved pre-activations, same interleaved layout as W13 packed
                         __nv_bfloat16* abrow = p.ab + r * (2 * p.ldo) + ti.n * BN + 64 * hf + 32 * c;
-                        store_bf16x32(abrow, f + 32 * c);
-                        store_bf16x32(abrow + BN / 2, f + 64 + 32 * c);
+                        store_bf16x32(abrow, f + 32 * c, p.st32);
+                        store_bf16x32(abrow + BN / 2, f + 64 + 32 * c, p.st32);
                     }
                     // h = silu(a) * b, written over the gate values it no longer needs
                     float* hv = reinterpret_cast<float*>(v) + 32 * c;
@@ -545,14 +563,12 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                             w[i] = (uint32_t)f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
                                    ((uint32_t)f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
                         if (valid) {
-                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + r * p.ldo + hcol);
-                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            store_32B(static_cast<uint8_t*>(p.out) + r * p.ldo + hcol, w, p.st32);
                             p.out_scales[r * (p.ldo / 32) + hcol / 32] = (uint8_t)sbyte;
-                            if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + hcol, hv);
+                            if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + hcol, hv, p.st32);
                         }
                     } else {
-                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + hcol, hv);
+                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + hcol, hv, p.st32);
                     }
                 }
             } else if constexpr (MODE == MODE_DGRAD) {
@@ -588,10 +604,10 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 for (int c = 0; c < 4; c++) {
                     if (p.out2) {  // split: column half 0 of the tile -> out, half 1 -> out2
                         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(hf ? p.out2 : p.out);
-                        store_bf16x32(o + orow * (p.N / 2) + ti.n * (BN / 2) + 32 * c, f + 32 * c);
+                        store_bf16x32(o + orow * (p.N / 2) + ti.n * (BN / 2) + 32 * c, f + 32 * c, p.st32);
                     } else {
                         store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + orow * p.N + ti.n * BN + 128 * hf + 32 * c,
-                                      f + 32 * c);
+                                      f + 32 * c, p.st32);
                     }
                 }
             } else {  // MODE_DOWN
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 4; c++)
                         store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + ti.n * BN + 128 * hf + 32 * c,
-                                      f + 32 * c);
+                                      f + 32 * c, p.st32);
                 }
             }
         }
@@ -684,6 +700,13 @@ moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b
         tmSB = tmB;
     }
     if (MODE == MODE_WGRAD) a.m_tiles = a.M / C::TM;
+    {
+        // outputs are written in 32-byte row segments (at multiples of 32 elements) when every
+        // output base and row pitch allows it
+        auto al32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+        const bool pitch_ok = MODE == MODE_WGRAD ? (a.N % 32 == 0) : (a.ldo % 32 == 0);
+        a.st32 = pitch_ok && al32(a.out) && al32(a.out2) && al32(a.ab) && al32(a.h_bf16) ? 1 : 0;
+    }
     const size_t smem = smem_bytes_for<FP8, PAIR>(a.E);
     auto kern = grouped_gemm_kernel<MODE, FP8, PAIR>;
     // raise the kernel's dynamic shared-memory limit once per process and size (not a stream operation,

@@ -192,6 +192,14 @@ def test_backward_small_ragged(precision):
     _check_small(wl, _ids_from_sizes(T, 1, sizes), precision)
 
 
+def test_backward_mxfp8_wide_h_ragged():
+    """MXFP8 backward on a wider layer (H = 3584: 14 output tiles of the dx product)."""
+    sizes = (0, 37, 100, 1)
+    T = sum(sizes) + 3
+    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=3584, F=512, precision="mxfp8", act_std=0.3)
+    _check_small(wl, _ids_from_sizes(T, 1, sizes), "mxfp8")
+
+
 def test_backward_bf16_pair_tiles_ragged():
     """bf16 backward with groups large enough for 256-row CTA-pair tiles (dgrad, dx, wgrad)."""
     sizes = (300, 0, 1100, 513)

@@ -194,5 +194,14 @@ def test_gemm_mxfp8_ragged_groups(sizes):
     _check_mxfp8(_run(wl, "mxfp8", sizes=list(sizes)))
 
 
+def test_gemm_mxfp8_wide_h_ragged():
+    """A wider MXFP8 layer (H = 3584, seven scale boxes per row; 14 output tiles of the
+    down projection), every row of ragged groups checked."""
+    sizes = (0, 1, 127, 129, 300, 0, 3)
+    T = int(sum(sizes)) + 5
+    wl = W.get("tiny", T=T, E=len(sizes), K=1, H=3584, F=512, precision="mxfp8")
+    _check_mxfp8(_run(wl, "mxfp8", sizes=list(sizes)))
+
+
 def test_gemm_mxfp8_dsv3_sampled():
     _check_mxfp8(_run(W.get("dsv3"), "mxfp8", n_random=64))
