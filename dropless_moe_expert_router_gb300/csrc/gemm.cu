@@ -33,7 +33,7 @@
 //              commit hands the accumulator to the epilogue. For MXFP8 the warp
 //              first rearranges the k-block's scale words into the layout
 //              tcgen05.cp expects and copies them to TMEM.
-//   warp 10    (MXFP8) rearranges each landed stage's scale words for tcgen05.cp.
+//   warp 10    (MXFP8) rearranges each landed slot of scales (four k-blocks) for tcgen05.cp.
 //   warps 2-9  epilogue: two warps per TMEM lane quarter, each copying its half of
 //              the fp32 accumulator columns to registers with tcgen05.ld and
 //              handing TMEM back before the mode's math and stores (so with one
@@ -84,12 +84,16 @@ struct Cfg {
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows this CTA loads
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = B_ROWS * 128;
-    // scale landing zones: a TMA box of 16 scale bytes (four k-blocks) per operand row;
-    // the k-block's 32-bit word is then rearranged in place for tcgen05.cp
-    static constexpr int SFA_BYTES = FP8 ? BM * 16 : 0;
-    static constexpr int SFB_BYTES = FP8 ? BN * 16 : 0;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = PAIR ? 6 : 4;
+    // MXFP8 scales: one TMA box of 16 scale bytes (a group of four k-blocks) per operand row,
+    // loaded once per group into a ring of SF_SLOTS slots beside the operand stages; A rows
+    // first, then B rows. The scale warp rearranges a landed slot in place into four
+    // k-block chunks of SF_CHUNK bytes (A 512, B 2 x 512) laid out for tcgen05.cp.
+    static constexpr int SF_SLOTS = FP8 ? 2 : 0;
+    static constexpr int SF_SLOT_BYTES = FP8 ? (BM + BN) * 16 : 0;
+    static constexpr int SF_CHUNK = 3 * 512;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES + SF_SLOTS * SF_SLOT_BYTES;
     static constexpr int ACC_STAGES = FP8 ? 1 : 2;
     static constexpr int SF_COLS = 12;              // TMEM columns of one stage's scales (4 A + 8 B)
     static constexpr int THREADS = FP8 ? NUM_THREADS : NUM_THREADS - 32;  // the scale warp exists for MXFP8 only
@@ -119,7 +123,7 @@ struct GemmArgs {
 template <bool FP8, bool PAIR = false>
 constexpr size_t smem_bytes_for(int E) {
     using C = Cfg<FP8, PAIR>;
-    return 1024 /* alignment slack */ + (size_t)C::STAGES * C::STAGE_BYTES + 256 /* barriers, flags */ +
+    return 1024 /* alignment slack */ + (size_t)C::RING_BYTES + 256 /* barriers, flags */ +
            (size_t)C::THREADS * 4 + (size_t)2 * (E + 1) * 4;
 }
 
@@ -246,16 +250,19 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ring = smem;  // STAGES x [A | B | SFA | SFB]
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)STAGES * C::STAGE_BYTES);
+    uint8_t* ring = smem;  // STAGES x [A | B]
+    uint8_t* sfring = ring + (size_t)STAGES * C::STAGE_BYTES;  // MXFP8: SF_SLOTS x [A scales | B scales]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)C::RING_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
-    uint64_t* sfready = done + 1;   // MXFP8: a stage's scale words are rearranged for tcgen05.cp
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sfready + STAGES);
+    uint64_t* sf_full = done + 1;   // MXFP8 scale slots: landed / rearranged / free again
+    uint64_t* sf_ready = sf_full + 2;
+    uint64_t* sf_empty = sf_ready + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_empty + 2);
     volatile uint32_t* s_abort = s_tmem + 1;
-    int* s_part = reinterpret_cast<int*>(smem + (size_t)STAGES * C::STAGE_BYTES + 256);
+    int* s_part = reinterpret_cast<int*>(smem + (size_t)C::RING_BYTES + 256);
     int* s_goff = s_part + C::THREADS;
     int* s_mtp = s_goff + (p.E + 1);
 
@@ -273,7 +280,11 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         for (int s = 0; s < STAGES; s++) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
-            ptx::mbar_init(&sfready[s], 1);
+        }
+        for (int s = 0; s < 2; s++) {
+            ptx::mbar_init(&sf_full[s], 1);
+            ptx::mbar_init(&sf_ready[s], 1);
+            ptx::mbar_init(&sf_empty[s], 1);
         }
         for (int a = 0; a < 2; a++) {
             ptx::mbar_init(&tfull[a], 1);
@@ -345,15 +356,33 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         // ------------------------------------------------------------ producer
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0;
+        int issued = 0, sf_issued = 0;
+        int sslot = 0;
+        uint32_t sphase = 0;
         bool ok = true;
         for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
             const TileInfo ti = decode<MODE, FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
             for (int kb = 0; kb < ti.nkb; kb++) {
+                const int k = ti.k0 + kb * C::BK;
+                if constexpr (FP8) {
+                    if (kb == 0 || ((k / C::BK) & 3) == 0) {
+                        // first k-block of a scale group in this tile: the group's 16 scale bytes per row
+                        if (!ptx::wait_parity(&sf_empty[sslot], sphase ^ 1u, s_abort)) { ok = false; break; }
+                        if (lane == 0) {
+                            uint8_t* sf = sfring + (size_t)sslot * C::SF_SLOT_BYTES;
+                            const int kx = (k / 32) & ~15;
+                            ptx::mbar_arrive_expect_tx(&sf_full[sslot], C::SF_SLOT_BYTES);
+                            ptx::tma_load_2d(sf, &tmSA, &sf_full[sslot], kx, ti.a_row);
+                            ptx::tma_load_2d(sf + BM * 16, &tmSB, &sf_full[sslot], kx, ti.b_row);
+                        }
+                        __syncwarp();
+                        sf_issued++;
+                        if (++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1u; }
+                    }
+                }
                 if (!ptx::wait_parity(&empty[stage], phase ^ 1u, s_abort)) { ok = false; break; }
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
-                const int k = ti.k0 + kb * C::BK;
                 if (lane == 0) {
                     if constexpr (PAIR) {
                         // the even CTA's full barrier counts both CTAs' bytes
@@ -365,12 +394,6 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                         ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                         ptx::tma_load_2d(sa, &tmA, &full[stage], k, ti.a_row);
                         ptx::tma_load_2d(sb, &tmB, &full[stage], k, ti.b_row);
-                        if constexpr (FP8) {
-                            // 16 scale bytes per row (the 16-byte aligned group of four k-blocks holding this one)
-                            const int kx = (k / 32) & ~15;
-                            ptx::tma_load_2d(sb + C::B_BYTES, &tmSA, &full[stage], kx, ti.a_row);
-                            ptx::tma_load_2d(sb + C::B_BYTES + C::SFA_BYTES, &tmSB, &full[stage], kx, ti.b_row);
-                        }
                     }
                 }
                 __syncwarp();
@@ -385,6 +408,11 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 volatile uint32_t never = 0u;
                 ptx::wait_parity(&full[stage], phase, &never, 100000000ull);
             }
+            for (int i = 0; i < C::SF_SLOTS && i < sf_issued; i++) {
+                if (--sslot < 0) { sslot = C::SF_SLOTS - 1; sphase ^= 1u; }
+                volatile uint32_t never = 0u;
+                ptx::wait_parity(&sf_full[sslot], sphase, &never, 100000000ull);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA of a pair)
@@ -392,32 +420,43 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int sslot = 0;
+        uint32_t sphase = 0;
         bool ok = leader;
         for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
             const int nkb =
                 MODE == MODE_WGRAD ? decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank).nkb : p.Kdim / C::BK;
+            const int k0b = tile_k0_div128<MODE>(p, tile, s_goff);
             if (!ptx::wait_parity(&tempty[acc], acc_phase ^ 1u, s_abort)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
             for (int kb = 0; kb < nkb; kb++) {
-                // MXFP8: the scale warp signals once the stage has landed and its scales are rearranged
-                if (!ptx::wait_parity(FP8 ? &sfready[stage] : &full[stage], phase, s_abort)) { ok = false; break; }
+                const int gk = k0b + kb;                 // k-block index along the contraction
+                if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
+                // MXFP8: the group's scales, rearranged by the scale warp
+                if (FP8 && (kb == 0 || (gk & 3) == 0) && !ptx::wait_parity(&sf_ready[sslot], sphase, s_abort)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
+                const bool group_end = kb == nkb - 1 || (gk & 3) == 3;
                 if (lane == 0) {
                     const uint32_t a0 = ptx::smem_addr(sa), b0 = ptx::smem_addr(sb);
                     if constexpr (FP8) {
                         const uint32_t sf_t = tmem + (uint32_t)(BN + stage * C::SF_COLS);
-                        const uint32_t sfa_s = ptx::smem_addr(sb + C::B_BYTES);
+                        const uint32_t sfa_s =
+                            ptx::smem_addr(sfring + (size_t)sslot * C::SF_SLOT_BYTES + (gk & 3) * C::SF_CHUNK);
                         ptx::tc_cp_32x128b_warpx4(sf_t, ptx::sdesc_plain(sfa_s));
-                        ptx::tc_cp_32x128b_warpx4(sf_t + 4, ptx::sdesc_plain(sfa_s + C::SFA_BYTES));
-                        ptx::tc_cp_32x128b_warpx4(sf_t + 8, ptx::sdesc_plain(sfa_s + C::SFA_BYTES + 512));
+                        ptx::tc_cp_32x128b_warpx4(sf_t + 4, ptx::sdesc_plain(sfa_s + 512));
+                        ptx::tc_cp_32x128b_warpx4(sf_t + 8, ptx::sdesc_plain(sfa_s + 1024));
 #pragma unroll
                         for (int k = 0; k < C::KSTEPS; k++)
                             ptx::mma_mxf8(d_tmem, ptx::sdesc_k_sw128(a0 + k * 32), ptx::sdesc_k_sw128(b0 + k * 32),
                                           ptx::idesc_mxf8(BM, BN, k, k), sf_t, sf_t + 4, (kb | k) != 0);
                         ptx::tc_commit(&empty[stage]);
+                        if (group_end) ptx::tc_commit(&sf_empty[sslot]);  // the slot's last copies are done
                     } else if constexpr (PAIR) {
 #pragma unroll
                         for (int k = 0; k < C::KSTEPS; k++)
@@ -435,6 +474,7 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 }
                 __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (FP8 && group_end && ++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1u; }
             }
             if (!ok) break;
             if (lane == 0) {
@@ -456,40 +496,42 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         }
     } else if (FP8 && warp == 10) {
         // ------------------------------------------------------------ scale warp (MXFP8)
-        // Rearranges each landed stage's scale words for tcgen05.cp .32x128b -- word
-        // (lane*4 + j) of a 512-byte chunk must hold row 32*j + lane of that chunk -- in
-        // place (the landing zone holds 16 bytes, four k-blocks, per row), then releases
-        // the stage to the MMA warp. Runs ahead of the MMA issue, off its critical path.
+        // Rearranges each landed scale slot for tcgen05.cp .32x128b: the slot holds 16 bytes
+        // (the words of four k-blocks) per row; k-block w's chunk at w * SF_CHUNK holds the A
+        // rows (word lane*4 + j = row 32 j + lane) and then the B rows 0-127 and 128-255 in
+        // the same order. Done in place, ahead of the MMA issue, off its critical path.
         if constexpr (FP8) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int sslot = 0;
+            uint32_t sphase = 0;
             bool ok = true;
             for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
                 const int nkb = MODE == MODE_WGRAD ? decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank).nkb : p.Kdim / C::BK;
                 const int k0b = tile_k0_div128<MODE>(p, tile, s_goff);
                 for (int kb = 0; kb < nkb; kb++) {
-                    if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
-                    uint8_t* sb = ring + (size_t)stage * C::STAGE_BYTES + C::A_BYTES;
-                    const int w = (k0b + kb) & 3;
-                    const uint32_t* la = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES);
-                    const uint32_t* lb = reinterpret_cast<const uint32_t*>(sb + C::B_BYTES + C::SFA_BYTES);
-                    uint32_t va[4], vb0[4], vb1[4];
+                    if (kb != 0 && ((k0b + kb) & 3) != 0) continue;   // not the first k-block of a group
+                    if (!ptx::wait_parity(&sf_full[sslot], sphase, s_abort)) { ok = false; break; }
+                    uint8_t* sf = sfring + (size_t)sslot * C::SF_SLOT_BYTES;
+                    const uint4* la = reinterpret_cast<const uint4*>(sf);
+                    const uint4* lb = reinterpret_cast<const uint4*>(sf + BM * 16);
+                    uint4 va[4], vb[8];
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        va[j] = la[(32 * j + lane) * 4 + w];
-                        vb0[j] = lb[(32 * j + lane) * 4 + w];
-                        vb1[j] = lb[(128 + 32 * j + lane) * 4 + w];
-                    }
+                    for (int j = 0; j < 4; j++) va[j] = la[32 * j + lane];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) vb[j] = lb[32 * j + lane];
                     __syncwarp();
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES)[lane] = make_uint4(va[0], va[1], va[2], va[3]);
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES)[lane] =
-                        make_uint4(vb0[0], vb0[1], vb0[2], vb0[3]);
-                    reinterpret_cast<uint4*>(sb + C::B_BYTES + C::SFA_BYTES + 512)[lane] =
-                        make_uint4(vb1[0], vb1[1], vb1[2], vb1[3]);
+                    uint4* out = reinterpret_cast<uint4*>(sf);
+#pragma unroll
+                    for (int w = 0; w < 4; w++) {
+                        auto word = [w](const uint4& v) { return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w; };
+                        uint4* chunk = out + w * (C::SF_CHUNK / 16);
+                        chunk[lane] = make_uint4(word(va[0]), word(va[1]), word(va[2]), word(va[3]));
+                        chunk[32 + lane] = make_uint4(word(vb[0]), word(vb[1]), word(vb[2]), word(vb[3]));
+                        chunk[64 + lane] = make_uint4(word(vb[4]), word(vb[5]), word(vb[6]), word(vb[7]));
+                    }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&sfready[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (lane == 0) ptx::mbar_arrive(&sf_ready[sslot]);
+                    if (++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1u; }
                 }
             }
         }
