@@ -87,10 +87,11 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = PAIR ? 6 : 4;
     // MXFP8 scales: one TMA box of 16 scale bytes (a group of four k-blocks) per operand row,
-    // loaded once per group into a ring of SF_SLOTS slots beside the operand stages; A rows
-    // first, then B rows. The scale warp rearranges a landed slot in place into four
-    // k-block chunks of SF_CHUNK bytes (A 512, B 2 x 512) laid out for tcgen05.cp.
-    static constexpr int SF_SLOTS = FP8 ? 2 : 0;
+    // loaded once per group by the scale warp, up to SF_SLOTS groups ahead of the MMA warp,
+    // into a ring of slots beside the operand stages; A rows first, then B rows. The scale
+    // warp rearranges a landed slot in place into four k-block chunks of SF_CHUNK bytes
+    // (A 512, B 2 x 512) laid out for tcgen05.cp.
+    static constexpr int SF_SLOTS = FP8 ? 3 : 0;
     static constexpr int SF_SLOT_BYTES = FP8 ? (BM + BN) * 16 : 0;
     static constexpr int SF_CHUNK = 3 * 512;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES + SF_SLOTS * SF_SLOT_BYTES;
@@ -258,9 +259,9 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
     uint64_t* sf_full = done + 1;   // MXFP8 scale slots: landed / rearranged / free again
-    uint64_t* sf_ready = sf_full + 2;
-    uint64_t* sf_empty = sf_ready + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_empty + 2);
+    uint64_t* sf_ready = sf_full + 3;
+    uint64_t* sf_empty = sf_ready + 3;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sf_empty + 3);
     volatile uint32_t* s_abort = s_tmem + 1;
     int* s_part = reinterpret_cast<int*>(smem + (size_t)C::RING_BYTES + 256);
     int* s_goff = s_part + C::THREADS;
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < 2; s++) {
+        for (int s = 0; s < 3; s++) {
             ptx::mbar_init(&sf_full[s], 1);
             ptx::mbar_init(&sf_ready[s], 1);
             ptx::mbar_init(&sf_empty[s], 1);
@@ -356,30 +357,12 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         // ------------------------------------------------------------ producer
         int stage = 0;
         uint32_t phase = 0;
-        int issued = 0, sf_issued = 0;
-        int sslot = 0;
-        uint32_t sphase = 0;
+        int issued = 0;
         bool ok = true;
         for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
             const TileInfo ti = decode<MODE, FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
             for (int kb = 0; kb < ti.nkb; kb++) {
                 const int k = ti.k0 + kb * C::BK;
-                if constexpr (FP8) {
-                    if (kb == 0 || ((k / C::BK) & 3) == 0) {
-                        // first k-block of a scale group in this tile: the group's 16 scale bytes per row
-                        if (!ptx::wait_parity(&sf_empty[sslot], sphase ^ 1u, s_abort)) { ok = false; break; }
-                        if (lane == 0) {
-                            uint8_t* sf = sfring + (size_t)sslot * C::SF_SLOT_BYTES;
-                            const int kx = (k / 32) & ~15;
-                            ptx::mbar_arrive_expect_tx(&sf_full[sslot], C::SF_SLOT_BYTES);
-                            ptx::tma_load_2d(sf, &tmSA, &sf_full[sslot], kx, ti.a_row);
-                            ptx::tma_load_2d(sf + BM * 16, &tmSB, &sf_full[sslot], kx, ti.b_row);
-                        }
-                        __syncwarp();
-                        sf_issued++;
-                        if (++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1u; }
-                    }
-                }
                 if (!ptx::wait_parity(&empty[stage], phase ^ 1u, s_abort)) { ok = false; break; }
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
@@ -407,11 +390,6 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
                 volatile uint32_t never = 0u;
                 ptx::wait_parity(&full[stage], phase, &never, 100000000ull);
-            }
-            for (int i = 0; i < C::SF_SLOTS && i < sf_issued; i++) {
-                if (--sslot < 0) { sslot = C::SF_SLOTS - 1; sphase ^= 1u; }
-                volatile uint32_t never = 0u;
-                ptx::wait_parity(&sf_full[sslot], sphase, &never, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -496,21 +474,60 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         }
     } else if (FP8 && warp == 10) {
         // ------------------------------------------------------------ scale warp (MXFP8)
-        // Rearranges each landed scale slot for tcgen05.cp .32x128b: the slot holds 16 bytes
-        // (the words of four k-blocks) per row; k-block w's chunk at w * SF_CHUNK holds the A
-        // rows (word lane*4 + j = row 32 j + lane) and then the B rows 0-127 and 128-255 in
-        // the same order. Done in place, ahead of the MMA issue, off its critical path.
+        // Loads this CTA's scale groups (the 16 scale bytes per row of a group of four
+        // k-blocks), up to SF_SLOTS groups ahead of the MMA warp, and rearranges each landed
+        // slot for tcgen05.cp .32x128b: k-block w's chunk at w * SF_CHUNK holds the A rows
+        // (word lane*4 + j = row 32 j + lane) and then the B rows 0-127 and 128-255 in the
+        // same order. In place, off the MMA warp's critical path. Groups are walked in the
+        // MMA warp's order: every tile with k-blocks, a group starting at its first k-block
+        // and at every k-block index that is a multiple of four.
         if constexpr (FP8) {
-            int sslot = 0;
-            uint32_t sphase = 0;
-            bool ok = true;
-            for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
-                const int nkb = MODE == MODE_WGRAD ? decode_wgrad<FP8, PAIR>(tile, s_goff, p, rank).nkb : p.Kdim / C::BK;
-                const int k0b = tile_k0_div128<MODE>(p, tile, s_goff);
-                for (int kb = 0; kb < nkb; kb++) {
-                    if (kb != 0 && ((k0b + kb) & 3) != 0) continue;   // not the first k-block of a group
-                    if (!ptx::wait_parity(&sf_full[sslot], sphase, s_abort)) { ok = false; break; }
-                    uint8_t* sf = sfring + (size_t)sslot * C::SF_SLOT_BYTES;
+            struct Cursor {
+                int tile, kb;
+                TileInfo ti;
+            };
+            auto first_from = [&](int tile) {
+                Cursor c;
+                c.tile = tile;
+                c.kb = 0;
+                for (; c.tile < total_tiles; c.tile += tile_step) {
+                    c.ti = decode<MODE, FP8, PAIR>(c.tile, s_mtp, s_goff, p, rank);
+                    if (c.ti.nkb > 0) break;
+                }
+                return c;
+            };
+            auto next_group = [&](Cursor c) {
+                c.kb += 4 - ((c.ti.k0 / C::BK + c.kb) & 3);
+                return c.kb < c.ti.nkb ? c : first_from(c.tile + tile_step);
+            };
+            Cursor ld = first_from(tile0), pr = ld;
+            int ld_slot = 0, pr_slot = 0, loaded = 0;   // loaded: issued and not yet rearranged
+            uint32_t ld_phase = 0, pr_phase = 0;
+            // Neither step blocks the other (non-blocking barrier tests): a load is issued when its
+            // slot is free again (the MMA warp finished the group it held) and a landed group is
+            // rearranged at once, so the groups after the one in use are always ready or in flight.
+            uint64_t t_idle = ptx::globaltimer_ns();
+            while (pr.tile < total_tiles) {
+                bool progress = false;
+                // (every lane polls, so each has acquired what it reads; the branch is taken only
+                // when all lanes saw the phase complete, keeping the warp converged)
+                if (ld.tile < total_tiles && loaded < C::SF_SLOTS &&
+                    __all_sync(FULL, ptx::mbar_test_wait(&sf_empty[ld_slot], ld_phase ^ 1u))) {
+                    if (lane == 0) {
+                        uint8_t* sf = sfring + (size_t)ld_slot * C::SF_SLOT_BYTES;
+                        const int kx = ((ld.ti.k0 + ld.kb * C::BK) / 32) & ~15;
+                        ptx::mbar_arrive_expect_tx(&sf_full[ld_slot], C::SF_SLOT_BYTES);
+                        ptx::tma_load_2d(sf, &tmSA, &sf_full[ld_slot], kx, ld.ti.a_row);
+                        ptx::tma_load_2d(sf + BM * 16, &tmSB, &sf_full[ld_slot], kx, ld.ti.b_row);
+                    }
+                    __syncwarp();
+                    loaded++;
+                    ld = next_group(ld);
+                    if (++ld_slot == C::SF_SLOTS) { ld_slot = 0; ld_phase ^= 1u; }
+                    progress = true;
+                }
+                if (loaded > 0 && __all_sync(FULL, ptx::mbar_test_wait(&sf_full[pr_slot], pr_phase))) {
+                    uint8_t* sf = sfring + (size_t)pr_slot * C::SF_SLOT_BYTES;
                     const uint4* la = reinterpret_cast<const uint4*>(sf);
                     const uint4* lb = reinterpret_cast<const uint4*>(sf + BM * 16);
                     uint4 va[4], vb[8];
@@ -530,9 +547,28 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&sf_ready[sslot]);
-                    if (++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1u; }
+                    if (lane == 0) ptx::mbar_arrive(&sf_ready[pr_slot]);
+                    loaded--;
+                    pr = next_group(pr);
+                    if (++pr_slot == C::SF_SLOTS) { pr_slot = 0; pr_phase ^= 1u; }
+                    progress = true;
                 }
+                // bounded: give up (and flag it) when nothing has moved for the wait limit
+                if (progress) {
+                    t_idle = ptx::globaltimer_ns();
+                } else if (__nanosleep(64), *s_abort) {
+                    break;
+                } else if (ptx::globaltimer_ns() - t_idle > ptx::WAIT_LIMIT_NS) {
+                    *s_abort = 1u;
+                    raise_device_error(MOE_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+            // give the scale loads still in flight a bounded chance to land before the CTA exits
+            for (int i = 0; i < loaded; i++) {
+                volatile uint32_t never = 0u;
+                ptx::wait_parity(&sf_full[pr_slot], pr_phase, &never, 100000000ull);
+                if (++pr_slot == C::SF_SLOTS) { pr_slot = 0; pr_phase ^= 1u; }
             }
         }
     } else {
@@ -614,30 +650,46 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                     }
                 }
             } else if constexpr (MODE == MODE_DGRAD) {
-                // dh columns fc = n*256 + 128 hf + 32c + i; (a | b) and (da | db) interleaved per 128
+                // dh columns fc = n*256 + 128 hf + 32c + i; (a | b) and (da | db) interleaved per 128.
+                // The saved (a | b) is read-only here: a chunk's eight 16-byte loads are issued
+                // before its math, one memory round trip per chunk of 32 columns.
                 if (valid) {
                     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
                         const int fc = ti.n * BN + 128 * hf + 32 * c;
                         const long long off = r * p.ldo + (long long)(fc / 128) * 256 + (fc % 128);
+                        const uint4* src = reinterpret_cast<const uint4*>(p.ab + off);
+                        uint4 av[4], bv[4];
 #pragma unroll
                         for (int sbk = 0; sbk < 4; sbk++) {
-                            const uint4 av = *reinterpret_cast<const uint4*>(p.ab + off + 8 * sbk);
-                            const uint4 bv = *reinterpret_cast<const uint4*>(p.ab + off + 128 + 8 * sbk);
-                            float a[8], b[8], da[8], db[8];
-                            bf16x8_to_f32(av, a);
-                            bf16x8_to_f32(bv, b);
-#pragma unroll
-                            for (int i = 0; i < 8; i++) {
-                                const float dh = f[32 * c + 8 * sbk + i];
-                                const float sg = __fdividef(1.0f, 1.0f + __expf(-a[i]));
-                                da[i] = dh * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
-                                db[i] = dh * a[i] * sg;
-                            }
-                            *reinterpret_cast<uint4*>(o + off + 8 * sbk) = f32_to_bf16x8(da);
-                            *reinterpret_cast<uint4*>(o + off + 128 + 8 * sbk) = f32_to_bf16x8(db);
+                            av[sbk] = __ldg(src + sbk);
+                            bv[sbk] = __ldg(src + 16 + sbk);   // + 128 elements
                         }
+                        uint32_t wa[16], wb[16];
+#pragma unroll
+                        for (int sbk = 0; sbk < 4; sbk++) {
+                            float a[8], b[8];
+                            bf16x8_to_f32(av[sbk], a);
+                            bf16x8_to_f32(bv[sbk], b);
+#pragma unroll
+                            for (int i = 0; i < 8; i += 2) {
+                                float da2[2], db2[2];
+#pragma unroll
+                                for (int u = 0; u < 2; u++) {
+                                    const float dh = f[32 * c + 8 * sbk + i + u];
+                                    const float sg = __fdividef(1.0f, 1.0f + __expf(-a[i + u]));
+                                    da2[u] = dh * b[i + u] * (sg * (1.0f + a[i + u] * (1.0f - sg)));
+                                    db2[u] = dh * a[i + u] * sg;
+                                }
+                                wa[4 * sbk + i / 2] = pack_bf16x2(da2[0], da2[1]);
+                                wb[4 * sbk + i / 2] = pack_bf16x2(db2[0], db2[1]);
+                            }
+                        }
+                        store_32B(o + off, wa, p.st32);
+                        store_32B(o + off + 16, wa + 8, p.st32);
+                        store_32B(o + off + 128, wb, p.st32);
+                        store_32B(o + off + 144, wb + 8, p.st32);
                     }
                 }
             } else if constexpr (MODE == MODE_WGRAD) {

@@ -63,27 +63,36 @@ __global__ void perm_rank_kernel(const void* __restrict__ ids, bool i16, int T, 
     long long i1 = (long long)(tile + 1) * TT * K;
     const long long nroutes = (long long)T * K;
     if (i1 > nroutes) i1 = nroutes;
-    for (long long c = i0; c < i1; c += 32) {
-        long long i = c + lane;
-        int e = -1;
-        if (i < i1) {
-            e = load_id(ids, i, i16);
-            if (e < -1 || e >= E) {
+    // U rows of 32 routes are loaded before any is ranked: one memory latency per 32 U routes
+    constexpr int U = 16;
+    for (long long c0 = i0; c0 < i1; c0 += 32 * U) {
+        int ev[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const long long i = c0 + u * 32 + lane;
+            ev[u] = i < i1 ? load_id(ids, i, i16) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            if (c0 + u * 32 >= i1) break;   // warp-uniform
+            const long long i = c0 + u * 32 + lane;
+            int e = ev[u];
+            if (i < i1 && (e < -1 || e >= E)) {
                 raise_device_error(MOE_DEVERR_BAD_ID);
                 e = -1;
             }
+            const unsigned grp = __match_any_sync(FULL, e);
+            const int leader = __ffs(grp) - 1;
+            const int rk = __popc(grp & lanemask_lt());
+            int old = 0;
+            if (lane == leader && e >= 0) {
+                old = cnt[e];
+                cnt[e] = old + __popc(grp);
+            }
+            old = __shfl_sync(FULL, old, leader);
+            if (i < i1) row_map[i] = (e >= 0) ? old + rk : -1;
+            __syncwarp();
         }
-        unsigned grp = __match_any_sync(FULL, e);
-        int leader = __ffs(grp) - 1;
-        int rk = __popc(grp & lanemask_lt());
-        int old = 0;
-        if (lane == leader && e >= 0) {
-            old = cnt[e];
-            cnt[e] = old + __popc(grp);
-        }
-        old = __shfl_sync(FULL, old, leader);
-        if (i < i1) row_map[i] = (e >= 0) ? old + rk : -1;
-        __syncwarp();
     }
     for (int e = lane; e < E; e += 32) table[(size_t)e * tiles + tile] = cnt[e];
 }
