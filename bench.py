@@ -49,8 +49,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the dominant kernel, from an ncu capture,
 # keyed by the hash of the kernel's sources; a changed kernel reports null.
 TRAFFIC_BY_SOURCE = {
-    # Mixtral-like GEMM up: 2.01 GB read + 0.456 GB written (profiles/grouped_gemm_bf16_mixtral_dram.md)
-    "9c30eb1ff9c2a7e5": 2.01e9 + 0.45649e9,
+    # Mixtral-like GEMM up: 2.120 GB read + 0.461 GB written (ncu dram__bytes_read.sum / _write.sum, full size)
+    "4a49a83d2f2672ec": 2.11978e9 + 0.46091e9,
 }
 
 

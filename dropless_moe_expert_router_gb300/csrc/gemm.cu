@@ -209,9 +209,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Epilogue outputs are streamed (evict-first in L2): the operand tiles that the other CTAs
+// are about to re-read stay resident instead.
 // One 32-byte global store (dst 32-byte aligned): a whole sector per thread.
 __device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* w) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
                  "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
 }
@@ -222,8 +224,8 @@ __device__ __forceinline__ void store_32B(void* dst, const uint32_t* w, bool st3
         st_global_32B(dst, w);
     } else {
         uint4* d = reinterpret_cast<uint4*>(dst);
-        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        __stcs(d, make_uint4(w[0], w[1], w[2], w[3]));
+        __stcs(d + 1, make_uint4(w[4], w[5], w[6], w[7]));
     }
 }
 
