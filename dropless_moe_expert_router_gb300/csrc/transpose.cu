@@ -26,6 +26,24 @@ namespace {
 constexpr int TR_ROWS = 128;  // padded rows per block
 constexpr int TR_COLS = 64;   // columns per block
 
+// Shared tile: row r starts at element r * 72 + (r / 32) * 16 -- rows of 144 bytes (16-byte
+// vector access) and an 8-word skew per 32 rows, so that the column reads of the quantiser
+// (4 columns x the four 32-row blocks per warp instruction) fall in 16 distinct banks.
+constexpr int TR_STRIDE = TR_COLS + 8;
+constexpr int TR_TILE = TR_ROWS * TR_STRIDE + (TR_ROWS / 32) * 16;
+__device__ __forceinline__ int tr_row(int r) { return r * TR_STRIDE + (r >> 5) * 16; }
+
+// 16-byte asynchronous global -> shared copies (the next column chunk streams in while the
+// current one is quantised and stored).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Last e with e + goff[e] / 128 <= pb (the function is strictly increasing in e),
 // by a 32-way search of one warp: each round narrows [lo, hi] by a factor of 32.
 __device__ __forceinline__ int find_group_warp(const int* __restrict__ goff, int E, int pb, int lane) {
@@ -45,13 +63,13 @@ __device__ __forceinline__ int find_group_warp(const int* __restrict__ goff, int
 }
 
 // Block = one 128-row block of the padded axis x CHUNKS column chunks of 64.
-template <bool FP8, int CHUNKS>
+template <bool FP8, int CHUNKS, bool SCALE_WORDS>
 __global__ void __launch_bounds__(256) grouped_transpose_kernel(const __nv_bfloat16* __restrict__ x,
                                                                 const int* __restrict__ src_rows, int C,
                                                                 const int* __restrict__ goff, int E, int kpad,
                                                                 void* __restrict__ xT,
                                                                 uint8_t* __restrict__ xT_scales) {
-    __shared__ __align__(16) __nv_bfloat16 tile[TR_ROWS][TR_COLS + 8];  // rows of 144 B: 16-byte vector access
+    __shared__ __align__(16) __nv_bfloat16 tiles[2][TR_TILE];   // double buffer over the column chunks
     __shared__ int s_base, s_valid;
     __shared__ int s_src[TR_ROWS];
     const int pb = blockIdx.x;  // 128-row block of the padded axis
@@ -74,16 +92,28 @@ __global__ void __launch_bounds__(256) grouped_transpose_kernel(const __nv_bfloa
     const int valid = s_valid;
     if (valid < 0) return;  // padding that no GEMM reads
     const long long kcol = (long long)TR_ROWS * pb;  // first padded column of this block
-    for (int ck = 0; ck < CHUNKS; ck++) {
+    // load 128 rows x 64 columns of chunk ck into buffer ck & 1 (16-byte pieces; rows past the group are zeros)
+    auto issue = [&](int ck) {
+        __nv_bfloat16* t = tiles[ck & 1];
         const int c0 = (blockIdx.y * CHUNKS + ck) * TR_COLS;
-        if (ck > 0) __syncthreads();   // the previous chunk's readers are done with the tile
-        // load 128 rows x 64 columns (16-byte chunks; rows past the group are zeros)
         for (int i = threadIdx.x; i < TR_ROWS * (TR_COLS / 8); i += blockDim.x) {
             const int r = i / (TR_COLS / 8), ch = i % (TR_COLS / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
             const int c = c0 + ch * 8;
-            if (r < valid && c < C) v = *reinterpret_cast<const uint4*>(x + (long long)s_src[r] * C + c);
-            *reinterpret_cast<uint4*>(&tile[r][ch * 8]) = v;
+            void* dst = &t[tr_row(r) + ch * 8];
+            if (r < valid && c < C) cp_async16(dst, x + (long long)s_src[r] * C + c);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+    };
+    issue(0);
+    for (int ck = 0; ck < CHUNKS; ck++) {
+        const int c0 = (blockIdx.y * CHUNKS + ck) * TR_COLS;
+        const __nv_bfloat16* tile = tiles[ck & 1];
+        if (ck + 1 < CHUNKS) {
+            issue(ck + 1);            // its buffer's previous readers finished at the end of iteration ck - 1
+            cp_async_wait<1>();       // chunk ck has landed (this thread's part)
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
         if (!FP8) {
@@ -94,36 +124,46 @@ __global__ void __launch_bounds__(256) grouped_transpose_kernel(const __nv_bfloa
                 if (c >= C) continue;
                 float f[8];
 #pragma unroll
-                for (int j = 0; j < 8; j++) f[j] = __bfloat162float(tile[ch * 8 + j][cc]);
+                for (int j = 0; j < 8; j++) f[j] = __bfloat162float(tile[tr_row(ch * 8 + j) + cc]);
                 reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(xT) + (long long)c * kpad + kcol)[ch] =
                     f32_to_bf16x8(f);
             }
         } else {
-            // thread = (column, 32-row block)
-            const int cc = threadIdx.x % TR_COLS, sbk = threadIdx.x / TR_COLS;  // sbk in [0, 4)
+            // thread = (column cc = t / 4, 32-row block sbk = t % 4): the four threads of a column
+            // write its 128 contiguous output bytes, and one word holds its four scale bytes
+            const int cc = threadIdx.x >> 2, sbk = threadIdx.x & 3;
             const int c = c0 + cc;
+            float v[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                v[i] = __bfloat162float(tile[tr_row(32 * sbk + i) + cc]);
+                amax = fmaxf(amax, fabsf(v[i]));
+            }
+            const int sb = e8m0_scale_byte(amax);
+            const float inv = e8m0_inv_scale(sb);
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                w[i] = (uint32_t)f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+                       ((uint32_t)f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+            uint32_t sw = (uint32_t)sb << (8 * sbk);
+            sw |= __shfl_xor_sync(FULL, sw, 1);
+            sw |= __shfl_xor_sync(FULL, sw, 2);
             if (c < C) {
-                float v[32];
-                float amax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    v[i] = __bfloat162float(tile[32 * sbk + i][cc]);
-                    amax = fmaxf(amax, fabsf(v[i]));
-                }
-                const int sb = e8m0_scale_byte(amax);
-                const float inv = e8m0_inv_scale(sb);
-                uint32_t w[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    w[i] = (uint32_t)f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
-                           ((uint32_t)f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
                 uint4* d =
                     reinterpret_cast<uint4*>(static_cast<uint8_t*>(xT) + (long long)c * kpad + kcol + 32 * sbk);
                 d[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                xT_scales[(long long)c * (kpad / 32) + kcol / 32 + sbk] = (uint8_t)sb;
+                uint8_t* srow = xT_scales + (long long)c * (kpad / 32) + kcol / 32;
+                if (SCALE_WORDS) {
+                    if (sbk == 0) *reinterpret_cast<uint32_t*>(srow) = sw;
+                } else {
+                    srow[sbk] = (uint8_t)sb;
+                }
             }
         }
+        __syncthreads();   // this buffer is refilled by the issue of iteration ck + 1
     }
 }
 
@@ -147,14 +187,22 @@ extern "C" moe_status moe_grouped_transpose(const void* x, const int32_t* src_ro
     cudaStream_t s = moe_host::as_stream(stream);
     const unsigned gx = (unsigned)(kpad / TR_ROWS);
     const auto* xb = (const __nv_bfloat16*)x;
+    // scale rows start at multiples of 4 bytes (kpad / 32 and kcol / 32 are): word stores when the base allows
+    const bool words = fp8 && moe_host::aligned(xT_scales, 4);
+#define MOE_TRANSPOSE(f8, ch, sw)                                                                          \
+    grouped_transpose_kernel<f8, ch, sw><<<grid, 256, 0, s>>>(xb, src_rows, C, group_offsets, E, (int)kpad, xT, \
+                                                              f8 ? xT_scales : nullptr)
     if (C % (4 * TR_COLS) == 0) {
         dim3 grid(gx, (unsigned)(C / (4 * TR_COLS)));
-        if (fp8) grouped_transpose_kernel<true, 4><<<grid, 256, 0, s>>>(xb, src_rows, C, group_offsets, E, (int)kpad, xT, xT_scales);
-        else grouped_transpose_kernel<false, 4><<<grid, 256, 0, s>>>(xb, src_rows, C, group_offsets, E, (int)kpad, xT, nullptr);
+        if (!fp8) MOE_TRANSPOSE(false, 4, false);
+        else if (words) MOE_TRANSPOSE(true, 4, true);
+        else MOE_TRANSPOSE(true, 4, false);
     } else {
         dim3 grid(gx, (unsigned)(C / TR_COLS));
-        if (fp8) grouped_transpose_kernel<true, 1><<<grid, 256, 0, s>>>(xb, src_rows, C, group_offsets, E, (int)kpad, xT, xT_scales);
-        else grouped_transpose_kernel<false, 1><<<grid, 256, 0, s>>>(xb, src_rows, C, group_offsets, E, (int)kpad, xT, nullptr);
+        if (!fp8) MOE_TRANSPOSE(false, 1, false);
+        else if (words) MOE_TRANSPOSE(true, 1, true);
+        else MOE_TRANSPOSE(true, 1, false);
     }
+#undef MOE_TRANSPOSE
     return moe_host::launch_status();
 }
