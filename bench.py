@@ -261,11 +261,12 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     errs = api.moe_get_device_errors()
     R = int(layer.perm.group_offsets[-1].item())
+    active = int((layer.perm.group_sizes > 0).sum().item())      # experts that received routes
     launches = MoELayer.LAUNCHES_PER_FORWARD + (layer.launches_per_backward if wl.backward else 0)
 
     if world > 1:
         total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)
-    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, clocks=clocks, R=R, errs=errs,
+    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, clocks=clocks, R=R, active=active, errs=errs,
                 h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2, launches=K * launches)
 
 
@@ -283,18 +284,26 @@ def whole_job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, ma
     return world * tokens_per_rank_step * steps / (max_total_ms / 1e3)
 
 
-def stage_report(wl, R, stage_ms):
-    """Algorithmic bytes / FLOPs of each stage (minimum traffic, not counters)."""
+def stage_report(wl, R, stage_ms, active=None):
+    """Algorithmic bytes / FLOPs of each stage (minimum traffic, not counters). GEMM bytes:
+    operands read once (weights of the experts with routes), outputs written once."""
     T, H, E, K, F = wl.T, wl.H, wl.E, wl.K, wl.F
+    Ea = E if active is None else active
     idb = 2 if wl.id_bits == 16 else 4
     fp8 = wl.precision == "mxfp8"
     b_out = 1 if fp8 else 2
+    q = (1 + 1 / 32) if fp8 else 2           # bytes per operand element (MXFP8: code + scale share)
     bytes_ = {
         "route": T * E * 4 + T * K * (idb + 4),
         "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
         "combine": R * H * 2 + T * K * 8 + T * H * 2,
         # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands
         "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
+        "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * q,
+        "gemm_down": R * F * q + Ea * F * H * q + R * H * 2,
+        "dgrad_dh": R * H * q + Ea * F * H * q + R * 2 * F * 2 * 2,
+        "dgrad_dx": R * 2 * F * q + Ea * 2 * F * H * q + R * H * 2,
+        "wgrad_gemm": R * (F + H + H + 2 * F) * q + Ea * 3 * H * F * 2,
     }
     flops = {"gemm_up": 4.0 * R * H * F, "gemm_down": 2.0 * R * H * F, "dgrad_dh": 2.0 * R * H * F,
              "dgrad_dx": 4.0 * R * H * F, "wgrad_gemm": 6.0 * R * H * F}
@@ -306,7 +315,7 @@ def stage_report(wl, R, stage_ms):
         if n in flops:
             d["TFLOP/s"] = round(flops[n] / (ms * 1e-3) / 1e12, 1)
         out[n] = d
-    return out, flops
+    return out, flops, bytes_
 
 
 def main():
@@ -367,17 +376,23 @@ def main():
 
     r = run_ours(args, wl, rank, world, local_rank)
     peaks, peak_kind = load_peaks()
-    stages, flops = stage_report(wl, r["R"], r["stage_ms"])
+    stages, flops, gbytes = stage_report(wl, r["R"], r["stage_ms"], r["active"])
     # dominant kernel: the GEMM stage with the largest time (one kernel launch per stage)
     dom = max((n for n in flops if n in r["stage_ms"] and n != "wgrad_gemm" and n != "dgrad_dx"),
               key=lambda n: r["stage_ms"][n])
-    achieved = flops[dom] / (r["stage_ms"][dom] * 1e-3) / 1e12
     fp8_ratio = 2.0 if wl.precision == "mxfp8" else 1.0
     # The timed loop is well under a second and the SM clock stays at its maximum
     # (see "clocks"), the conditions of the burst measurement: report against the
     # burst peak, and the sustained figure beside it.
     peak = peaks["bf16_tflops"] * fp8_ratio
     peak_sustained = peaks["bf16_tflops_sustained"] * fp8_ratio
+    # the bound is whichever peak the algorithmic work needs longer for: tensor (FLOPs) or HBM (bytes)
+    hbm_bound = gbytes[dom] / (peaks["hbm_gbs"] * 1e9) > flops[dom] / (peak * 1e12)
+    if hbm_bound:
+        achieved = gbytes[dom] / (r["stage_ms"][dom] * 1e-3) / 1e9
+        peak, peak_sustained = peaks["hbm_gbs"], peaks["hbm_gbs"]
+    else:
+        achieved = flops[dom] / (r["stage_ms"][dom] * 1e-3) / 1e12
     traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash()) if (wl.name == "mixtral" and dom == "gemm_up") else None
     if world > 1:
         dist.destroy_process_group()
@@ -392,11 +407,13 @@ def main():
         "e2e": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
-        "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "tensor",
+        "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "hbm" if hbm_bound else "tensor",
                      "achieved": round(achieved, 1),
-                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak": round(peak, 1), "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
                      "traffic": traffic,
-                     "peak_source": f"{peak_kind} dense bf16 burst" + (" x2 (fp8)" if fp8_ratio > 1 else ""),
+                     "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
+                                     f"{peak_kind} dense bf16 burst" + (" x2 (fp8)" if fp8_ratio > 1 else "")),
                      "frac_of_sustained": round(achieved / peak_sustained, 4)},
         "stages": stages,
         "routes": r["R"],

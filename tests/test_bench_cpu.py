@@ -79,3 +79,31 @@ def test_max_over_ranks_with_gloo_world_size_2():
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     for r in range(world):
         assert out[r] == [15.0, 30.0]
+
+
+def test_stage_report_bytes_and_roofline_bound():
+    """GEMM stages carry algorithmic bytes beside FLOPs; at the measured peaks the
+    Mixtral-like up projection is tensor-bound and the 2,304-expert one HBM-bound
+    (about 3 GB of expert weights against a few hundred GFLOP)."""
+    import bench
+    from dropless_moe_expert_router_gb300 import workloads as W
+    peaks = {"hbm_gbs": 6806.2, "bf16_tflops": 1906.5}
+
+    def bound(name, stage):
+        wl = W.get(name)
+        R = wl.T * wl.K
+        ms = {stage: 1.0}
+        out, flops, nbytes = bench.stage_report(wl, R, ms, active=wl.E)
+        assert "GB/s" in out[stage] and "TFLOP/s" in out[stage]
+        peak_f = peaks["bf16_tflops"] * (2 if wl.precision == "mxfp8" else 1)
+        return "hbm" if nbytes[stage] / (peaks["hbm_gbs"] * 1e9) > flops[stage] / (peak_f * 1e12) else "tensor"
+
+    assert bound("mixtral", "gemm_up") == "tensor"
+    assert bound("dsv3", "gemm_down") == "tensor"
+    assert bound("large_e", "gemm_up") == "hbm"
+    assert bound("large_e", "gemm_down") == "hbm"
+    # up projection bytes, large-E shape: x_perm + W1|W3 + h, bf16
+    wl = W.get("large_e")
+    R = wl.T * wl.K
+    _, _, nbytes = bench.stage_report(wl, R, {"gemm_up": 1.0}, active=wl.E)
+    assert nbytes["gemm_up"] == R * wl.H * 2 + wl.E * wl.H * 2 * wl.F * 2 + R * wl.F * 2
