@@ -262,7 +262,7 @@ def run_ours(args, wl, rank, world, local_rank):
     errs = api.moe_get_device_errors()
     R = int(layer.perm.group_offsets[-1].item())
     active = int((layer.perm.group_sizes > 0).sum().item())      # experts that received routes
-    launches = MoELayer.LAUNCHES_PER_FORWARD + (layer.launches_per_backward if wl.backward else 0)
+    launches = layer.launches_per_forward + (layer.launches_per_backward if wl.backward else 0)
 
     if world > 1:
         total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)

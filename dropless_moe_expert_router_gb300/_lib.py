@@ -20,6 +20,7 @@ P, I, U, SZ = C.c_void_p, C.c_int, C.c_uint, C.c_size_t
 SIGNATURES = {
     "moe_route_topk": (I, [P, I, I, I, P, I, P, U, P]),
     "moe_permute_workspace_size": (SZ, [I, I, I]),
+    "moe_permute_kernel_launches": (I, [I, I, I]),
     "moe_permute": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, U, P, SZ, P]),
     "moe_permute_noalloc_max_scratch": (SZ, []),
     "moe_permute_noalloc": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, U, P]),

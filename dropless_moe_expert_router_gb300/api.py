@@ -95,6 +95,10 @@ def moe_permute_workspace_size(T: int, K: int, E: int) -> int:
     return int(_lib.load().moe_permute_workspace_size(T, K, E))
 
 
+def moe_permute_kernel_launches(T: int, K: int, E: int) -> int:
+    return int(_lib.load().moe_permute_kernel_launches(T, K, E))
+
+
 def permute_buffers(T: int, H: int, K: int, E: int, device, fuse_mxfp8: bool = False) -> Permuted:
     R_cap = T * K
     dev = torch.device(device)

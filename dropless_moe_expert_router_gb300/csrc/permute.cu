@@ -9,14 +9,17 @@
 // processing visits only the selected slots of a token, found by a warp ballot):
 //
 //   1. rank    (warp per tile of TT tokens): walks the tile's routes in
-//              flattened order, 32 at a time; __match_any groups the lanes of
+//              flattened order, 32 at a time (16 such rows of ids loaded ahead,
+//              one memory latency per 512 routes); __match_any groups the lanes of
 //              one expert, so each valid route gets its rank among the tile's
 //              earlier routes of the same expert. Writes per-(expert, tile)
 //              counts to the workspace table [E][tiles] and the tile-local rank
 //              into row_map.
 //   2. scan    (warp per expert, then the last block to finish): exclusive scan
 //              of each expert's counts over tiles -> per-tile bases, group_sizes;
-//              the last block scans group_sizes -> group_offsets.
+//              the last block scans group_sizes -> group_offsets. When the table
+//              is small (E * tiles <= 8192) this step is not a kernel of its own:
+//              every scatter block scans the table in shared memory first.
 //   3. scatter (warp per token): row = group_offsets[e] + base[e][tile] + rank;
 //              a ballot over the token's valid slots gives the destinations,
 //              the token row is read once and stored to each of them with 16-byte
@@ -166,17 +169,82 @@ __global__ void __launch_bounds__(SCAN_THREADS) perm_scan_kernel(int E, int tile
 }
 
 // ---------------------------------------------------------------- 3. scatter
-// Up to KC*32 routes per token (K <= 128).
-template <int KC, bool FUSE>
+// Up to KC*32 routes per token (K <= 128). SCAN: the count table is small (E * tiles <=
+// SCAN_IN_BLOCK_MAX): every block scans it in shared memory itself (the work of step 2),
+// and block 0 publishes group_sizes and group_offsets.
+constexpr int SCAN_IN_BLOCK_MAX = 8192;
+
+// The table and the offsets fit the default 48 KB of dynamic shared memory.
+inline bool scan_in_block(int E, long long tiles) {
+    return (long long)E * tiles <= SCAN_IN_BLOCK_MAX && ((long long)E * tiles + E + 1) * 4 <= 48 * 1024;
+}
+
+template <int KC, bool FUSE, bool SCAN>
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restrict__ x, int T, int H,
-                                                           const void* __restrict__ ids, bool i16, int K,
+                                                           const void* __restrict__ ids, bool i16, int K, int E,
                                                            int TT, int tiles, const int* __restrict__ table,
-                                                           const int* __restrict__ group_offsets,
+                                                           int* __restrict__ group_sizes,
+                                                           int* __restrict__ group_offsets,
                                                            int* __restrict__ row_map, int* __restrict__ perm_src,
                                                            void* __restrict__ x_perm,
                                                            uint8_t* __restrict__ scales) {
+    extern __shared__ int s_dyn[];  // SCAN: table [E][tiles], then offsets [E + 1]
     const int lane = (int)lane_id();
     const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    int* s_tab = s_dyn;
+    int* s_off = s_dyn + (SCAN ? E * tiles : 0);
+    if constexpr (SCAN) {
+        const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+        for (int i = threadIdx.x; i < E * tiles; i += blockDim.x) s_tab[i] = __ldcg(table + i);
+        __syncthreads();
+        // warp per expert: exclusive scan of its per-tile counts (in place), its total
+        for (int e = warp; e < E; e += nwarps) {
+            int* row = s_tab + (size_t)e * tiles;
+            int carry = 0;
+            for (int j0 = 0; j0 < tiles; j0 += 32) {
+                const int j = j0 + lane;
+                const int v = j < tiles ? row[j] : 0;
+                int inc = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int o = __shfl_up_sync(FULL, inc, d);
+                    if (lane >= d) inc += o;
+                }
+                if (j < tiles) row[j] = carry + inc - v;
+                carry += __shfl_sync(FULL, inc, 31);
+            }
+            if (lane == 0) s_off[e] = carry;
+        }
+        __syncthreads();
+        // exclusive scan of the totals (warp 0, a contiguous run of experts per lane)
+        if (warp == 0) {
+            const int per = (E + 31) / 32, b0 = lane * per;
+            int local = 0;
+            for (int j = 0; j < per; j++)
+                if (b0 + j < E) local += s_off[b0 + j];
+            int inc = local;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(FULL, inc, d);
+                if (lane >= d) inc += o;
+            }
+            int run = inc - local;
+            for (int j = 0; j < per; j++)
+                if (b0 + j < E) {
+                    const int v = s_off[b0 + j];
+                    s_off[b0 + j] = run;
+                    run += v;
+                }
+            if (lane == 31) s_off[E] = inc;
+        }
+        __syncthreads();
+        if (blockIdx.x == 0) {
+            for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+                group_offsets[e] = s_off[e];
+                if (e < E) group_sizes[e] = s_off[e + 1] - s_off[e];
+            }
+        }
+    }
     const int H8 = H >> 3;     // 16-byte chunks per row
     const int iters = (H8 + 31) >> 5;
     for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
@@ -192,7 +260,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
                 int lr = row_map[i];
                 if (lr >= 0) {
                     int e = load_id(ids, i, i16);
-                    r = group_offsets[e] + table[(size_t)e * tiles + tile] + lr;
+                    r = SCAN ? s_off[e] + s_tab[(size_t)e * tiles + tile] + lr
+                             : group_offsets[e] + table[(size_t)e * tiles + tile] + lr;
                     perm_src[r] = (int)t;
                 }
                 row_map[i] = r;
@@ -347,6 +416,15 @@ int rank_warps_per_block(int E) {
 }  // namespace
 }  // namespace moe
 
+extern "C" int moe_permute_kernel_launches(int T, int K, int E) {
+    using namespace moe;
+    if (T < 0 || K < 1 || E < 1) return -1;
+    if (T == 0) return 0;
+    const int TT = tile_tokens(E);
+    const long long tiles = ((long long)T + TT - 1) / TT;
+    return scan_in_block(E, tiles) ? 2 : 3;
+}
+
 extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
     using namespace moe;
     if (T < 0 || K < 1 || E < 1) return 0;
@@ -397,32 +475,38 @@ extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, 
     perm_rank_kernel<<<(tiles + wpb - 1) / wpb, wpb * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
                                                                       row_map, w.ticket);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    // 2. scan
-    const int experts_per_block = SCAN_THREADS / 32;
-    int sblocks = (E + experts_per_block - 1) / experts_per_block;
+    // 2. scan (a separate kernel only when the count table is too large for one block's shared memory)
     const int cap = sm_count();
-    if (sblocks > cap) sblocks = cap;
-    perm_scan_kernel<<<sblocks, SCAN_THREADS, 0, s>>>(E, tiles, w.table, group_sizes, group_offsets, w.ticket);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    // 3. scatter: warp per token
+    const bool in_block = scan_in_block(E, tiles);
+    if (!in_block) {
+        const int experts_per_block = SCAN_THREADS / 32;
+        int sblocks = (E + experts_per_block - 1) / experts_per_block;
+        if (sblocks > cap) sblocks = cap;
+        perm_scan_kernel<<<sblocks, SCAN_THREADS, 0, s>>>(E, tiles, w.table, group_sizes, group_offsets, w.ticket);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    // 3. scatter: warp per token (with the scan in every block: four blocks per SM, each warp takes
+    //    several tokens, so the scan of each block is spread over more rows)
     const long long warps_needed = T;
     long long blocks = (warps_needed + 7) / 8;
-    const long long bcap = (long long)cap * 16;
+    const long long bcap = (long long)cap * (in_block ? 4 : 16);
     if (blocks > bcap) blocks = bcap;
     const int KC = (K + 31) / 32;
-#define MOE_SCATTER(kc, fz)                                                                              \
-    perm_scatter_kernel<kc, fz><<<(int)blocks, 256, 0, s>>>((const uint4*)x, T, H, ids, i16, K, TT, tiles, \
-                                                            w.table, group_offsets, row_map, perm_src,     \
-                                                            x_perm, x_perm_scales)
+    const size_t ssmem = in_block ? ((size_t)E * tiles + E + 1) * sizeof(int) : 0;
+#define MOE_SCATTER(kc, fz, sc)                                                                                  \
+    perm_scatter_kernel<kc, fz, sc><<<(int)blocks, 256, ssmem, s>>>((const uint4*)x, T, H, ids, i16, K, E, TT,   \
+                                                                    tiles, w.table, group_sizes, group_offsets, \
+                                                                    row_map, perm_src, x_perm, x_perm_scales)
+#define MOE_SCATTER_KC(fz, sc)        \
+    if (KC == 1) MOE_SCATTER(1, fz, sc); \
+    else if (KC == 2) MOE_SCATTER(2, fz, sc); \
+    else MOE_SCATTER(4, fz, sc);
     if (fuse) {
-        if (KC == 1) MOE_SCATTER(1, true);
-        else if (KC == 2) MOE_SCATTER(2, true);
-        else MOE_SCATTER(4, true);
+        if (in_block) { MOE_SCATTER_KC(true, true) } else { MOE_SCATTER_KC(true, false) }
     } else {
-        if (KC == 1) MOE_SCATTER(1, false);
-        else if (KC == 2) MOE_SCATTER(2, false);
-        else MOE_SCATTER(4, false);
+        if (in_block) { MOE_SCATTER_KC(false, true) } else { MOE_SCATTER_KC(false, false) }
     }
+#undef MOE_SCATTER_KC
 #undef MOE_SCATTER
     return moe_host::launch_status();
 }

@@ -65,8 +65,11 @@ class MoELayer:
             self.dW3 = torch.empty((E, H, F), dtype=bf, device=dev)
             self.dW2 = torch.empty((E, F, H), dtype=bf, device=dev)
 
-    # number of library kernel launches one forward enqueues
-    LAUNCHES_PER_FORWARD = 7   # router 1, permute 3 (rank, scan, scatter), GEMM 2, combine 1
+    # number of library kernel launches one forward enqueues: router 1, permute 2 or 3
+    # (rank, [scan,] scatter), GEMM 2, combine 1
+    @property
+    def launches_per_forward(self) -> int:
+        return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E)
 
     def stage_route(self, logits, stream=None):
         api.moe_route_topk(logits, self.K, renorm=self.renorm, ids=self.ids, probs=self.probs, stream=stream)

@@ -123,6 +123,12 @@ moe_status moe_route_topk(const float *logits, int T, int E, int K,
  * ------------------------------------------------------------------------ */
 size_t moe_permute_workspace_size(int T, int K, int E);
 
+/* Number of kernels moe_permute launches for this shape (2 when the per-expert,
+ * per-token-tile count table is small enough to be scanned inside the scatter
+ * kernel, else 3; 0 for T == 0; -1 for invalid sizes). Host-only, no GPU work;
+ * not an operation of the pages, a count for launch accounting. */
+int moe_permute_kernel_launches(int T, int K, int E);
+
 moe_status moe_permute(const void *x, int T, int H,
                        const void *ids, moe_dtype id_dtype, int K, int E,
                        void *x_perm, uint8_t *x_perm_scales,
