@@ -9,13 +9,15 @@
 // One warp per token: a ballot over the token's K route slots (row_map >= 0)
 // gives the rows to pull; each lane owns 16-byte column chunks and accumulates
 // probs[t,k] * y_perm[row, chunk] in fp32, in ascending k, then rounds to bf16.
+// RB routes are pulled at a time (all their loads issued before any of them is
+// accumulated), so a token costs about K / RB memory latencies, not K.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-// KC * 32 route slots per token, CHUNKS 16-byte chunks in flight per lane and route
-template <int KC, int CHUNKS>
+// KC * 32 route slots per token, CHUNKS 16-byte chunks per lane and route, RB routes in flight
+template <int KC, int CHUNKS, int RB>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
                                                       const int* __restrict__ row_map,
                                                       const float* __restrict__ probs, int T, int K, int H,
@@ -50,22 +52,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
             for (int c = 0; c < KC; c++) {
                 unsigned m = mask[c];
                 while (m) {
-                    const int b = __ffs(m) - 1;
-                    m &= m - 1;
-                    const int r = __shfl_sync(FULL, rows[c], b);
-                    const float pk = __shfl_sync(FULL, p[c], b);
-                    uint4 v[CHUNKS];
+                    // the next (up to) RB selected slots, in ascending k (warp-uniform)
+                    int rr[RB];
+                    float pp[RB];
+                    bool on[RB];
 #pragma unroll
-                    for (int u = 0; u < CHUNKS; u++) {
-                        const int j = j0 + u * 32 + lane;
-                        v[u] = j < H8 ? __ldg(y_perm + (long long)r * H8 + j) : make_uint4(0, 0, 0, 0);
+                    for (int q = 0; q < RB; q++) {
+                        on[q] = m != 0u;
+                        const int b = on[q] ? __ffs(m) - 1 : 0;
+                        if (on[q]) m &= m - 1;
+                        rr[q] = __shfl_sync(FULL, rows[c], b);
+                        pp[q] = __shfl_sync(FULL, p[c], b);
                     }
+                    uint4 v[RB][CHUNKS];
 #pragma unroll
-                    for (int u = 0; u < CHUNKS; u++) {
-                        float f[8];
-                        bf16x8_to_f32(v[u], f);
+                    for (int q = 0; q < RB; q++)
 #pragma unroll
-                        for (int i = 0; i < 8; i++) acc[u][i] = fmaf(pk, f[i], acc[u][i]);
+                        for (int u = 0; u < CHUNKS; u++) {
+                            const int j = j0 + u * 32 + lane;
+                            v[q][u] = on[q] && j < H8 ? __ldg(y_perm + (long long)rr[q] * H8 + j)
+                                                      : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                    for (int q = 0; q < RB; q++) {
+                        if (!on[q]) break;
+#pragma unroll
+                        for (int u = 0; u < CHUNKS; u++) {
+                            float f[8];
+                            bf16x8_to_f32(v[q][u], f);
+#pragma unroll
+                            for (int i = 0; i < 8; i++) acc[u][i] = fmaf(pp[q], f[i], acc[u][i]);
+                        }
                     }
                 }
             }
@@ -102,7 +119,8 @@ extern "C" moe_status moe_unpermute_combine(const void* y_perm, const int32_t* r
     const int CH = H8 >= 128 ? 4 : (H8 >= 64 ? 2 : 1);  // no more chunks than a row has per lane
     const uint4* yp = (const uint4*)y_perm;
     uint4* yo = (uint4*)y;
-#define MOE_COMBINE(kc, ch) combine_kernel<kc, ch><<<(int)blocks, 256, 0, s>>>(yp, row_map, probs, T, K, H, yo)
+#define MOE_COMBINE(kc, ch) \
+    combine_kernel<kc, ch, (ch == 4 ? 2 : 4)><<<(int)blocks, 256, 0, s>>>(yp, row_map, probs, T, K, H, yo)
     if (KC == 1) {
         if (CH == 4) MOE_COMBINE(1, 4); else if (CH == 2) MOE_COMBINE(1, 2); else MOE_COMBINE(1, 1);
     } else if (KC == 2) {
