@@ -8,7 +8,9 @@
 // end-to-end", section "Remove work that has no selected route": local
 // processing visits only the selected slots of a token, found by a warp ballot):
 //
-//   1. rank    (warp per tile of TT tokens): walks the tile's routes in
+//   1. rank    (warp per tile of TT tokens; for large E, where tiles are 32
+//              tokens, a CTA per tile whose eight warps rank contiguous eighths
+//              of the tile and are joined by a per-expert prefix): walks the tile's routes in
 //              flattened order, 32 at a time (16 such rows of ids loaded ahead,
 //              one memory latency per 512 routes); __match_any groups the lanes of
 //              one expert, so each valid route gets its rank among the tile's
@@ -98,6 +100,81 @@ __global__ void perm_rank_kernel(const void* __restrict__ ids, bool i16, int T, 
         }
     }
     for (int e = lane; e < E; e += 32) table[(size_t)e * tiles + tile] = cnt[e];
+}
+
+// Large E (TT = 32 tokens): one CTA of 8 warps per tile. Warp w ranks the w-th contiguous
+// eighth of the tile's routes against its own 16-bit counters (at most 512 routes each);
+// an exclusive prefix over the warps, per expert, turns the counters into each warp's base
+// (and gives the tile's counts for the table); a route's rank in the tile is its rank in
+// its warp's range plus that base -- the same rank the flattened order gives.
+constexpr int RANK_CTA_WARPS = 8;
+constexpr int RANK_CTA_MAXU = 16;  // rows of 32 routes per warp: TT * K / 8 <= 32 * 128 / 8
+
+__global__ void __launch_bounds__(RANK_CTA_WARPS * 32) perm_rank_cta_kernel(const void* __restrict__ ids, bool i16,
+                                                                           int T, int K, int E, int TT, int tiles,
+                                                                           int* __restrict__ table,
+                                                                           int* __restrict__ row_map,
+                                                                           unsigned* __restrict__ ticket) {
+    extern __shared__ __align__(16) uint16_t s_c16[];  // [warps][E]
+    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
+    const int tile = blockIdx.x;
+    // zero the counters (8 E 16-bit values = E 16-byte pieces)
+    for (int i = threadIdx.x; i < E; i += blockDim.x) reinterpret_cast<uint4*>(s_c16)[i] = make_uint4(0, 0, 0, 0);
+    const long long i0 = (long long)tile * TT * K;
+    long long i1 = i0 + (long long)TT * K;
+    const long long nroutes = (long long)T * K;
+    if (i1 > nroutes) i1 = nroutes;
+    const long long n = i1 - i0;
+    const long long per = (n + RANK_CTA_WARPS * 32 - 1) / (RANK_CTA_WARPS * 32) * 32;   // routes of one warp
+    const long long w0 = i0 + warp * per;
+    const long long w1 = w0 + per < i1 ? w0 + per : i1;
+    int ev[RANK_CTA_MAXU], rk[RANK_CTA_MAXU];
+#pragma unroll
+    for (int u = 0; u < RANK_CTA_MAXU; u++) {
+        const long long i = w0 + u * 32 + lane;
+        int e = i < w1 ? load_id(ids, i, i16) : -1;
+        if (i < w1 && (e < -1 || e >= E)) {
+            raise_device_error(MOE_DEVERR_BAD_ID);
+            e = -1;
+        }
+        ev[u] = e;
+        rk[u] = 0;
+    }
+    __syncthreads();
+    uint16_t* cnt = s_c16 + (size_t)warp * E;
+#pragma unroll
+    for (int u = 0; u < RANK_CTA_MAXU; u++) {
+        if (w0 + u * 32 >= w1) break;   // warp-uniform
+        const int e = ev[u];
+        const unsigned grp = __match_any_sync(FULL, e);
+        const int leader = __ffs(grp) - 1;
+        int old = 0;
+        if (lane == leader && e >= 0) {
+            old = cnt[e];
+            cnt[e] = (uint16_t)(old + __popc(grp));
+        }
+        rk[u] = __shfl_sync(FULL, old, leader) + __popc(grp & lanemask_lt());
+        __syncwarp();
+    }
+    __syncthreads();
+    // per expert: exclusive prefix over the warps; the total is the tile's count
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < RANK_CTA_WARPS; w++) {
+            const int c = s_c16[(size_t)w * E + e];
+            s_c16[(size_t)w * E + e] = (uint16_t)run;
+            run += c;
+        }
+        table[(size_t)e * tiles + tile] = run;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < RANK_CTA_MAXU; u++) {
+        const long long i = w0 + u * 32 + lane;
+        if (i < w1) row_map[i] = ev[u] >= 0 ? rk[u] + cnt[ev[u]] : -1;
+    }
 }
 
 // ---------------------------------------------------------------- 2. scan
@@ -465,15 +542,27 @@ extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, 
         return MOE_OK;
     }
     // 1. rank
-    const int wpb = rank_warps_per_block(E);
-    const size_t smem = (size_t)wpb * E * sizeof(int);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+    if (TT == 32) {
+        // large E: a CTA per tile (TT * K <= 32 * 128 routes, at most 512 per warp)
+        const size_t smem = (size_t)RANK_CTA_WARPS * E * sizeof(uint16_t);
+        if (smem > 48 * 1024) {
+            if (cudaFuncSetAttribute(perm_rank_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        perm_rank_cta_kernel<<<tiles, RANK_CTA_WARPS * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
+                                                                       row_map, w.ticket);
+    } else {
+        const int wpb = rank_warps_per_block(E);
+        const size_t smem = (size_t)wpb * E * sizeof(int);
+        if (smem > 48 * 1024) {
+            if (cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        perm_rank_kernel<<<(tiles + wpb - 1) / wpb, wpb * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
+                                                                          row_map, w.ticket);
     }
-    perm_rank_kernel<<<(tiles + wpb - 1) / wpb, wpb * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
-                                                                      row_map, w.ticket);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     // 2. scan (a separate kernel only when the count table is too large for one block's shared memory)
     const int cap = sm_count();
