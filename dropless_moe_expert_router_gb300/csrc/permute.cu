@@ -20,7 +20,7 @@
 //   2. scan    (warp per expert, then the last block to finish): exclusive scan
 //              of each expert's counts over tiles -> per-tile bases, group_sizes;
 //              the last block scans group_sizes -> group_offsets. When the table
-//              is small (E * tiles <= 8192) this step is not a kernel of its own:
+//              is small (E * tiles <= 2048) this step is not a kernel of its own:
 //              every scatter block scans the table in shared memory first.
 //   3. scatter (warp per token): row = group_offsets[e] + base[e][tile] + rank;
 //              a ballot over the token's valid slots gives the destinations,
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) perm_scan_kernel(int E, int tile
 // Up to KC*32 routes per token (K <= 128). SCAN: the count table is small (E * tiles <=
 // SCAN_IN_BLOCK_MAX): every block scans it in shared memory itself (the work of step 2),
 // and block 0 publishes group_sizes and group_offsets.
-constexpr int SCAN_IN_BLOCK_MAX = 8192;
+constexpr int SCAN_IN_BLOCK_MAX = 2048;   // larger tables: the scatter is long and wants the full grid
 
 // The table and the offsets fit the default 48 KB of dynamic shared memory.
 inline bool scan_in_block(int E, long long tiles) {

@@ -67,9 +67,10 @@ def test_workspace_size_covers_the_tile_table(lib):
 
 
 def test_permute_launch_count(lib):
-    # the count table is scanned inside the scatter kernel when it is small (<= 8192 entries)
+    # the count table is scanned inside the scatter kernel when it is small (<= 2048 entries)
     assert lib.moe_permute_kernel_launches(8192, 2, 8) == 2          # 8 experts x 64 tiles
-    assert lib.moe_permute_kernel_launches(32768, 8, 32) == 2        # 32 x 256
+    assert lib.moe_permute_kernel_launches(8192, 4, 32) == 2         # 32 x 64
+    assert lib.moe_permute_kernel_launches(32768, 8, 32) == 3        # 32 x 256: separate scan
     assert lib.moe_permute_kernel_launches(8192, 36, 2304) == 3      # 2304 x 256: separate scan
     assert lib.moe_permute_kernel_launches(32, 2, 8192) == 3         # table + offsets past 48 KB
     assert lib.moe_permute_kernel_launches(0, 2, 8) == 0
