@@ -68,6 +68,12 @@ def lib():
             L.oracle_permute.argtypes = [P, i32, i32, P, i32, i32, P, P, P, P, P]
             L.oracle_combine.restype = None
             L.oracle_combine.argtypes = [P, P, P, i32, i32, i32, P]
+            L.oracle_route_backward.restype = None
+            L.oracle_route_backward.argtypes = [P, P, P, i32, i32, i32, i32, P]
+            L.oracle_combine_backward.restype = None
+            L.oracle_combine_backward.argtypes = [P, P, P, P, i32, i32, i32, P, P]
+            L.oracle_permute_backward.restype = None
+            L.oracle_permute_backward.argtypes = [P, P, i32, i32, i32, P]
             L.oracle_swiglu_rows.restype = None
             L.oracle_swiglu_rows.argtypes = [i32, P, P, i32, P, P, P, P, P, P, P, i32, i32, i32,
                                              i64, P, i64, i32, P, P, P, P, P, P, P, P]
@@ -189,6 +195,45 @@ def combine(y_perm_bf16, row_map, probs):
     y = np.zeros((T, H), np.uint16)
     lib().oracle_combine(_p(yp), _p(rm), _p(pr), T, K, H, _p(y))
     return y
+
+
+# ---------------------------------------------------------------- backward
+def route_backward(logits, ids, dprobs, renorm: bool = False):
+    """dlogits [T, E] (float64) of the router's probabilities, selection held fixed."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    idv = _c(ids, np.int32)
+    K = idv.shape[1]
+    dp = _c(dprobs, np.float32)
+    out = np.zeros((T, E), np.float64)
+    lib().oracle_route_backward(_p(lg), _p(idv), _p(dp), T, E, K, int(bool(renorm)), _p(out))
+    return out
+
+
+def combine_backward(dy_bf16, y_perm_bf16, row_map, probs, dy_perm_init=None):
+    """(dy_perm [rows of y_perm, H] bf16 bits -- rows no route maps to keep dy_perm_init
+    (zeros by default) --, dprobs [T, K] float64)."""
+    dy = _c(dy_bf16, np.uint16)
+    yp = _c(y_perm_bf16, np.uint16)
+    rm = _c(row_map, np.int32)
+    pr = _c(probs, np.float32)
+    T, K = rm.shape
+    H = yp.shape[1]
+    dyp = np.zeros(yp.shape, np.uint16) if dy_perm_init is None else np.array(dy_perm_init, np.uint16)
+    dp = np.zeros((T, K), np.float64)
+    lib().oracle_combine_backward(_p(dy), _p(yp), _p(rm), _p(pr), T, K, H, _p(dyp), _p(dp))
+    return dyp, dp
+
+
+def permute_backward(dx_perm_bf16, row_map):
+    """dx [T, H] bf16 bits: the sum over each token's valid routes of its dx_perm rows."""
+    dxp = _c(dx_perm_bf16, np.uint16)
+    rm = _c(row_map, np.int32)
+    T, K = rm.shape
+    H = dxp.shape[1]
+    dx = np.zeros((T, H), np.uint16)
+    lib().oracle_permute_backward(_p(dxp), _p(rm), T, K, H, _p(dx))
+    return dx
 
 
 # ------------------------------------------------------------ grouped MLP

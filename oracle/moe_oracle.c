@@ -356,6 +356,129 @@ void oracle_combine(const uint16_t *y_perm, const int32_t *row_map, const float 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Backward of the router, the combine and the permute                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Router backward. [SPARSER] "The workload changes the bottleneck" lists a
+ * router backward among the Transformer Engine kernels and "Preserve a compact
+ * route" extends the router work to forward and backward kernels; neither
+ * defines it. Reading taken: the gradient of the forward's probabilities with
+ * respect to the logits, the selection held fixed (top-K is piecewise
+ * constant). For row t, with S the selected experts (ids[t,k] in [0, E); -1
+ * and other ids are skipped), g[k] = dprobs[t,k] and G_e = sum of g[k] over
+ * the k with ids[t,k] = e:
+ *   softmax over all E:   p_e = exp(l_e - m) / sum_j exp(l_j - m),
+ *                         dlogits[t,e] = p_e * (G_e - sum_{valid k} g[k] p_{ids[t,k]});
+ *   renormalised over S:  q_e = exp(l_e - m) / sum_{j in S} exp(l_j - m) for e in S,
+ *                         dlogits[t,e] = q_e * (G_e - sum_{valid k} g[k] q_{ids[t,k]}) on S,
+ *                         0 off S.
+ * (Each is J^T g for the softmax Jacobian d p_i / d l_j = p_i (delta_ij - p_j).)
+ * m is the row maximum, as in the forward. dlogits is [T, E] doubles.
+ */
+void oracle_route_backward(const float *logits, const int32_t *ids, const float *dprobs,
+                           int T, int E, int K, int renorm, double *dlogits)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    double *G = (double *)malloc(sizeof(double) * (size_t)E);
+    char *sel = (char *)malloc((size_t)E);
+    for (int t = 0; t < T; t++) {
+        const float *l = logits + (size_t)t * E;
+        for (int e = 0; e < E; e++) {
+            G[e] = 0.0;
+            sel[e] = 0;
+        }
+        for (int k = 0; k < K; k++) {
+            int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            sel[e] = 1;
+            G[e] += (double)dprobs[(size_t)t * K + k];
+        }
+        double m = (double)l[0];
+        for (int e = 1; e < E; e++)
+            if ((double)l[e] > m)
+                m = (double)l[e];
+        double denom = 0.0;
+        for (int e = 0; e < E; e++)
+            if (!renorm || sel[e])
+                denom += exp((double)l[e] - m);
+        for (int e = 0; e < E; e++)
+            p[e] = (!renorm || sel[e]) ? exp((double)l[e] - m) / denom : 0.0;
+        double s = 0.0;
+        for (int k = 0; k < K; k++) {
+            int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            s += (double)dprobs[(size_t)t * K + k] * p[e];
+        }
+        for (int e = 0; e < E; e++)
+            dlogits[(size_t)t * E + e] = (renorm && !sel[e]) ? 0.0 : p[e] * (G[e] - s);
+    }
+    free(p);
+    free(G);
+    free(sel);
+}
+
+/*
+ * Combine backward: the adjoint of oracle_combine. The pages give the forward
+ * ([TEJAX] "Optimization 2": results routed back and accumulated in token
+ * order; [SPARSER] "Remove work that has no selected route": combine with
+ * probabilities); reading taken for the backward: the chain rule through
+ * y[t] = sum_k p[t,k] y_perm[row_map[t,k]]:
+ *   dy_perm[row_map[t,k]] = p[t,k] * dy[t]         (rounded once to bf16),
+ *   dprobs[t,k] = sum_j dy[t,j] * y_perm[row_map[t,k], j]   (double),
+ * for every valid route; an invalid route (row_map < 0) gets dprobs 0 and no
+ * row. Rows of dy_perm that no route maps to are left as they are.
+ */
+void oracle_combine_backward(const uint16_t *dy, const uint16_t *y_perm, const int32_t *row_map,
+                             const float *probs, int T, int K, int H, uint16_t *dy_perm,
+                             double *dprobs)
+{
+    for (int t = 0; t < T; t++) {
+        for (int k = 0; k < K; k++) {
+            long r = row_map[(size_t)t * K + k];
+            double d = 0.0;
+            if (r >= 0) {
+                double p = (double)probs[(size_t)t * K + k];
+                for (int j = 0; j < H; j++) {
+                    double g = oracle_bf16_to_double(dy[(size_t)t * H + j]);
+                    d += g * oracle_bf16_to_double(y_perm[r * H + j]);
+                    dy_perm[r * H + j] = oracle_double_to_bf16(p * g);
+                }
+            }
+            dprobs[(size_t)t * K + k] = d;
+        }
+    }
+}
+
+/*
+ * Permute backward: the adjoint of the permute's row copies (x_perm[row] =
+ * x[t] for every valid route of t), i.e. dx[t] = sum over the valid k of
+ * dx_perm[row_map[t,k]], accumulated in ascending k and rounded once to bf16
+ * (the combine with every weight 1). Tokens without a valid route get 0.
+ */
+void oracle_permute_backward(const uint16_t *dx_perm, const int32_t *row_map, int T, int K, int H,
+                             uint16_t *dx)
+{
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int t = 0; t < T; t++) {
+        for (int j = 0; j < H; j++)
+            acc[j] = 0.0;
+        for (int k = 0; k < K; k++) {
+            long r = row_map[(size_t)t * K + k];
+            if (r < 0)
+                continue;
+            for (int j = 0; j < H; j++)
+                acc[j] += oracle_bf16_to_double(dx_perm[r * H + j]);
+        }
+        for (int j = 0; j < H; j++)
+            dx[(size_t)t * H + j] = oracle_double_to_bf16(acc[j]);
+    }
+    free(acc);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Grouped SwiGLU expert MLP                                                 */
 /* ------------------------------------------------------------------------ */
 
