@@ -199,6 +199,63 @@ def moe_unpermute_combine(y_perm: torch.Tensor, row_map: torch.Tensor, probs: to
     return y
 
 
+# -------------------------------------------------------------------- backward of route / permute / combine
+def moe_route_topk_backward(logits: torch.Tensor, ids: torch.Tensor, dprobs: torch.Tensor, *,
+                            renorm: bool = False, dlogits: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """logits [T, E] fp32, ids [T, K], dprobs [T, K] fp32 -> dlogits [T, E] fp32."""
+    _want(logits, "logits", torch.float32, 2)
+    _want(ids, "ids", None, 2)
+    _want(dprobs, "dprobs", torch.float32, 2)
+    T, E = logits.shape
+    K = ids.shape[1]
+    if dlogits is None:
+        dlogits = torch.empty((T, E), dtype=torch.float32, device=logits.device)
+    _want(dlogits, "dlogits", torch.float32, 2)
+    st = _lib.load().moe_route_topk_backward(_ptr(logits), _ptr(ids), _id_code(ids.dtype), _ptr(dprobs), T, E, K,
+                                             MOE_ROUTE_RENORM if renorm else 0, _ptr(dlogits), _stream(stream))
+    _check("moe_route_topk_backward", st)
+    return dlogits
+
+
+def moe_unpermute_combine_backward(dy: torch.Tensor, y_perm: torch.Tensor, row_map: torch.Tensor,
+                                   probs: torch.Tensor, *, dy_perm: Optional[torch.Tensor] = None,
+                                   dprobs: Optional[torch.Tensor] = None, stream=None):
+    """dy [T, H] bf16, y_perm [R_cap, H] bf16, row_map [T, K], probs [T, K] ->
+    (dy_perm [R_cap, H] bf16, dprobs [T, K] fp32)."""
+    _want(dy, "dy", torch.bfloat16, 2)
+    _want(y_perm, "y_perm", torch.bfloat16, 2)
+    _want(row_map, "row_map", torch.int32, 2)
+    _want(probs, "probs", torch.float32, 2)
+    T, K = row_map.shape
+    H = y_perm.shape[1]
+    if dy_perm is None:
+        dy_perm = torch.empty_like(y_perm)    # rows no route maps to are not written
+    if dprobs is None:
+        dprobs = torch.empty((T, K), dtype=torch.float32, device=dy.device)
+    _want(dy_perm, "dy_perm", torch.bfloat16, 2)
+    _want(dprobs, "dprobs", torch.float32, 2)
+    st = _lib.load().moe_unpermute_combine_backward(_ptr(dy), _ptr(y_perm), _ptr(row_map), _ptr(probs), T, K, H,
+                                                    _ptr(dy_perm), _ptr(dprobs), _stream(stream))
+    _check("moe_unpermute_combine_backward", st)
+    return dy_perm, dprobs
+
+
+def moe_permute_backward(dx_perm: torch.Tensor, row_map: torch.Tensor, *, dx: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """dx_perm [R_cap, H] bf16, row_map [T, K] -> dx [T, H] bf16 (each token's rows summed)."""
+    _want(dx_perm, "dx_perm", torch.bfloat16, 2)
+    _want(row_map, "row_map", torch.int32, 2)
+    T, K = row_map.shape
+    H = dx_perm.shape[1]
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dx_perm.device)
+    _want(dx, "dx", torch.bfloat16, 2)
+    st = _lib.load().moe_permute_backward(_ptr(dx_perm), _ptr(row_map), T, K, H, _ptr(dx), _stream(stream))
+    _check("moe_permute_backward", st)
+    return dx
+
+
 # -------------------------------------------------------------------- errors
 def moe_get_device_errors(clear: bool = True) -> int:
     v = C.c_uint32(0)

@@ -819,3 +819,137 @@ extern "C" size_t moe_route_probs_bytes(int T, int K) {
     if (T < 0 || K < 0) return 0;
     return (size_t)T * (size_t)K * 4u;
 }
+
+// ---------------------------------------------------------------------------
+// Router backward ("Sparser MoE end-to-end", sections "The workload changes the
+// bottleneck" and "Preserve a compact route": a router backward kernel beside
+// the forward; the pages do not define it). The gradient of the forward's
+// probabilities with respect to the logits, the selection held fixed: for row
+// t with selected set S (valid ids), g[k] = dprobs[t,k], G_e = sum of g[k] over
+// the k with ids[t,k] = e, p the softmax over all E (or, renormalised, over S,
+// 0 off S) and s = sum over valid k of g[k] p_{ids[t,k]}:
+//   dlogits[t,e] = p_e (G_e - s)   (0 off S when renormalised).
+// One warp per row: the row maximum and the denominator, s from the selected
+// slots, then every dlogit is written as -p_e s and the selected ones are
+// overwritten (by the lane of each id's first occurrence) with p_e (G_e - s).
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+template <int KC>
+__global__ void __launch_bounds__(256) route_backward_kernel(const float* __restrict__ logits,
+                                                             const void* __restrict__ ids, bool i16,
+                                                             const float* __restrict__ dprobs, int T, int E,
+                                                             int K, bool renorm, float* __restrict__ dlogits) {
+    const int lane = (int)lane_id();
+    const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
+        const float* l = logits + t * E;
+        float* out = dlogits + t * E;
+        // the route slots of this row: id (or -1), gradient, and whether it is the id's first occurrence
+        int id[KC];
+        float g[KC];
+        bool first[KC];
+#pragma unroll
+        for (int c = 0; c < KC; c++) {
+            const int k = c * 32 + lane;
+            int e = -1;
+            float gk = 0.0f;
+            if (k < K) {
+                e = i16 ? (int)reinterpret_cast<const int16_t*>(ids)[t * K + k]
+                        : reinterpret_cast<const int32_t*>(ids)[t * K + k];
+                if (e < 0 || e >= E) e = -1;
+                gk = e >= 0 ? __ldg(dprobs + t * K + k) : 0.0f;
+            }
+            id[c] = e;
+            g[c] = gk;
+            first[c] = e >= 0;
+        }
+        // G_e accumulated on the first occurrence; later duplicates contribute and step aside
+#pragma unroll
+        for (int c2 = 0; c2 < KC; c2++)
+            for (int b = 0; b < 32; b++) {
+                if (c2 * 32 + b >= K) break;          // warp-uniform
+                const int e2 = __shfl_sync(FULL, id[c2], b);
+                const float g2 = __shfl_sync(FULL, g[c2], b);
+                const int k2 = c2 * 32 + b;
+#pragma unroll
+                for (int c = 0; c < KC; c++) {
+                    const int k = c * 32 + lane;
+                    if (id[c] >= 0 && e2 == id[c] && k2 != k) {
+                        if (k2 < k) first[c] = false;
+                        else g[c] += g2;      // a later slot of the same expert: its gradient joins
+                    }
+                }
+            }
+        // row maximum over all E (as in the forward)
+        float m = -INFINITY;
+        for (int e = lane; e < E; e += 32) m = fmaxf(m, __ldg(l + e));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+        // denominator: all E, or the selected set (each expert once)
+        float den = 0.0f;
+        if (!renorm) {
+            for (int e = lane; e < E; e += 32) den += __expf(__ldg(l + e) - m);
+        } else {
+#pragma unroll
+            for (int c = 0; c < KC; c++)
+                if (first[c]) den += __expf(__ldg(l + id[c]) - m);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(FULL, den, o);
+        const float inv = 1.0f / den;
+        // s = sum over the selected experts of G_e p_e (first occurrences carry G_e)
+        float sp = 0.0f;
+        float pe[KC];
+#pragma unroll
+        for (int c = 0; c < KC; c++) {
+            pe[c] = first[c] ? __expf(__ldg(l + id[c]) - m) * inv : 0.0f;
+            sp += first[c] ? g[c] * pe[c] : 0.0f;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(FULL, sp, o);
+        // every dlogit: -p_e s (0 off the selection when renormalised) ...
+        for (int e = lane; e < E; e += 32) out[e] = renorm ? 0.0f : -(__expf(__ldg(l + e) - m) * inv) * sp;
+        __syncwarp();
+        // ... the selected ones: p_e (G_e - s)
+#pragma unroll
+        for (int c = 0; c < KC; c++)
+            if (first[c]) out[id[c]] = pe[c] * (g[c] - sp);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_topk_backward(const float* logits, const void* ids, moe_dtype id_dtype,
+                                              const float* dprobs, int T, int E, int K, unsigned flags,
+                                              float* dlogits, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || E < 1 || K < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
+    if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
+    if (flags & ~MOE_ROUTE_RENORM) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !ids || !dprobs || !dlogits) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned(logits, 4) || !moe_host::aligned(dprobs, 4) || !moe_host::aligned(dlogits, 4) ||
+        !moe_host::aligned(ids, id_dtype == MOE_I16 ? 2 : 4))
+        return MOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = ((long long)T + 7) / 8;
+    const long long cap = (long long)sms * 16;
+    if (blocks > cap) blocks = cap;
+    cudaStream_t s = moe_host::as_stream(stream);
+    const bool i16 = id_dtype == MOE_I16;
+    const bool renorm = (flags & MOE_ROUTE_RENORM) != 0;
+    const int KC = (K + 31) / 32;
+#define MOE_ROUTE_BWD(kc) \
+    route_backward_kernel<kc><<<(int)blocks, 256, 0, s>>>(logits, ids, i16, dprobs, T, E, K, renorm, dlogits)
+    if (KC == 1) MOE_ROUTE_BWD(1);
+    else if (KC == 2) MOE_ROUTE_BWD(2);
+    else MOE_ROUTE_BWD(4);
+#undef MOE_ROUTE_BWD
+    return moe_host::launch_status();
+}

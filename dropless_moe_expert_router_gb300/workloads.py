@@ -143,3 +143,16 @@ _YPERM = 9
 def expert_out(wl: Workload, seed: int = 0) -> torch.Tensor:
     """Synthetic expert outputs in permuted order [T*K, H] bf16 ~ N(0, 0.02) (to test combine alone)."""
     return _normal((wl.R_cap, wl.H), wl.act_std, seed, _YPERM)
+
+
+_DYOUT, _DPROBS = 10, 11
+
+
+def dy(wl: Workload, seed: int = 0) -> torch.Tensor:
+    """Upstream gradient of the layer output [T, H] bf16 ~ N(0, 0.02)."""
+    return _normal((wl.T, wl.H), wl.act_std, seed, _DYOUT)
+
+
+def dprobs(wl: Workload, seed: int = 0) -> torch.Tensor:
+    """Upstream gradient of the router probabilities [T, K] fp32 ~ N(0, 1)."""
+    return torch.randn((wl.T, wl.K), generator=_gen(seed, _DPROBS)).contiguous()

@@ -97,6 +97,25 @@ moe_status moe_route_topk(const float *logits, int T, int E, int K,
                           unsigned flags, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Router backward ([SPARSER] "The workload changes the bottleneck" names a
+ * router backward among the kernels, "Preserve a compact route" a backward
+ * beside the forward; neither defines it). The gradient of moe_route_topk's
+ * probs with respect to the logits, the selection held fixed (top-K is
+ * piecewise constant): for row t, S = its valid ids (0 <= id < E; others
+ * skipped), g[k] = dprobs[t,k], G_e = sum of g[k] over the k with ids[t,k] = e,
+ * p the softmax over all E (with MOE_ROUTE_RENORM: over S, and 0 off S),
+ * s = sum over valid k of g[k] p_{ids[t,k]}:
+ *   dlogits[t,e] = p_e (G_e - s)       (0 off S with MOE_ROUTE_RENORM).
+ * logits [T, E] fp32 (the forward's input), ids [T, K] int16/int32, dprobs
+ * [T, K] fp32 in; dlogits [T, E] fp32 out (every element written). Same size
+ * limits as moe_route_topk (K <= 128); fp32 arithmetic, within 1e-6 absolute
+ * of the exact value for logits of the workloads' scale.
+ * ------------------------------------------------------------------------ */
+moe_status moe_route_topk_backward(const float *logits, const void *ids, moe_dtype id_dtype,
+                                   const float *dprobs, int T, int E, int K,
+                                   unsigned flags, float *dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Permute / dispatch ([TEJAX] "Dropless vs capacity-based MoE": every routed
  * token is processed, nothing dropped or padded; MoE-layer figure: tokens are
  * grouped per expert and combine restores token order; [SPARSER] "Remove work
@@ -320,6 +339,32 @@ moe_status moe_grouped_gemm_wgrad(const void *aT, const uint8_t *aT_scales, cons
 moe_status moe_unpermute_combine(const void *y_perm, const int32_t *row_map,
                                  const float *probs, int T, int K, int H,
                                  void *y, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine backward: the adjoint of moe_unpermute_combine (the chain rule
+ * through y[t] = sum_k p[t,k] y_perm[row_map[t,k]]; the pages give the
+ * forward, [TEJAX] "Optimization 2", and name training, not this step).
+ * For every valid route (t, k) with row r = row_map[t,k]:
+ *   dy_perm[r]   = bf16(p[t,k] * dy[t])                  (one rounding)
+ *   dprobs[t,k]  = sum_j dy[t,j] * y_perm[r,j]            (fp32 accumulation)
+ * and dprobs[t,k] = 0 for invalid routes. dy [T, H] bf16, y_perm [R_cap, H]
+ * bf16 (the forward's), row_map [T, K], probs [T, K] fp32 in; dy_perm
+ * [R_cap, H] bf16 (rows no route maps to are not written) and dprobs [T, K]
+ * fp32 out. Requires H % 8 == 0, 1 <= K <= 128; 16-byte aligned rows.
+ * ------------------------------------------------------------------------ */
+moe_status moe_unpermute_combine_backward(const void *dy, const void *y_perm,
+                                          const int32_t *row_map, const float *probs,
+                                          int T, int K, int H, void *dy_perm,
+                                          float *dprobs, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Permute backward: the adjoint of moe_permute's row copies, dx[t] = bf16(sum
+ * over the valid k, ascending, of dx_perm[row_map[t,k]]) with fp32
+ * accumulation; tokens without a valid route get 0. dx_perm [R_cap, H] bf16,
+ * row_map [T, K] in; dx [T, H] bf16 out. Requires H % 8 == 0, 1 <= K <= 128.
+ * ------------------------------------------------------------------------ */
+moe_status moe_permute_backward(const void *dx_perm, const int32_t *row_map,
+                                int T, int K, int H, void *dx, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Device error word. Copies the word to *flags_out (synchronising the device)
