@@ -6,7 +6,9 @@ grouped SwiGLU GEMMs -> combine) on one node, one process per GPU.
 
 A step is one forward pass of the whole layer over one batch of T tokens of
 the workload (default: Mixtral-like, T=8192, H=4096, E=8, top-2, F=14336, bf16,
-synthetic seeded inputs). Each rank runs the same layer on its own batch
+synthetic seeded inputs); for the training workload (heavy skew) it is the
+forward and the whole layer's backward from the gradient of its output
+(combine, expert-MLP dgrad/dx/wgrad, permute and router backward). Each rank runs the same layer on its own batch
 (replicas: weak scaling, no collective on the data path). Rank 0 prints one
 JSON line:
 
@@ -189,7 +191,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      renorm=wl.renorm, id_dtype=torch.int16 if wl.id_bits == 16 else torch.int32,
                      training=wl.backward)
     del w1, w3, w2
-    dy = W.dy_perm(wl, seed=rank).to(dev) if wl.backward else None
+    dy = W.dy(wl, seed=rank).to(dev) if wl.backward else None        # gradient of the layer output
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -197,8 +199,13 @@ def run_ours(args, wl, rank, world, local_rank):
               ("gemm_up", layer.stage_gemm_up), ("gemm_down", layer.stage_gemm_down),
               ("combine", layer.stage_combine)]
     if wl.backward:
-        stages += [("dgrad_dh", lambda: layer.stage_dgrad_dh(dy)), ("dgrad_dx", layer.stage_dgrad_dx),
-                   ("wgrad_transpose", lambda: layer.stage_transposes(x, dy)), ("wgrad_gemm", layer.stage_wgrad_gemm)]
+        # the whole layer's backward, from dy [T, H]: combine, expert MLP (dgrad, dx, transposes,
+        # wgrad), permute and router backward
+        stages += [("combine_bwd", lambda: layer.stage_combine_backward(dy)),
+                   ("dgrad_dh", lambda: layer.stage_dgrad_dh(layer.dy_perm)), ("dgrad_dx", layer.stage_dgrad_dx),
+                   ("wgrad_transpose", lambda: layer.stage_transposes(x, layer.dy_perm)),
+                   ("wgrad_gemm", layer.stage_wgrad_gemm), ("permute_bwd", layer.stage_permute_backward),
+                   ("route_bwd", lambda: layer.stage_route_backward(logits))]
 
     def step():
         for _, fn in stages:
@@ -234,7 +241,7 @@ def run_ours(args, wl, rank, world, local_rank):
     total_ms = sum(step_ms)
 
     # end to end through the host-memory call: x and logits in, y out (for the training
-    # workload dy_perm stays on the device, where the next layer's backward produces it)
+    # workload dy stays on the device, where the next layer's backward produces it)
     x_host = W.x(wl, seed=rank).pin_memory()
     lg_host = W.logits(wl, seed=rank).pin_memory()
     y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
@@ -242,7 +249,7 @@ def run_ours(args, wl, rank, world, local_rank):
     def e2e_step():
         layer.forward_host(x_host, lg_host, y_host)
         if wl.backward:
-            layer.backward(layer.x_dev, dy)
+            layer.backward_full(layer.x_dev, layer.logits_dev, dy)
 
     for _ in range(max(2, args.warmup // 2)):
         e2e_step()
@@ -262,7 +269,7 @@ def run_ours(args, wl, rank, world, local_rank):
     errs = api.moe_get_device_errors()
     R = int(layer.perm.group_offsets[-1].item())
     active = int((layer.perm.group_sizes > 0).sum().item())      # experts that received routes
-    launches = layer.launches_per_forward + (layer.launches_per_backward if wl.backward else 0)
+    launches = layer.launches_per_forward + (layer.launches_per_backward_full if wl.backward else 0)
 
     if world > 1:
         total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)
@@ -297,6 +304,10 @@ def stage_report(wl, R, stage_ms, active=None):
         "route": T * E * 4 + T * K * (idb + 4),
         "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
         "combine": R * H * 2 + T * K * 8 + T * H * 2,
+        # read dy and y_perm, write dy_perm; route metadata and dprobs
+        "combine_bwd": T * H * 2 + R * H * 2 + R * H * 2 + T * K * 12,
+        "permute_bwd": R * H * 2 + T * H * 2 + T * K * 4,
+        "route_bwd": T * E * 4 * 2 + T * K * (idb + 4),
         # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands
         "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
         "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * q,

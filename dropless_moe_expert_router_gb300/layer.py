@@ -50,6 +50,11 @@ class MoELayer:
             self.h_bf16 = torch.empty((R_cap, F), dtype=bf, device=dev) if self.fp8 else None
             self.dab = torch.empty((R_cap, 2 * F), dtype=bf, device=dev)
             self.dx = torch.empty((R_cap, H), dtype=bf, device=dev)
+            # full-layer backward: gradients of y_perm, probs, the tokens and the logits
+            self.dy_perm = torch.empty((R_cap, H), dtype=bf, device=dev)
+            self.dprobs = torch.empty((T, K), dtype=torch.float32, device=dev)
+            self.dx_tokens = torch.empty((T, H), dtype=bf, device=dev)
+            self.dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
             u8 = torch.uint8
             self.dy_q = torch.empty((R_cap, H), dtype=u8, device=dev) if self.fp8 else None
             self.dy_s = torch.empty((R_cap, H // 32), dtype=u8, device=dev) if self.fp8 else None
@@ -110,10 +115,29 @@ class MoELayer:
         return self.y
 
     # ------------------------------------------------------------ backward
-    # library launches of one backward: dgrad 1, dx 1, transposes 4, wgrad 2 (+ 2 quantisations for MXFP8)
+    # library launches of the expert-MLP backward: dgrad 1, dx 1, transposes 4, wgrad 2 (+ 2
+    # quantisations for MXFP8); the full layer backward adds combine, permute and router backward
     @property
     def launches_per_backward(self) -> int:
         return 8 + (2 if self.fp8 else 0)
+
+    @property
+    def launches_per_backward_full(self) -> int:
+        return self.launches_per_backward + 3
+
+    def stage_combine_backward(self, dy: torch.Tensor, stream=None):
+        """dy [T, H] bf16 (gradient of the layer output) -> dy_perm [R_cap, H], dprobs [T, K]."""
+        api.moe_unpermute_combine_backward(dy, self.y_perm, self.perm.row_map, self.probs, dy_perm=self.dy_perm,
+                                           dprobs=self.dprobs, stream=stream)
+
+    def stage_permute_backward(self, stream=None):
+        """dx_perm (the expert backward's) -> dx [T, H]: each token's rows summed."""
+        api.moe_permute_backward(self.dx, self.perm.row_map, dx=self.dx_tokens, stream=stream)
+
+    def stage_route_backward(self, logits: torch.Tensor, stream=None):
+        """dprobs -> dlogits [T, E] through the router's softmax (selection fixed)."""
+        api.moe_route_topk_backward(logits, self.ids, self.dprobs, renorm=self.renorm, dlogits=self.dlogits,
+                                    stream=stream)
 
     def stage_dgrad_dh(self, dy_perm: torch.Tensor, stream=None):
         """dy_perm [R_cap, H] bf16 -> dab = SwiGLU backward of dh = dy W2^T (bf16)."""
@@ -164,6 +188,15 @@ class MoELayer:
         dx = self.stage_dgrad_dx(stream)
         self.stage_transposes(x, dy_perm, stream)
         return (dx,) + tuple(self.stage_wgrad_gemm(stream))
+
+    def backward_full(self, x: torch.Tensor, logits: torch.Tensor, dy: torch.Tensor, stream=None):
+        """Backward of the whole layer after a training forward (x, logits: the forward's inputs;
+        dy [T, H]: gradient of its output) -> (dx [T, H], dlogits [T, E], dW1, dW3, dW2)."""
+        self.stage_combine_backward(dy, stream)
+        _, dw1, dw3, dw2 = self.backward(x, self.dy_perm, stream)
+        self.stage_permute_backward(stream)
+        self.stage_route_backward(logits, stream)
+        return self.dx_tokens, self.dlogits, dw1, dw3, dw2
 
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor,
                      stream=None) -> torch.Tensor:
