@@ -12,16 +12,21 @@ forward and the whole layer's backward from the gradient of its output
 (replicas: weak scaling, no collective on the data path). Rank 0 prints one
 JSON line:
 
-  value      tokens/s over all ranks, inputs resident in HBM; every step timed
-             with CUDA events on the launching stream, L2 flushed (512 MiB write)
-             before every timed step, outside the timed interval;
+  value      tokens/s over all ranks, inputs resident in HBM; the step (every
+             kernel of it) captured once as a CUDA graph -- the path is
+             graph-capturable, group sizes stay on the device -- and every
+             timed replay bracketed by CUDA events on the launching stream, L2
+             flushed (512 MiB write) before every timed step, outside the timed
+             interval;
   e2e        the same metric through MoELayer.forward_host: pinned host inputs
              copied in and the output copied out inside the timed interval;
   roofline   the dominant kernel (grouped GEMM, up projection with SwiGLU):
              algorithmic FLOPs (2 * R * H * 2F) / its mean event-timed duration,
              against the measured dense bf16 burst peak (the timed loop is short
              and runs at maximum SM clock), the sustained figure given beside it;
-  stages     mean per-stage time and the bandwidth / FLOP rate of each stage;
+  stages     mean per-stage time and the bandwidth / FLOP rate of each stage,
+             from the same steps run eagerly with an event between stages (so a
+             stage includes any host launch gap before its kernels);
   cpu_baseline  the CPU oracle (single-threaded C) timed on this host on a
              bounded sample of the same workload (rank 0, N=1 only).
 
@@ -216,17 +221,35 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     assert api.moe_get_device_errors() == 0, "device error during warm-up"
 
+    # the whole step as one CUDA graph (group sizes stay on the device, so the captured step is
+    # valid for any routing); replays carry no host launch gaps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert api.moe_get_device_errors() == 0, "device error during graph warm-up"
+
     K = args.steps
     ns = len(stages)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(local_rank))
     sampler.start()
     time.sleep(0.2)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # timed steps: graph replays (the step time); then the same steps eagerly with an event
+    # between stages (the per-stage breakdown)
     for i in range(K):
         flush.zero_()                                       # L2 flush, outside the timed interval
+        gev[i][0].record(stream)
+        graph.replay()
+        gev[i][1].record(stream)
+    for i in range(K):
+        flush.zero_()
         e = ev[i]
         e[0].record(stream)
         for j, (_, fn) in enumerate(stages):
@@ -235,7 +258,8 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][ns]) for i in range(K)]
+    step_ms = [a.elapsed_time(b) for a, b in gev]
+    eager_step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][ns]) for i in range(K))
     stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
                 for j, (name, _) in enumerate(stages)}
     total_ms = sum(step_ms)
@@ -273,7 +297,8 @@ def run_ours(args, wl, rank, world, local_rank):
 
     if world > 1:
         total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)
-    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, clocks=clocks, R=R, active=active, errs=errs,
+    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, eager_step_ms=eager_step_ms, clocks=clocks,
+                R=R, active=active, errs=errs,
                 h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2, launches=K * launches)
 
 
@@ -426,6 +451,9 @@ def main():
                      "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
                                      f"{peak_kind} dense bf16 burst" + (" x2 (fp8)" if fp8_ratio > 1 else "")),
                      "frac_of_sustained": round(achieved / peak_sustained, 4)},
+        "timing": "step = CUDA-graph replay of the whole step (events around each replay); stages = the "
+                  "same step run eagerly with an event between stages (eager step "
+                  f"{r['eager_step_ms']:.4f} ms); e2e = the eager host-buffer call",
         "stages": stages,
         "routes": r["R"],
         "clocks": r["clocks"],
