@@ -25,8 +25,9 @@ JSON line:
              against the measured dense bf16 burst peak (the timed loop is short
              and runs at maximum SM clock), the sustained figure given beside it;
   stages     mean per-stage time and the bandwidth / FLOP rate of each stage,
-             from the same steps run eagerly with an event between stages (so a
-             stage includes any host launch gap before its kernels);
+             from CUDA events recorded inside the captured graph between stages
+             (external event nodes, read after each replay); where the CUDA
+             runtime cannot be loaded for that, from the same steps run eagerly;
   cpu_baseline  the CPU oracle (single-threaded C) timed on this host on a
              bounded sample of the same workload (rank 0, N=1 only).
 
@@ -131,6 +132,44 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class GraphStageEvents:
+    """CUDA events recorded inside a captured graph as external event nodes
+    (cudaEventRecordWithFlags with cudaEventRecordExternal), read back after each replay:
+    per-stage device times of a graph replay, with no host launch gaps between stages.
+    Uses the CUDA runtime library through ctypes; `ok` is False where it cannot be loaded."""
+
+    def __init__(self, n: int):
+        import ctypes
+        import glob
+        self.C = ctypes
+        self.rt = None
+        cands = glob.glob("/usr/local/cuda/lib64/libcudart.so*") + glob.glob("/usr/local/cuda/lib/libcudart.so*")
+        for c in sorted(cands, reverse=True):
+            try:
+                self.rt = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        self.ev = []
+        self.ok = self.rt is not None
+        for _ in range(n if self.ok else 0):
+            e = ctypes.c_void_p()
+            if self.rt.cudaEventCreate(ctypes.byref(e)) != 0:
+                self.ok = False
+                break
+            self.ev.append(e)
+
+    def record(self, j: int, stream) -> None:
+        if self.rt.cudaEventRecordWithFlags(self.ev[j], self.C.c_void_p(stream.cuda_stream), 1) != 0:
+            self.ok = False
+
+    def elapsed_ms(self, a: int, b: int) -> float:
+        ms = self.C.c_float()
+        if self.rt.cudaEventElapsedTime(self.C.byref(ms), self.ev[a], self.ev[b]) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return float(ms.value)
+
+
 def gpu_id_for(dev_index: int) -> str:
     import torch
     try:
@@ -222,17 +261,25 @@ def run_ours(args, wl, rank, world, local_rank):
     assert api.moe_get_device_errors() == 0, "device error during warm-up"
 
     # the whole step as one CUDA graph (group sizes stay on the device, so the captured step is
-    # valid for any routing); replays carry no host launch gaps
+    # valid for any routing); replays carry no host launch gaps. Events recorded inside the graph
+    # between stages give each stage's device time within the replay.
+    ns = len(stages)
+    gse = GraphStageEvents(ns + 1)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        step()
+        cap = torch.cuda.current_stream()
+        for j, (_, fn) in enumerate(stages):
+            if gse.ok:
+                gse.record(j, cap)
+            fn()
+        if gse.ok:
+            gse.record(ns, cap)
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
     assert api.moe_get_device_errors() == 0, "device error during graph warm-up"
 
     K = args.steps
-    ns = len(stages)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(local_rank))
@@ -241,27 +288,41 @@ def run_ours(args, wl, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    # timed steps: graph replays (the step time); then the same steps eagerly with an event
-    # between stages (the per-stage breakdown)
+    # timed steps: graph replays; the step time and the per-stage times from the events inside
+    # the graph (read after each replay), else from events around the replay plus an eager pass
+    step_ms = []
+    per_stage = [[] for _ in range(ns)]
     for i in range(K):
         flush.zero_()                                       # L2 flush, outside the timed interval
         gev[i][0].record(stream)
         graph.replay()
         gev[i][1].record(stream)
-    for i in range(K):
-        flush.zero_()
-        e = ev[i]
-        e[0].record(stream)
-        for j, (_, fn) in enumerate(stages):
-            fn()
-            e[j + 1].record(stream)
+        if gse.ok:
+            torch.cuda.synchronize()
+            for j in range(ns):
+                per_stage[j].append(gse.elapsed_ms(j, j + 1))
+            step_ms.append(gse.elapsed_ms(0, ns))      # first to last stage, inside the replay
+    if not gse.ok:
+        for i in range(K):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            for j, (_, fn) in enumerate(stages):
+                fn()
+                e[j + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in gev]
-    eager_step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][ns]) for i in range(K))
-    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
-                for j, (name, _) in enumerate(stages)}
+    replay_ms = [a.elapsed_time(b) for a, b in gev]
+    inner_ms = statistics.mean(step_ms) if step_ms else None
+    step_ms = replay_ms                                   # the step time: events around each replay
+    if gse.ok:
+        stage_ms = {name: statistics.mean(per_stage[j]) for j, (name, _) in enumerate(stages)}
+        stage_source = "events inside the graph between stages"
+    else:
+        stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+                    for j, (name, _) in enumerate(stages)}
+        stage_source = "the same steps run eagerly with an event between stages"
     total_ms = sum(step_ms)
 
     # end to end through the host-memory call: x and logits in, y out (for the training
@@ -297,8 +358,8 @@ def run_ours(args, wl, rank, world, local_rank):
 
     if world > 1:
         total_ms, e2e_ms = reduce_max_over_ranks([total_ms, e2e_ms], dev)
-    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, eager_step_ms=eager_step_ms, clocks=clocks,
-                R=R, active=active, errs=errs,
+    return dict(total_ms=total_ms, e2e_ms=e2e_ms, stage_ms=stage_ms, stage_source=stage_source,
+                inner_ms=inner_ms, clocks=clocks, R=R, active=active, errs=errs,
                 h2d=x_host.numel() * 2 + lg_host.numel() * 4, d2h=y_host.numel() * 2, launches=K * launches)
 
 
@@ -451,9 +512,9 @@ def main():
                      "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
                                      f"{peak_kind} dense bf16 burst" + (" x2 (fp8)" if fp8_ratio > 1 else "")),
                      "frac_of_sustained": round(achieved / peak_sustained, 4)},
-        "timing": "step = CUDA-graph replay of the whole step (events around each replay); stages = the "
-                  "same step run eagerly with an event between stages (eager step "
-                  f"{r['eager_step_ms']:.4f} ms); e2e = the eager host-buffer call",
+        "timing": "step = CUDA-graph replay of the whole step, CUDA events around each replay"
+                  + (f" (first to last stage inside the replay: {r['inner_ms']:.4f} ms)" if r["inner_ms"] else "")
+                  + f"; stages = {r['stage_source']}; e2e = the eager host-buffer call",
         "stages": stages,
         "routes": r["R"],
         "clocks": r["clocks"],
