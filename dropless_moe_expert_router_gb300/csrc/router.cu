@@ -52,7 +52,9 @@ __device__ __forceinline__ bool beats(bool aa, float av, int ai, bool ba, float 
 
 // ---------------------------------------------------------------------------
 // Small path: G lanes per row (32 / G rows per warp), V logits per lane
-// (expert index = i * G + lane_in_group). E <= G * V, K <= 16.
+// (expert index = i * G + lane_in_group). E <= G * V, K <= 16. With one logit
+// per lane each lane ranks its logit against the row's G in one pass; with
+// more, K rounds of a segmented arg-max.
 // ---------------------------------------------------------------------------
 template <int G, int V>
 __global__ void __launch_bounds__(256) route_small_kernel(const float* __restrict__ logits, int T, int E,
@@ -81,26 +83,39 @@ __global__ void __launch_bounds__(256) route_small_kernel(const float* __restric
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
 
-    // K rounds of segmented arg-max
-    for (int k = 0; k < K; k++) {
-        bool ba = false;
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < V; i++) {
-            int e = i * G + gl;
-            if (beats(avail[i], v[i], e, ba, bv, bi)) { ba = avail[i]; bv = v[i]; bi = e; }
+    if constexpr (V == 1) {
+        // one logit per lane: its rank among the row's G logits (larger first, lower index
+        // on ties) in one pass of G compares; a rank below K is the output slot
+        const int e = gl;
+        int r = 0;
+        for (int j = 0; j < G; j++) {
+            const bool oa = __shfl_sync(FULL, avail[0], (lane & ~(G - 1)) + j);
+            const float ov = __shfl_sync(FULL, v[0], (lane & ~(G - 1)) + j);
+            r += beats(oa, ov, j, avail[0], v[0], e) ? 1 : 0;
         }
+        if (avail[0] && r < K) rank[0] = r;
+    } else {
+        // K rounds of segmented arg-max
+        for (int k = 0; k < K; k++) {
+            bool ba = false;
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
 #pragma unroll
-        for (int o = G / 2; o > 0; o >>= 1) {
-            bool oa = __shfl_xor_sync(FULL, ba, o);
-            float ov = __shfl_xor_sync(FULL, bv, o);
-            int oi = __shfl_xor_sync(FULL, bi, o);
-            if (beats(oa, ov, oi, ba, bv, bi)) { ba = oa; bv = ov; bi = oi; }
+            for (int i = 0; i < V; i++) {
+                int e = i * G + gl;
+                if (beats(avail[i], v[i], e, ba, bv, bi)) { ba = avail[i]; bv = v[i]; bi = e; }
+            }
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1) {
+                bool oa = __shfl_xor_sync(FULL, ba, o);
+                float ov = __shfl_xor_sync(FULL, bv, o);
+                int oi = __shfl_xor_sync(FULL, bi, o);
+                if (beats(oa, ov, oi, ba, bv, bi)) { ba = oa; bv = ov; bi = oi; }
+            }
+#pragma unroll
+            for (int i = 0; i < V; i++)
+                if (avail[i] && i * G + gl == bi) { avail[i] = false; rank[i] = k; }
         }
-#pragma unroll
-        for (int i = 0; i < V; i++)
-            if (avail[i] && i * G + gl == bi) { avail[i] = false; rank[i] = k; }
     }
     // denominators
     float den = 0.0f;
