@@ -246,7 +246,7 @@ def run_ours(args, wl, rank, world, local_rank):
         # the whole layer's backward, from dy [T, H]: combine, expert MLP (dgrad, dx, transposes,
         # wgrad), permute and router backward
         stages += [("combine_bwd", lambda: layer.stage_combine_backward(dy)),
-                   ("dgrad_dh", lambda: layer.stage_dgrad_dh(layer.dy_perm)), ("dgrad_dx", layer.stage_dgrad_dx),
+                   ("dgrad_dh", lambda: layer.stage_dgrad_dh(layer.dy_perm, dy_quantised=layer.fp8)), ("dgrad_dx", layer.stage_dgrad_dx),
                    ("wgrad_transpose", lambda: layer.stage_transposes(x, layer.dy_perm)),
                    ("wgrad_gemm", layer.stage_wgrad_gemm), ("permute_bwd", layer.stage_permute_backward),
                    ("route_bwd", lambda: layer.stage_route_backward(logits))]
@@ -390,8 +390,8 @@ def stage_report(wl, R, stage_ms, active=None):
         "route": T * E * 4 + T * K * (idb + 4),
         "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
         "combine": R * H * 2 + T * K * 8 + T * H * 2,
-        # read dy and y_perm, write dy_perm; route metadata and dprobs
-        "combine_bwd": T * H * 2 + R * H * 2 + R * H * 2 + T * K * 12,
+        # read dy and y_perm, write dy_perm (MXFP8: and its codes and scales); route metadata and dprobs
+        "combine_bwd": T * H * 2 + R * H * 2 + R * H * 2 + (R * H * (1 + 1 / 32) if fp8 else 0) + T * K * 12,
         "permute_bwd": R * H * 2 + T * H * 2 + T * K * 4,
         "route_bwd": T * E * 4 * 2 + T * K * (idb + 4),
         # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands

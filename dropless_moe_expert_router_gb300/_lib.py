@@ -26,7 +26,7 @@ SIGNATURES = {
     "moe_permute_noalloc": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, U, P]),
     "moe_quant_mxfp8_grouped": (I, [P, I, I, P, I, P, P, U, P]),
     "moe_unpermute_combine": (I, [P, P, P, I, I, I, P, P]),
-    "moe_unpermute_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P]),
+    "moe_unpermute_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P, P, P]),
     "moe_permute_backward": (I, [P, P, I, I, I, P, P]),
     "moe_route_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
     "moe_packed_weights_bytes": (SZ, [I, I, I, I, I]),

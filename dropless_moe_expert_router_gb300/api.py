@@ -220,9 +220,12 @@ def moe_route_topk_backward(logits: torch.Tensor, ids: torch.Tensor, dprobs: tor
 
 def moe_unpermute_combine_backward(dy: torch.Tensor, y_perm: torch.Tensor, row_map: torch.Tensor,
                                    probs: torch.Tensor, *, dy_perm: Optional[torch.Tensor] = None,
-                                   dprobs: Optional[torch.Tensor] = None, stream=None):
+                                   dprobs: Optional[torch.Tensor] = None, dy_perm_q: Optional[torch.Tensor] = None,
+                                   dy_perm_scales: Optional[torch.Tensor] = None, stream=None):
     """dy [T, H] bf16, y_perm [R_cap, H] bf16, row_map [T, K], probs [T, K] ->
-    (dy_perm [R_cap, H] bf16, dprobs [T, K] fp32)."""
+    (dy_perm [R_cap, H] bf16, dprobs [T, K] fp32). With dy_perm_q [R_cap, H] uint8 and
+    dy_perm_scales [R_cap, H/32] uint8 given, the kernel also writes the row-wise MXFP8
+    codes and scales of dy_perm into them."""
     _want(dy, "dy", torch.bfloat16, 2)
     _want(y_perm, "y_perm", torch.bfloat16, 2)
     _want(row_map, "row_map", torch.int32, 2)
@@ -235,8 +238,16 @@ def moe_unpermute_combine_backward(dy: torch.Tensor, y_perm: torch.Tensor, row_m
         dprobs = torch.empty((T, K), dtype=torch.float32, device=dy.device)
     _want(dy_perm, "dy_perm", torch.bfloat16, 2)
     _want(dprobs, "dprobs", torch.float32, 2)
+    if (dy_perm_q is None) != (dy_perm_scales is None):
+        raise ValueError("dy_perm_q and dy_perm_scales go together")
+    if dy_perm_q is not None:
+        _want(dy_perm_q, "dy_perm_q", torch.uint8, 2)
+        _want(dy_perm_scales, "dy_perm_scales", torch.uint8, 2)
+        if tuple(dy_perm_q.shape) != tuple(y_perm.shape) or tuple(dy_perm_scales.shape) != (y_perm.shape[0], H // 32):
+            raise ValueError("dy_perm_q must be [R_cap, H] and dy_perm_scales [R_cap, H/32]")
     st = _lib.load().moe_unpermute_combine_backward(_ptr(dy), _ptr(y_perm), _ptr(row_map), _ptr(probs), T, K, H,
-                                                    _ptr(dy_perm), _ptr(dprobs), _stream(stream))
+                                                    _ptr(dy_perm), _ptr(dprobs),
+                                                    _ptr(dy_perm_q), _ptr(dy_perm_scales), _stream(stream))
     _check("moe_unpermute_combine_backward", st)
     return dy_perm, dprobs
 

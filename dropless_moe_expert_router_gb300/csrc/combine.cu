@@ -143,16 +143,20 @@ namespace {
 
 // Combine backward, one warp per token: for each valid route (t, k) with row r,
 // dy_perm[r] = bf16(p[t,k] * dy[t]) and dprobs[t,k] = <dy[t], y_perm[r]> (fp32).
-// RB routes at a time; per 32-column slice of the row each lane loads one
-// 16-byte chunk of dy and of each route's y_perm row, writes the scaled dy
-// chunks and accumulates the routes' partial dot products, reduced at the end.
-template <int KC, int RB>
+// RB routes at a time; per 32-chunk slice of the row each lane loads one 16-byte
+// chunk of dy and of each route's y_perm row, writes the scaled dy chunks and
+// accumulates the routes' partial dot products, reduced at the end. Q: the bf16
+// dy_perm values are also quantised to MXFP8 along the row (1x32 blocks, four
+// lanes per block), the codes and scales of the next GEMM's operand.
+template <int KC, int RB, bool Q>
 __global__ void __launch_bounds__(256) combine_backward_kernel(const uint4* __restrict__ dy,
                                                                const uint4* __restrict__ y_perm,
                                                                const int* __restrict__ row_map,
                                                                const float* __restrict__ probs, int T, int K,
                                                                int H, uint4* __restrict__ dy_perm,
-                                                               float* __restrict__ dprobs) {
+                                                               float* __restrict__ dprobs,
+                                                               uint2* __restrict__ q,
+                                                               uint8_t* __restrict__ qs) {
     const int lane = (int)lane_id();
     const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
     const int H8 = H >> 3;
@@ -183,41 +187,54 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const uint4* __re
                 float pp[RB], dot[RB];
                 bool on[RB];
 #pragma unroll
-                for (int q = 0; q < RB; q++) {
-                    on[q] = m != 0u;
-                    const int b = on[q] ? __ffs(m) - 1 : 0;
-                    if (on[q]) m &= m - 1;
-                    rr[q] = __shfl_sync(FULL, rows[c], b);
-                    pp[q] = __shfl_sync(FULL, p[c], b);
-                    kk[q] = c * 32 + b;
-                    dot[q] = 0.0f;
+                for (int qq = 0; qq < RB; qq++) {
+                    on[qq] = m != 0u;
+                    const int b = on[qq] ? __ffs(m) - 1 : 0;
+                    if (on[qq]) m &= m - 1;
+                    rr[qq] = __shfl_sync(FULL, rows[c], b);
+                    pp[qq] = __shfl_sync(FULL, p[c], b);
+                    kk[qq] = c * 32 + b;
+                    dot[qq] = 0.0f;
                 }
-                for (int j = lane; j < H8; j += 32) {
+                for (int j0 = 0; j0 < H8; j0 += 32) {   // warp-uniform (the quantiser's quads)
+                    const int j = j0 + lane;
+                    const bool in = j < H8;
                     float gv[8];
-                    bf16x8_to_f32(__ldg(g + j), gv);
+                    bf16x8_to_f32(in ? __ldg(g + j) : make_uint4(0, 0, 0, 0), gv);
                     uint4 v[RB];
 #pragma unroll
-                    for (int q = 0; q < RB; q++)
-                        v[q] = on[q] ? __ldg(y_perm + (long long)rr[q] * H8 + j) : make_uint4(0, 0, 0, 0);
+                    for (int qq = 0; qq < RB; qq++)
+                        v[qq] = on[qq] && in ? __ldg(y_perm + (long long)rr[qq] * H8 + j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                    for (int q = 0; q < RB; q++) {
-                        if (!on[q]) continue;
+                    for (int qq = 0; qq < RB; qq++) {
+                        if (!on[qq]) continue;                 // warp-uniform
                         float yv[8], o[8];
-                        bf16x8_to_f32(v[q], yv);
+                        bf16x8_to_f32(v[qq], yv);
 #pragma unroll
                         for (int i = 0; i < 8; i++) {
-                            dot[q] = fmaf(gv[i], yv[i], dot[q]);
-                            o[i] = pp[q] * gv[i];
+                            dot[qq] = fmaf(gv[i], yv[i], dot[qq]);
+                            o[i] = pp[qq] * gv[i];
                         }
-                        __stcs(dy_perm + (long long)rr[q] * H8 + j, f32_to_bf16x8(o));
+                        const uint4 ob = f32_to_bf16x8(o);
+                        if (in) __stcs(dy_perm + (long long)rr[qq] * H8 + j, ob);
+                        if constexpr (Q) {
+                            float f[8];
+                            bf16x8_to_f32(ob, f);               // the stored bf16 values
+                            int sb;
+                            const uint2 code = quant8_in_quad(f, &sb);
+                            if (in) {
+                                q[(long long)rr[qq] * H8 + j] = code;
+                                if ((lane & 3) == 0) qs[(long long)rr[qq] * (H >> 5) + (j >> 2)] = (uint8_t)sb;
+                            }
+                        }
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < RB; q++) {
-                    float d = dot[q];
+                for (int qq = 0; qq < RB; qq++) {
+                    float d = dot[qq];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
-                    if (on[q] && lane == 0) dprobs[t * K + kk[q]] = d;
+                    if (on[qq] && lane == 0) dprobs[t * K + kk[qq]] = d;
                 }
             }
         }
@@ -266,26 +283,36 @@ extern "C" moe_status moe_permute_backward(const void* dx_perm, const int32_t* r
 
 extern "C" moe_status moe_unpermute_combine_backward(const void* dy, const void* y_perm, const int32_t* row_map,
                                                      const float* probs, int T, int K, int H, void* dy_perm,
-                                                     float* dprobs, moe_stream_t stream) {
+                                                     float* dprobs, uint8_t* dy_perm_q, uint8_t* dy_perm_scales,
+                                                     moe_stream_t stream) {
     using namespace moe;
     if (T < 0 || K < 1 || K > 128 || H < 8 || (H % 8) != 0) return MOE_ERR_INVALID_ARG;
+    const bool quant = dy_perm_q != nullptr || dy_perm_scales != nullptr;
+    if (quant && (!dy_perm_q || !dy_perm_scales || (H % 32) != 0)) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!dy || !y_perm || !row_map || !probs || !dy_perm || !dprobs) return MOE_ERR_INVALID_ARG;
     if (!moe_host::aligned(dy, 16) || !moe_host::aligned(y_perm, 16) || !moe_host::aligned(dy_perm, 16) ||
-        !moe_host::aligned(row_map, 4) || !moe_host::aligned(probs, 4) || !moe_host::aligned(dprobs, 4))
+        !moe_host::aligned(row_map, 4) || !moe_host::aligned(probs, 4) || !moe_host::aligned(dprobs, 4) ||
+        (quant && !moe_host::aligned(dy_perm_q, 8)))
         return MOE_ERR_ALIGNMENT;
     long long blocks = ((long long)T + 7) / 8;
     const long long cap = (long long)device_sms() * 16;
     if (blocks > cap) blocks = cap;
     cudaStream_t s = moe_host::as_stream(stream);
     const int KC = (K + 31) / 32;
-#define MOE_COMBINE_BWD(kc)                                                                              \
-    combine_backward_kernel<kc, 4><<<(int)blocks, 256, 0, s>>>((const uint4*)dy, (const uint4*)y_perm,  \
-                                                               row_map, probs, T, K, H, (uint4*)dy_perm, \
-                                                               dprobs)
-    if (KC == 1) MOE_COMBINE_BWD(1);
-    else if (KC == 2) MOE_COMBINE_BWD(2);
-    else MOE_COMBINE_BWD(4);
+#define MOE_COMBINE_BWD(kc, qz)                                                                          \
+    combine_backward_kernel<kc, 4, qz><<<(int)blocks, 256, 0, s>>>((const uint4*)dy, (const uint4*)y_perm, \
+                                                                   row_map, probs, T, K, H, (uint4*)dy_perm, \
+                                                                   dprobs, (uint2*)dy_perm_q, dy_perm_scales)
+    if (quant) {
+        if (KC == 1) MOE_COMBINE_BWD(1, true);
+        else if (KC == 2) MOE_COMBINE_BWD(2, true);
+        else MOE_COMBINE_BWD(4, true);
+    } else {
+        if (KC == 1) MOE_COMBINE_BWD(1, false);
+        else if (KC == 2) MOE_COMBINE_BWD(2, false);
+        else MOE_COMBINE_BWD(4, false);
+    }
 #undef MOE_COMBINE_BWD
     return moe_host::launch_status();
 }

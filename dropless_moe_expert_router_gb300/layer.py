@@ -121,14 +121,17 @@ class MoELayer:
     def launches_per_backward(self) -> int:
         return 8 + (2 if self.fp8 else 0)
 
+    # (for MXFP8 the combine backward also quantises dy_perm, so dy's quantisation drops out)
     @property
     def launches_per_backward_full(self) -> int:
-        return self.launches_per_backward + 3
+        return self.launches_per_backward + 3 - (1 if self.fp8 else 0)
 
     def stage_combine_backward(self, dy: torch.Tensor, stream=None):
-        """dy [T, H] bf16 (gradient of the layer output) -> dy_perm [R_cap, H], dprobs [T, K]."""
+        """dy [T, H] bf16 (gradient of the layer output) -> dy_perm [R_cap, H], dprobs [T, K]
+        (MXFP8: and dy_perm's row-wise codes and scales, the down-projection dgrad's operand)."""
         api.moe_unpermute_combine_backward(dy, self.y_perm, self.perm.row_map, self.probs, dy_perm=self.dy_perm,
-                                           dprobs=self.dprobs, stream=stream)
+                                           dprobs=self.dprobs, dy_perm_q=self.dy_q, dy_perm_scales=self.dy_s,
+                                           stream=stream)
 
     def stage_permute_backward(self, stream=None):
         """dx_perm (the expert backward's) -> dx [T, H]: each token's rows summed."""
@@ -139,12 +142,14 @@ class MoELayer:
         api.moe_route_topk_backward(logits, self.ids, self.dprobs, renorm=self.renorm, dlogits=self.dlogits,
                                     stream=stream)
 
-    def stage_dgrad_dh(self, dy_perm: torch.Tensor, stream=None):
-        """dy_perm [R_cap, H] bf16 -> dab = SwiGLU backward of dh = dy W2^T (bf16)."""
+    def stage_dgrad_dh(self, dy_perm: torch.Tensor, stream=None, dy_quantised: bool = False):
+        """dy_perm [R_cap, H] bf16 -> dab = SwiGLU backward of dh = dy W2^T (bf16). dy_quantised:
+        (MXFP8) dy_perm's codes and scales are already in dy_q / dy_s (the combine backward's)."""
         goff = self.perm.group_offsets
         bw = self.bwd_weights
         if self.fp8:
-            api.moe_quant_mxfp8_grouped(dy_perm, goff, q=self.dy_q, scales=self.dy_s, stream=stream)
+            if not dy_quantised:
+                api.moe_quant_mxfp8_grouped(dy_perm, goff, q=self.dy_q, scales=self.dy_s, stream=stream)
             api.moe_grouped_swiglu_dgrad(self.dy_q, self.dy_s, bw, self.ab, goff, dab=self.dab, stream=stream)
         else:
             api.moe_grouped_swiglu_dgrad(dy_perm, None, bw, self.ab, goff, dab=self.dab, stream=stream)
@@ -181,10 +186,10 @@ class MoELayer:
                                    split=True, dw=self.dW1, dw2=self.dW3, stream=stream)
         return self.dW1, self.dW3, self.dW2
 
-    def backward(self, x: torch.Tensor, dy_perm: torch.Tensor, stream=None):
+    def backward(self, x: torch.Tensor, dy_perm: torch.Tensor, stream=None, dy_quantised: bool = False):
         """Grouped backward of the expert MLP after a training forward (x: the forward's tokens,
         dy_perm: gradient of y_perm) -> (dx_perm, dW1, dW3, dW2)."""
-        self.stage_dgrad_dh(dy_perm, stream)
+        self.stage_dgrad_dh(dy_perm, stream, dy_quantised)
         dx = self.stage_dgrad_dx(stream)
         self.stage_transposes(x, dy_perm, stream)
         return (dx,) + tuple(self.stage_wgrad_gemm(stream))
@@ -193,7 +198,7 @@ class MoELayer:
         """Backward of the whole layer after a training forward (x, logits: the forward's inputs;
         dy [T, H]: gradient of its output) -> (dx [T, H], dlogits [T, E], dW1, dW3, dW2)."""
         self.stage_combine_backward(dy, stream)
-        _, dw1, dw3, dw2 = self.backward(x, self.dy_perm, stream)
+        _, dw1, dw3, dw2 = self.backward(x, self.dy_perm, stream, dy_quantised=self.fp8)
         self.stage_permute_backward(stream)
         self.stage_route_backward(logits, stream)
         return self.dx_tokens, self.dlogits, dw1, dw3, dw2

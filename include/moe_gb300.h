@@ -351,11 +351,17 @@ moe_status moe_unpermute_combine(const void *y_perm, const int32_t *row_map,
  * bf16 (the forward's), row_map [T, K], probs [T, K] fp32 in; dy_perm
  * [R_cap, H] bf16 (rows no route maps to are not written) and dprobs [T, K]
  * fp32 out. Requires H % 8 == 0, 1 <= K <= 128; 16-byte aligned rows.
+ * Optional (both or neither; NULL skips): dy_perm_q [R_cap, H] E4M3 bytes
+ * (8-byte aligned) and dy_perm_scales [R_cap, H/32] E8M0 bytes, the row-wise
+ * MXFP8 quantisation (1x32 blocks along H, as moe_quant_mxfp8_grouped writes
+ * it) of the bf16 dy_perm values, for the next grouped GEMM; requires
+ * H % 32 == 0. Same rows written as dy_perm.
  * ------------------------------------------------------------------------ */
 moe_status moe_unpermute_combine_backward(const void *dy, const void *y_perm,
                                           const int32_t *row_map, const float *probs,
                                           int T, int K, int H, void *dy_perm,
-                                          float *dprobs, moe_stream_t stream);
+                                          float *dprobs, uint8_t *dy_perm_q,
+                                          uint8_t *dy_perm_scales, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Permute backward: the adjoint of moe_permute's row copies, dx[t] = bf16(sum

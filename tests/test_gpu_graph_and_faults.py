@@ -88,10 +88,14 @@ def test_training_step_graph_matches_eager():
         assert torch.equal(a, b)
 
 
-def test_full_layer_backward_graph_matches_eager():
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_full_layer_backward_graph_matches_eager(precision):
     """Forward + the whole layer's backward (combine, expert MLP, permute and router backward)
-    captured in one graph: replays give the eager results bit for bit."""
-    wl = W.get("tiny", T=512, H=256, F=256)
+    captured in one graph: replays give the eager results bit for bit. MXFP8: the combine
+    backward's fused quantisation of dy_perm feeds the dgrad exactly as the separate row
+    quantiser would."""
+    hf = 512 if precision == "mxfp8" else 256    # MXFP8 GEMMs take H, F in multiples of 512
+    wl = W.get("tiny", T=512, H=hf, F=hf, precision=precision)
     layer = _layer(wl, training=True)
     x = W.x(wl).cuda()
     lg = W.logits(wl).cuda()
@@ -113,6 +117,14 @@ def test_full_layer_backward_graph_matches_eager():
         assert torch.equal(a, b)
     # the pieces compose: dx is the permute backward of the expert backward's dx_perm
     assert torch.equal(outs[0], api.moe_permute_backward(layer.dx, layer.perm.row_map))
+    if precision == "mxfp8":
+        dab = layer.dab.clone()
+        q, sc = layer.dy_q.clone(), layer.dy_s.clone()
+        layer.stage_dgrad_dh(layer.dy_perm, dy_quantised=False)
+        torch.cuda.synchronize()
+        R = int(layer.perm.group_offsets[-1].item())
+        assert torch.equal(layer.dy_q[:R], q[:R]) and torch.equal(layer.dy_s[:R], sc[:R])
+        assert torch.equal(layer.dab, dab)
 
 
 def test_bounded_wait_gives_up_and_reports():

@@ -107,3 +107,47 @@ def test_combine_backward_all_routes_invalid_and_single_token():
     assert np.all(dpr.cpu().numpy() == 0.0)
     dx = api.moe_permute_backward(yp.cuda(), torch.from_numpy(rm).cuda())
     assert torch.count_nonzero(dx.float()).item() == 0
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"H": 96}), ("tiny", {"H": 2080, "T": 77}),
+                                       ("mixtral", {"T": 1024}), ("dsv3", {"T": 512}), ("heavy", {"T": 256})])
+def test_combine_backward_fused_mxfp8_matches_oracle(name, over):
+    """The combine backward's row-wise MXFP8 codes and scales of dy_perm: with power-of-two
+    probabilities p * dy is exact, so dy_perm equals the oracle's bit for bit and its codes
+    and scales must equal the oracle's row quantiser of the oracle's dy_perm. H = 96 and
+    2080 leave a ragged last slice of the row (not a multiple of 256 columns)."""
+    wl = W.get(name, **over)
+    _, ids, _ = _routes(wl)
+    rng = np.random.default_rng(7)
+    probs = np.where(ids >= 0, 2.0 ** -rng.integers(0, 5, ids.shape), 0.0).astype(np.float32)
+    op = O.permute(None, ids, wl.E)
+    rm, R = op["row_map"], op["R"]
+    yp = W.expert_out(wl)
+    dy = W.dy(wl)
+    R_cap, H = yp.shape
+    q = torch.zeros((R_cap, H), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((R_cap, H // 32), dtype=torch.uint8, device="cuda")
+    dyp, dpr = api.moe_unpermute_combine_backward(dy.cuda(), yp.cuda(), torch.from_numpy(rm).cuda(),
+                                                  torch.from_numpy(probs).cuda(), dy_perm_q=q, dy_perm_scales=s)
+    ref_dyp, ref_dpr = O.combine_backward(bf16_bits(dy), bf16_bits(yp), rm, probs)
+    assert np.array_equal(bf16_bits(dyp)[:R], ref_dyp[:R])
+    ref_q, ref_s = O.quant_rows(ref_dyp[:R])
+    assert np.array_equal(q.cpu().numpy()[:R], ref_q)
+    assert np.array_equal(s.cpu().numpy()[:R], ref_s)
+    assert rel_err(dpr.cpu().numpy().astype(np.float64), ref_dpr) <= 1e-3
+    assert api.moe_get_device_errors() == 0
+
+
+def test_combine_backward_fused_mxfp8_argument_errors():
+    wl = W.get("tiny", H=72)                    # H % 32 != 0: no 1x32 blocks
+    _, ids, probs = _routes(wl)
+    rm = O.permute(None, ids, wl.E)["row_map"]
+    yp = W.expert_out(wl).cuda()
+    q = torch.zeros(yp.shape, dtype=torch.uint8, device="cuda")
+    s = torch.zeros((yp.shape[0], 2), dtype=torch.uint8, device="cuda")
+    with pytest.raises(Exception):
+        api.moe_unpermute_combine_backward(W.dy(wl).cuda(), yp, torch.from_numpy(rm).cuda(),
+                                           torch.from_numpy(probs).cuda(), dy_perm_q=q, dy_perm_scales=s)
+    with pytest.raises(ValueError):
+        api.moe_unpermute_combine_backward(W.dy(wl).cuda(), yp, torch.from_numpy(rm).cuda(),
+                                           torch.from_numpy(probs).cuda(), dy_perm_q=q)
