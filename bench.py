@@ -398,7 +398,8 @@ def stage_report(wl, R, stage_ms, active=None):
         "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
         "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * q,
         "gemm_down": R * F * q + Ea * F * H * q + R * H * 2,
-        "dgrad_dh": R * H * q + Ea * F * H * q + R * 2 * F * 2 * 2,
+        # read dy, W2, (a | b); write dab (MXFP8: and its codes and scales)
+        "dgrad_dh": R * H * q + Ea * F * H * q + R * 2 * F * 2 * 2 + (R * 2 * F * (1 + 1 / 32) if fp8 else 0),
         "dgrad_dx": R * 2 * F * q + Ea * 2 * F * H * q + R * H * 2,
         "wgrad_gemm": R * (F + H + H + 2 * F) * q + Ea * 3 * H * F * 2,
     }

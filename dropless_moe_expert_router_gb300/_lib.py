@@ -35,7 +35,7 @@ SIGNATURES = {
     "moe_grouped_gemm_up": (I, [P, P, P, P, I, P, I, I, I, I, P, P, P, P, P]),
     "moe_grouped_gemm_down": (I, [P, P, P, P, I, P, I, I, I, I, P, P]),
     "moe_prepare_weights_bwd": (I, [P, P, P, I, I, I, I, P, P, P, P, P]),
-    "moe_grouped_swiglu_dgrad": (I, [P, P, P, P, P, I, P, I, I, I, I, P, P]),
+    "moe_grouped_swiglu_dgrad": (I, [P, P, P, P, P, I, P, I, I, I, I, P, P, P, P]),
     "moe_grouped_gemm_dx": (I, [P, P, P, P, I, P, I, I, I, I, P, P]),
     "moe_grouped_transpose_kpad": (SZ, [I, I]),
     "moe_grouped_transpose": (I, [P, P, I, I, P, I, I, P, P, P]),

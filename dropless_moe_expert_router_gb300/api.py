@@ -405,14 +405,24 @@ def moe_prepare_weights_bwd(w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor
 
 def moe_grouped_swiglu_dgrad(dy: torch.Tensor, dy_scales: Optional[torch.Tensor], bw: BwdWeights,
                              ab: torch.Tensor, group_offsets: torch.Tensor, *, dab: Optional[torch.Tensor] = None,
+                             dab_q: Optional[torch.Tensor] = None, dab_scales: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
-    """dy [R_cap, H] (bf16 or MXFP8 codes) -> dab [R_cap, 2F] bf16 (da | db interleaved per 128)."""
+    """dy [R_cap, H] (bf16 or MXFP8 codes) -> dab [R_cap, 2F] bf16 (da | db interleaved per 128).
+    With dab_q [R_cap, 2F] uint8 and dab_scales [R_cap, 2F/32] uint8 given, the epilogue also
+    writes the row-wise MXFP8 codes and scales of dab into them."""
     R_cap = dy.shape[0]
     if dab is None:
         dab = torch.empty((R_cap, 2 * bw.F), dtype=torch.bfloat16, device=dy.device)
+    if (dab_q is None) != (dab_scales is None):
+        raise ValueError("dab_q and dab_scales go together")
+    if dab_q is not None:
+        _want(dab_q, "dab_q", torch.uint8, 2)
+        _want(dab_scales, "dab_scales", torch.uint8, 2)
+        if tuple(dab_q.shape) != (R_cap, 2 * bw.F) or tuple(dab_scales.shape) != (R_cap, 2 * bw.F // 32):
+            raise ValueError("dab_q must be [R_cap, 2F] and dab_scales [R_cap, 2F/32]")
     st = _lib.load().moe_grouped_swiglu_dgrad(
         _ptr(dy), _ptr(dy_scales), _ptr(bw.w2b), _ptr(bw.w2b_scales), _ptr(ab), _dt_code(bw.precision),
-        _ptr(group_offsets), bw.E, bw.H, bw.F, R_cap, _ptr(dab), _stream(stream))
+        _ptr(group_offsets), bw.E, bw.H, bw.F, R_cap, _ptr(dab), _ptr(dab_q), _ptr(dab_scales), _stream(stream))
     _check("moe_grouped_swiglu_dgrad", st)
     return dab
 

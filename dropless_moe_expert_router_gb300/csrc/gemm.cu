@@ -109,7 +109,8 @@ struct GemmArgs {
     int R_cap;                   // rows of A (row-grouped)
     void* out;                   // output (see the mode)
     int ldo;                     // output row stride in elements
-    uint8_t* out_scales;         // UP + MXFP8: h scales [R_cap, ldo/32]
+    uint8_t* out_scales;         // UP + MXFP8: h scales [R_cap, ldo/32]; DGRAD: optional dab scales
+    uint8_t* out_q;              // DGRAD: optional row-wise MXFP8 codes of dab [R_cap, ldo]
     const uint8_t* a_scales;     // MXFP8 scales of A: [rows of A][sf_row_bytes]
     const uint8_t* b_scales;     // MXFP8 scales of B
     int sf_row_bytes;            // scale bytes per operand row (= contraction length / 32)
@@ -126,6 +127,21 @@ constexpr size_t smem_bytes_for(int E) {
     using C = Cfg<FP8, PAIR>;
     return 1024 /* alignment slack */ + (size_t)C::RING_BYTES + 256 /* barriers, flags */ +
            (size_t)C::THREADS * 4 + (size_t)2 * (E + 1) * 4;
+}
+
+// One 1x32 MXFP8 block held by one thread: E8M0 scale byte from the block's amax,
+// E4M3 codes (RNE, saturating) of v / 2^(byte - 127) packed four per word.
+__device__ __forceinline__ int quant32_in_thread(const float* v, uint32_t* w) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(v[i]));
+    const int sbyte = e8m0_scale_byte(amax);
+    const float inv = e8m0_inv_scale(sbyte);
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        w[i] = (uint32_t)f32x2_to_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+               ((uint32_t)f32x2_to_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    return sbyte;
 }
 
 struct TileInfo {
@@ -632,16 +648,8 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; i++) hv[i] = silu_f(hv[i]) * f[64 + 32 * c + i];
                     if constexpr (FP8) {
-                        float amax = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(hv[i]));
-                        const int sbyte = e8m0_scale_byte(amax);
-                        const float inv = e8m0_inv_scale(sbyte);
                         uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; i++)
-                            w[i] = (uint32_t)f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
-                                   ((uint32_t)f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
+                        const int sbyte = quant32_in_thread(hv, w);
                         if (valid) {
                             store_32B(static_cast<uint8_t*>(p.out) + r * p.ldo + hcol, w, p.st32);
                             p.out_scales[r * (p.ldo / 32) + hcol / 32] = (uint8_t)sbyte;
@@ -692,6 +700,24 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                         store_32B(o + off + 16, wa + 8, p.st32);
                         store_32B(o + off + 128, wb, p.st32);
                         store_32B(o + off + 144, wb + 8, p.st32);
+                        if (p.out_q) {
+                            // row-wise MXFP8 of the bf16 da and db blocks just stored (the dx GEMM's operand)
+#pragma unroll
+                            for (int half = 0; half < 2; half++) {
+                                const uint32_t* src2 = half ? wb : wa;
+                                float fv[32];
+#pragma unroll
+                                for (int i = 0; i < 16; i++) {
+                                    fv[2 * i] = __uint_as_float(src2[i] << 16);
+                                    fv[2 * i + 1] = __uint_as_float(src2[i] & 0xffff0000u);
+                                }
+                                uint32_t w[8];
+                                const int sbyte = quant32_in_thread(fv, w);
+                                const long long qo = off + 128 * half;
+                                store_32B(p.out_q + qo, w, p.st32);
+                                p.out_scales[qo >> 5] = (uint8_t)sbyte;
+                            }
+                        }
                     }
                 }
             } else if constexpr (MODE == MODE_WGRAD) {
@@ -952,7 +978,8 @@ extern "C" moe_status moe_grouped_swiglu_gemm(const void* x_perm, const uint8_t*
 extern "C" moe_status moe_grouped_swiglu_dgrad(const void* dy, const uint8_t* dy_scales, const void* w2_bwd,
                                                const uint8_t* w2_bwd_scales, const void* ab, moe_dtype dtype,
                                                const int32_t* group_offsets, int E, int H, int F, int R_cap,
-                                               void* dab, moe_stream_t stream) {
+                                               void* dab, uint8_t* dab_q, uint8_t* dab_scales,
+                                               moe_stream_t stream) {
     using namespace moe;
     moe_status st = check_common(dtype, group_offsets, E, H, F, R_cap);
     if (st != MOE_OK) return st;
@@ -960,8 +987,9 @@ extern "C" moe_status moe_grouped_swiglu_dgrad(const void* dy, const uint8_t* dy
     if (R_cap == 0) return MOE_OK;
     const bool fp8 = dtype == MOE_MXFP8;
     if (!dy || !w2_bwd || !ab || !dab || (fp8 && (!dy_scales || !w2_bwd_scales))) return MOE_ERR_INVALID_ARG;
+    if ((dab_q == nullptr) != (dab_scales == nullptr)) return MOE_ERR_INVALID_ARG;
     if (!al(dy, 128) || !al(w2_bwd, 128) || !al(ab, 16) || !al(dab, 16) ||
-        (fp8 && (!al(dy_scales, 16) || !al(w2_bwd_scales, 16))))
+        (fp8 && (!al(dy_scales, 16) || !al(w2_bwd_scales, 16))) || (dab_q && !al(dab_q, 32)))
         return MOE_ERR_ALIGNMENT;
     GemmArgs a{};
     a.goff = group_offsets;
@@ -976,6 +1004,8 @@ extern "C" moe_status moe_grouped_swiglu_dgrad(const void* dy, const uint8_t* dy
     a.b_scales = w2_bwd_scales;
     a.sf_row_bytes = H / 32;
     a.ab = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ab));
+    a.out_q = dab_q;
+    a.out_scales = dab_scales;
     return launch_mode<MODE_DGRAD>(fp8, dy, (uint64_t)R_cap, w2_bwd, (uint64_t)E * F, (uint64_t)H, a,
                                    moe_host::as_stream(stream));
 }

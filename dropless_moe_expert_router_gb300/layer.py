@@ -115,16 +115,16 @@ class MoELayer:
         return self.y
 
     # ------------------------------------------------------------ backward
-    # library launches of the expert-MLP backward: dgrad 1, dx 1, transposes 4, wgrad 2 (+ 2
-    # quantisations for MXFP8); the full layer backward adds combine, permute and router backward
+    # library launches of the expert-MLP backward: dgrad 1, dx 1, transposes 4, wgrad 2 (+ dy's
+    # quantisation for MXFP8; dab's comes out of the dgrad epilogue); the full layer backward adds
+    # combine, permute and router backward (and for MXFP8 the combine backward quantises dy_perm)
     @property
     def launches_per_backward(self) -> int:
-        return 8 + (2 if self.fp8 else 0)
+        return 8 + (1 if self.fp8 else 0)
 
-    # (for MXFP8 the combine backward also quantises dy_perm, so dy's quantisation drops out)
     @property
     def launches_per_backward_full(self) -> int:
-        return self.launches_per_backward + 3 - (1 if self.fp8 else 0)
+        return 8 + 3
 
     def stage_combine_backward(self, dy: torch.Tensor, stream=None):
         """dy [T, H] bf16 (gradient of the layer output) -> dy_perm [R_cap, H], dprobs [T, K]
@@ -150,16 +150,17 @@ class MoELayer:
         if self.fp8:
             if not dy_quantised:
                 api.moe_quant_mxfp8_grouped(dy_perm, goff, q=self.dy_q, scales=self.dy_s, stream=stream)
-            api.moe_grouped_swiglu_dgrad(self.dy_q, self.dy_s, bw, self.ab, goff, dab=self.dab, stream=stream)
+            api.moe_grouped_swiglu_dgrad(self.dy_q, self.dy_s, bw, self.ab, goff, dab=self.dab, dab_q=self.dab_q,
+                                         dab_scales=self.dab_s, stream=stream)
         else:
             api.moe_grouped_swiglu_dgrad(dy_perm, None, bw, self.ab, goff, dab=self.dab, stream=stream)
 
     def stage_dgrad_dx(self, stream=None):
-        """dab -> dx = da W1^T + db W3^T [R_cap, H] bf16."""
+        """dab -> dx = da W1^T + db W3^T [R_cap, H] bf16 (MXFP8: from the codes and scales of dab
+        that the dgrad epilogue wrote)."""
         goff = self.perm.group_offsets
         bw = self.bwd_weights
         if self.fp8:
-            api.moe_quant_mxfp8_grouped(self.dab, goff, q=self.dab_q, scales=self.dab_s, stream=stream)
             api.moe_grouped_gemm_dx(self.dab_q, self.dab_s, bw, goff, dx=self.dx, stream=stream)
         else:
             api.moe_grouped_gemm_dx(self.dab, None, bw, goff, dx=self.dx, stream=stream)

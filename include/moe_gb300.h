@@ -282,7 +282,10 @@ moe_status moe_grouped_gemm_down(const void *h, const uint8_t *h_scales, const v
  *
  * moe_grouped_swiglu_dgrad: dy [R_cap, H] (bf16, or MXFP8 row-wise: E4M3 +
  *   dy_scales [R_cap, H/32]) -> dab [R_cap, 2F] bf16 = (da | db) interleaved per
- *   128 columns like ab. Requires F % 256 == 0.
+ *   128 columns like ab. Requires F % 256 == 0. Optional (both or neither, NULL
+ *   skips): dab_q [R_cap, 2F] E4M3 bytes (32-byte aligned) and dab_scales
+ *   [R_cap, 2F/32] E8M0, the row-wise MXFP8 of the bf16 dab (1x32 blocks along
+ *   2F, as moe_quant_mxfp8_grouped writes it), for moe_grouped_gemm_dx.
  * moe_grouped_gemm_dx: dab (bf16, or MXFP8 row-wise along 2F) -> dx [R_cap, H] bf16.
  * moe_grouped_transpose: makes a weight-gradient operand: for x [R_cap, C] bf16
  *   (or, with src_rows != NULL, x [*, C] read at row src_rows[r], e.g. the
@@ -307,7 +310,8 @@ moe_status moe_prepare_weights_bwd(const void *w1, const void *w3, const void *w
 moe_status moe_grouped_swiglu_dgrad(const void *dy, const uint8_t *dy_scales, const void *w2_bwd,
                                     const uint8_t *w2_bwd_scales, const void *ab, moe_dtype dtype,
                                     const int32_t *group_offsets, int E, int H, int F, int R_cap,
-                                    void *dab, moe_stream_t stream);
+                                    void *dab, uint8_t *dab_q, uint8_t *dab_scales,
+                                    moe_stream_t stream);
 
 moe_status moe_grouped_gemm_dx(const void *dab, const uint8_t *dab_scales, const void *w13t,
                                const uint8_t *w13t_scales, moe_dtype dtype,

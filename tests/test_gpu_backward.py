@@ -76,8 +76,13 @@ def _gpu_backward(wl, ids, precision, seed=0):
     dyd = dy.to(dev)
     if fp8:
         dyq, dys = api.moe_quant_mxfp8_grouped(dyd, goff)
-        dab = api.moe_grouped_swiglu_dgrad(dyq, dys, bw, ab, goff)
-        dabq, dabs = api.moe_quant_mxfp8_grouped(dab, goff)
+        dabq = torch.zeros((R_cap, 2 * wl.F), dtype=torch.uint8, device=dev)
+        dabs = torch.zeros((R_cap, 2 * wl.F // 32), dtype=torch.uint8, device=dev)
+        dab = api.moe_grouped_swiglu_dgrad(dyq, dys, bw, ab, goff, dab_q=dabq, dab_scales=dabs)
+        # the epilogue's codes and scales of dab are the row quantiser's (pinned to the oracle's)
+        sq, ss = api.moe_quant_mxfp8_grouped(dab, goff)
+        R = int(goff[-1].item())
+        assert torch.equal(dabq[:R], sq[:R]) and torch.equal(dabs[:R], ss[:R])
         dx = api.moe_grouped_gemm_dx(dabq, dabs, bw, goff)
     else:
         dab = api.moe_grouped_swiglu_dgrad(dyd, None, bw, ab, goff)
