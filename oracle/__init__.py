@@ -165,6 +165,29 @@ def route_topk(logits, K: int, renorm: bool = False):
     return ids, probs
 
 
+def route_sigmoid_topk(logits, K: int, bias=None, renorm: bool = False):
+    """Sigmoid scores, selection on score + bias -> (ids [T, K] int32, probs [T, K] fp32)."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.zeros((T, K), np.int32)
+    probs = np.zeros((T, K), np.float32)
+    lib().oracle_route_sigmoid_topk(_p(lg), _p(b), T, E, K, int(bool(renorm)), _p(ids), _p(probs))
+    return ids, probs
+
+
+def route_sigmoid_backward(logits, ids, dprobs, renorm: bool = False):
+    """dlogits [T, E] (float64) of route_sigmoid_topk's probabilities, selection held fixed."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    idv = _c(ids, np.int32)
+    K = idv.shape[1]
+    dp = _c(dprobs, np.float32)
+    out = np.zeros((T, E), np.float64)
+    lib().oracle_route_sigmoid_backward(_p(lg), _p(idv), _p(dp), T, E, K, int(bool(renorm)), _p(out))
+    return out
+
+
 # ----------------------------------------------------------------- permute
 def permute(x_bf16, ids, E: int):
     """Returns dict(x_perm [T*K, H] (rows >= R zero), group_sizes, group_offsets,

@@ -275,6 +275,108 @@ void oracle_route_topk(const float *logits, int T, int E, int K, int renorm,
     free(row);
 }
 
+/*
+ * Sigmoid-score routing with a per-expert selection bias. The pages name the
+ * router's "score transformation" and the "bias statistics" that compact
+ * routes must preserve ([SPARSER] "The workload changes the bottleneck",
+ * "Preserve a compact route") without defining either. Reading taken: the
+ * DeepSeek-style score function and bias-steered selection --
+ *   score     s_e = 1 / (1 + exp(-l_e))     (double, rounded once to fp32)
+ *   key       k_e = s_e + b_e               (fp32 addition; b = 0 when absent)
+ *   ids       the K largest keys, in descending key order, lower index first
+ *             on equal keys (IEEE compare)
+ *   probs     s at the selected ids, or with renorm s / (sum of the K selected
+ *             s) (double, rounded to fp32).
+ * The bias steers only the selection; the bias statistics are the per-expert
+ * counts of valid routes (oracle_permute's group_sizes).
+ */
+static float sigmoid_f32(float l)
+{
+    return (float)(1.0 / (1.0 + exp(-(double)l)));
+}
+
+void oracle_route_sigmoid_topk(const float *logits, const float *bias, int T, int E, int K, int renorm,
+                               int32_t *ids, float *probs)
+{
+    scored *row = (scored *)malloc(sizeof(scored) * (size_t)E);
+    float *sc = (float *)malloc(sizeof(float) * (size_t)E);
+    for (int t = 0; t < T; t++) {
+        const float *l = logits + (size_t)t * E;
+        for (int e = 0; e < E; e++) {
+            sc[e] = sigmoid_f32(l[e]);
+            volatile float key = sc[e] + (bias ? bias[e] : 0.0f);   /* one fp32 rounding */
+            row[e].v = key;
+            row[e].idx = e;
+        }
+        qsort(row, (size_t)E, sizeof(scored), cmp_scored);
+        double denom = 0.0;
+        for (int k = 0; k < K; k++)
+            denom += (double)sc[row[k].idx];
+        for (int k = 0; k < K; k++) {
+            ids[(size_t)t * K + k] = row[k].idx;
+            const double s = (double)sc[row[k].idx];
+            probs[(size_t)t * K + k] = (float)(renorm ? s / denom : s);
+        }
+    }
+    free(sc);
+    free(row);
+}
+
+/*
+ * Backward of oracle_route_sigmoid_topk's probabilities with respect to the
+ * logits, selection held fixed (the derivative of the forward's formulas; the
+ * pages name a router backward, [SPARSER] "The workload changes the
+ * bottleneck", without giving it). Row t: S = the distinct valid ids, g[k] =
+ * dprobs[t,k], G_e = sum of g[k] over k with ids[t,k] = e, s_e = sigmoid(l_e)
+ * in double.
+ *   without renorm:  dlogits[t,e] = G_e s_e (1 - s_e)                  (e in S)
+ *   with renorm:     Z = sum over S of s_e, p_e = s_e / Z,
+ *                    c = sum over valid k of g[k] p_{ids[t,k]},
+ *                    dlogits[t,e] = s_e (1 - s_e) (G_e - c) / Z         (e in S)
+ * and 0 for e outside S. The bias has no gradient path.
+ */
+void oracle_route_sigmoid_backward(const float *logits, const int32_t *ids, const float *dprobs,
+                                   int T, int E, int K, int renorm, double *dlogits)
+{
+    double *G = (double *)malloc(sizeof(double) * (size_t)E);
+    char *sel = (char *)malloc((size_t)E);
+    for (int t = 0; t < T; t++) {
+        const float *l = logits + (size_t)t * E;
+        for (int e = 0; e < E; e++) {
+            G[e] = 0.0;
+            sel[e] = 0;
+        }
+        for (int k = 0; k < K; k++) {
+            int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            sel[e] = 1;
+            G[e] += (double)dprobs[(size_t)t * K + k];
+        }
+        double Z = 0.0;
+        for (int e = 0; e < E; e++)
+            if (sel[e])
+                Z += 1.0 / (1.0 + exp(-(double)l[e]));
+        double c = 0.0;
+        for (int k = 0; k < K; k++) {
+            int e = ids[(size_t)t * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            c += (double)dprobs[(size_t)t * K + k] * (1.0 / (1.0 + exp(-(double)l[e]))) / Z;
+        }
+        for (int e = 0; e < E; e++) {
+            double d = 0.0;
+            if (sel[e]) {
+                const double s = 1.0 / (1.0 + exp(-(double)l[e]));
+                d = renorm ? s * (1.0 - s) * (G[e] - c) / Z : G[e] * s * (1.0 - s);
+            }
+            dlogits[(size_t)t * E + e] = d;
+        }
+    }
+    free(G);
+    free(sel);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Permute (dispatch into expert-contiguous order)                           */
 /* ------------------------------------------------------------------------ */
