@@ -187,7 +187,13 @@ def oracle_sample(wl, x_bits, logits_np, yperm_bits, gemm_rows: int, w_bits):
     import numpy as np
     import oracle as O
     t0 = time.perf_counter()
-    ids, probs = O.route_topk(logits_np, wl.K, wl.renorm)
+    if wl.score == "sigmoid":
+        from dropless_moe_expert_router_gb300 import workloads as W
+        eb = W.expert_bias(wl)
+        ids, probs = O.route_sigmoid_topk(logits_np, wl.K, bias=None if eb is None else eb.numpy(),
+                                          renorm=wl.renorm)
+    else:
+        ids, probs = O.route_topk(logits_np, wl.K, wl.renorm)
     t1 = time.perf_counter()
     op = O.permute(x_bits, ids, wl.E)
     t2 = time.perf_counter()
@@ -233,7 +239,8 @@ def run_ours(args, wl, rank, world, local_rank):
     logits = W.logits(wl, seed=rank).to(dev)
     layer = MoELayer(w1.to(dev), w3.to(dev), w2.to(dev), T=wl.T, K=wl.K, precision=wl.precision,
                      renorm=wl.renorm, id_dtype=torch.int16 if wl.id_bits == 16 else torch.int32,
-                     training=wl.backward)
+                     training=wl.backward, score=wl.score,
+                     expert_bias=None if W.expert_bias(wl) is None else W.expert_bias(wl).to(dev))
     del w1, w3, w2
     dy = W.dy(wl, seed=rank).to(dev) if wl.backward else None        # gradient of the layer output
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -387,7 +394,7 @@ def stage_report(wl, R, stage_ms, active=None):
     b_out = 1 if fp8 else 2
     q = (1 + 1 / 32) if fp8 else 2           # bytes per operand element (MXFP8: code + scale share)
     bytes_ = {
-        "route": T * E * 4 + T * K * (idb + 4),
+        "route": T * E * 4 + T * K * (idb + 4) + (E * 4 if wl.score == "sigmoid" else 0),
         "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
         "combine": R * H * 2 + T * K * 8 + T * H * 2,
         # read dy and y_perm, write dy_perm (MXFP8: and its codes and scales); route metadata and dprobs

@@ -29,6 +29,8 @@ SIGNATURES = {
     "moe_unpermute_combine_backward": (I, [P, P, P, P, I, I, I, P, P, P, P, P]),
     "moe_permute_backward": (I, [P, P, I, I, I, P, P]),
     "moe_route_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
+    "moe_route_sigmoid_topk": (I, [P, P, I, I, I, P, I, P, U, P]),
+    "moe_route_sigmoid_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
     "moe_packed_weights_bytes": (SZ, [I, I, I, I, I]),
     "moe_prepare_weights": (I, [P, P, P, I, I, I, I, P, P, P, P, P]),
     "moe_grouped_swiglu_gemm": (I, [P, P, P, P, P, P, I, P, I, I, I, I, P, P, P, P]),

@@ -81,6 +81,49 @@ def moe_route_topk(logits: torch.Tensor, K: int, *, id_dtype=torch.int32, renorm
     return ids, probs
 
 
+def moe_route_sigmoid_topk(logits: torch.Tensor, K: int, *, expert_bias: Optional[torch.Tensor] = None,
+                           id_dtype=torch.int32, renorm: bool = False, ids: Optional[torch.Tensor] = None,
+                           probs: Optional[torch.Tensor] = None, stream=None):
+    """logits [T, E] fp32 (+ expert_bias [E] fp32) -> (ids [T, K], probs [T, K] fp32): selection on
+    sigmoid(logit) + bias, probs the sigmoid scores (renormalised over the K selected with renorm)."""
+    _want(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    if expert_bias is not None:
+        _want(expert_bias, "expert_bias", torch.float32, 1)
+        if expert_bias.numel() != E:
+            raise ValueError("expert_bias must have E entries")
+    if ids is None:
+        ids = torch.empty((T, K), dtype=id_dtype, device=logits.device)
+    if probs is None:
+        probs = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    _want(ids, "ids", None, 2)
+    _want(probs, "probs", torch.float32, 2)
+    st = _lib.load().moe_route_sigmoid_topk(_ptr(logits), _ptr(expert_bias), T, E, K, _ptr(ids),
+                                            _id_code(ids.dtype), _ptr(probs), MOE_ROUTE_RENORM if renorm else 0,
+                                            _stream(stream))
+    _check("moe_route_sigmoid_topk", st)
+    return ids, probs
+
+
+def moe_route_sigmoid_topk_backward(logits: torch.Tensor, ids: torch.Tensor, dprobs: torch.Tensor, *,
+                                    renorm: bool = False, dlogits: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """logits [T, E], ids [T, K], dprobs [T, K] -> dlogits [T, E] fp32 of the sigmoid router."""
+    _want(logits, "logits", torch.float32, 2)
+    _want(ids, "ids", None, 2)
+    _want(dprobs, "dprobs", torch.float32, 2)
+    T, E = logits.shape
+    K = ids.shape[1]
+    if dlogits is None:
+        dlogits = torch.empty((T, E), dtype=torch.float32, device=logits.device)
+    _want(dlogits, "dlogits", torch.float32, 2)
+    st = _lib.load().moe_route_sigmoid_topk_backward(_ptr(logits), _ptr(ids), _id_code(ids.dtype), _ptr(dprobs),
+                                                     T, E, K, MOE_ROUTE_RENORM if renorm else 0, _ptr(dlogits),
+                                                     _stream(stream))
+    _check("moe_route_sigmoid_topk_backward", st)
+    return dlogits
+
+
 # -------------------------------------------------------------------- permute
 class Permuted(NamedTuple):
     x_perm: torch.Tensor          # [T*K, H] bf16, or uint8 E4M3 payloads when fused

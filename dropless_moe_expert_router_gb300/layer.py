@@ -20,11 +20,17 @@ from . import _lib, api
 class MoELayer:
     def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, *, T: int, K: int,
                  precision: str = "bf16", renorm: bool = False, id_dtype=torch.int32, training: bool = False,
-                 stream=None):
+                 score: str = "softmax", expert_bias: Optional[torch.Tensor] = None, stream=None):
         E, H, F = w1.shape
         self.E, self.H, self.F, self.T, self.K = E, H, F, T, K
         self.precision = precision
         self.renorm = renorm
+        if score not in ("softmax", "sigmoid"):
+            raise ValueError("score must be 'softmax' or 'sigmoid'")
+        if expert_bias is not None and score != "sigmoid":
+            raise ValueError("an expert bias steers only the sigmoid router's selection")
+        self.score = score
+        self.expert_bias = expert_bias      # [E] fp32 on the device; the caller may update it in place
         self.fp8 = precision == "mxfp8"
         self.training = training
         dev = w1.device
@@ -77,7 +83,17 @@ class MoELayer:
         return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E)
 
     def stage_route(self, logits, stream=None):
-        api.moe_route_topk(logits, self.K, renorm=self.renorm, ids=self.ids, probs=self.probs, stream=stream)
+        if self.score == "sigmoid":
+            api.moe_route_sigmoid_topk(logits, self.K, expert_bias=self.expert_bias, renorm=self.renorm, ids=self.ids,
+                                       probs=self.probs, stream=stream)
+        else:
+            api.moe_route_topk(logits, self.K, renorm=self.renorm, ids=self.ids, probs=self.probs, stream=stream)
+
+    @property
+    def expert_load(self) -> torch.Tensor:
+        """Valid routes per expert of the last forward ([E] int32 on the device): the statistics
+        a bias-balancing update of the sigmoid router reads (the permute's group sizes)."""
+        return self.perm.group_sizes
 
     def stage_permute(self, x, stream=None):
         api.moe_permute(x, self.ids, self.E, fuse_mxfp8=self.fp8, out=self.perm, workspace=self.workspace,
@@ -138,7 +154,11 @@ class MoELayer:
         api.moe_permute_backward(self.dx, self.perm.row_map, dx=self.dx_tokens, stream=stream)
 
     def stage_route_backward(self, logits: torch.Tensor, stream=None):
-        """dprobs -> dlogits [T, E] through the router's softmax (selection fixed)."""
+        """dprobs -> dlogits [T, E] through the router's score function (selection fixed)."""
+        if self.score == "sigmoid":
+            api.moe_route_sigmoid_topk_backward(logits, self.ids, self.dprobs, renorm=self.renorm,
+                                                dlogits=self.dlogits, stream=stream)
+            return
         api.moe_route_topk_backward(logits, self.ids, self.dprobs, renorm=self.renorm, dlogits=self.dlogits,
                                     stream=stream)
 

@@ -20,6 +20,9 @@ no trained model or dataset behind them):
                   about 2 % of the (t,k) routes are marked invalid (-1).
 * ``heavy``       T=32768, H=7168, E=32, K=8, F=2048, MXFP8, forward plus backward;
                   logits N(0,1) plus ln p_e with p_e ~ (e+1)^-1.5.
+* ``dsv3_sigmoid`` the ``dsv3`` layer and logits with the sigmoid-score router: selection
+                  on sigmoid(logit) plus a per-expert bias U(-0.05, 0.05) (a balancing
+                  correction), probs renormalised over the K selected scores.
 """
 from __future__ import annotations
 
@@ -30,6 +33,7 @@ import torch
 
 # tensor ids of the per-tensor generators
 _X, _LOGITS, _BIAS, _W1, _W3, _W2, _INVALID, _DY = 1, 2, 3, 4, 5, 6, 7, 8
+_EXPERT_BIAS = 12
 
 
 @dataclasses.dataclass(frozen=True)
@@ -49,6 +53,8 @@ class Workload:
     invalid_frac: float = 0.0
     backward: bool = False
     act_std: float = 0.02          # std of x, weights and dy
+    score: str = "softmax"         # router score function: "softmax" or "sigmoid"
+    expert_bias_scale: float = 0.0 # sigmoid router: selection bias ~ U(-scale, scale) per expert
 
     @property
     def R_cap(self) -> int:
@@ -65,6 +71,9 @@ WORKLOADS = {
                         invalid_frac=0.02),
     "heavy": Workload("heavy", T=32768, H=7168, E=32, K=8, F=2048, precision="mxfp8",
                       bias="zipf", bias_scale=1.0, zipf_s=1.5, backward=True),
+    "dsv3_sigmoid": Workload("dsv3_sigmoid", T=8192, H=7168, E=32, K=4, F=2048, precision="mxfp8",
+                             bias="zipf", bias_scale=2.0, zipf_s=1.1, score="sigmoid",
+                             expert_bias_scale=0.05, renorm=True),
     # reduced Mixtral-like shape for profiler captures (same tile shapes and K loop,
     # a quarter of F and half of T: about 1.5 GB on the device)
     "mixtral_prof": Workload("mixtral_prof", T=4096, H=4096, E=8, K=2, F=3584, bias="normal",
@@ -109,6 +118,14 @@ def logits(wl: Workload, seed: int = 0) -> torch.Tensor:
         lnp -= torch.logsumexp(lnp, 0)          # ln of the normalised Zipf pmf
         lg += (wl.bias_scale * lnp).to(torch.float32)
     return lg.contiguous()
+
+
+def expert_bias(wl: Workload, seed: int = 0):
+    """The sigmoid router's per-expert selection bias [E] fp32 ~ U(-s, s), or None."""
+    if wl.score != "sigmoid" or wl.expert_bias_scale <= 0:
+        return None
+    u = torch.rand((wl.E,), generator=_gen(seed, _EXPERT_BIAS), dtype=torch.float64)
+    return ((2 * u - 1) * wl.expert_bias_scale).to(torch.float32)
 
 
 def x(wl: Workload, seed: int = 0) -> torch.Tensor:

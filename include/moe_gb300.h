@@ -116,6 +116,44 @@ moe_status moe_route_topk_backward(const float *logits, const void *ids, moe_dty
                                    unsigned flags, float *dlogits, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Sigmoid-score routing with a per-expert selection bias ([SPARSER] "The
+ * workload changes the bottleneck": the router's score transformation and
+ * top-k selection; "Preserve a compact route": bias statistics carried with
+ * compact routes; the pages define neither, the DeepSeek-style reading is
+ * taken). For every row t and expert e:
+ *   s_e = 1 / (1 + exp(-logits[t,e]))      (fp32)
+ *   key_e = s_e + expert_bias[e]            (fp32; bias NULL means 0)
+ * ids[t, 0..K) = the K largest keys, in descending order, ties to the lower
+ * expert index; probs[t,k] = s at ids[t,k], or with MOE_ROUTE_RENORM that
+ * score divided by the sum of the K selected scores. The bias steers only the
+ * selection; its statistics (valid routes per expert) are the group_sizes that
+ * moe_permute writes. logits [T, E] fp32, expert_bias [E] fp32 (optional) in;
+ * ids [T, K] int16/int32 and probs [T, K] fp32 out. One warp per row, keys in
+ * registers. Requires 1 <= K <= E, E <= 1024 and K <= 64 (else
+ * MOE_ERR_UNSUPPORTED), no NaN logits or biases, finite biases. The score is
+ * CUDA's fp32 logistic (within 2 ulp of the correctly rounded value), so two
+ * keys within a few ulp of each other may be ordered either way.
+ * ------------------------------------------------------------------------ */
+moe_status moe_route_sigmoid_topk(const float *logits, const float *expert_bias, int T, int E,
+                                  int K, void *ids, moe_dtype id_dtype, float *probs,
+                                  unsigned flags, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of moe_route_sigmoid_topk's probs with respect to the logits, the
+ * selection held fixed. Row t: S = its distinct valid ids, G_e = sum of
+ * dprobs[t,k] over the k with ids[t,k] = e, s_e the score above, Z = sum over
+ * S of s_e, c = sum over S of G_e s_e / Z:
+ *   dlogits[t,e] = G_e s_e (1 - s_e)                  (e in S)
+ *   dlogits[t,e] = s_e (1 - s_e) (G_e - c) / Z        (e in S, MOE_ROUTE_RENORM)
+ * and 0 off S (the bias has no gradient path). logits [T, E], ids [T, K],
+ * dprobs [T, K] in; dlogits [T, E] fp32 out (every element written).
+ * Requires 1 <= K <= min(E, 128).
+ * ------------------------------------------------------------------------ */
+moe_status moe_route_sigmoid_topk_backward(const float *logits, const void *ids, moe_dtype id_dtype,
+                                           const float *dprobs, int T, int E, int K,
+                                           unsigned flags, float *dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Permute / dispatch ([TEJAX] "Dropless vs capacity-based MoE": every routed
  * token is processed, nothing dropped or padded; MoE-layer figure: tokens are
  * grouped per expert and combine restores token order; [SPARSER] "Remove work
