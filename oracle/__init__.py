@@ -85,6 +85,21 @@ def lib():
                                               P, i64, P]
             L.oracle_expert_of_row.restype = i32
             L.oracle_expert_of_row.argtypes = [P, i32, i64]
+            L.oracle_route_sigmoid_topk.restype = None
+            L.oracle_route_sigmoid_topk.argtypes = [P, P, i32, i32, i32, i32, P, P]
+            L.oracle_route_sigmoid_backward.restype = None
+            L.oracle_route_sigmoid_backward.argtypes = [P, P, P, i32, i32, i32, i32, P]
+            f32 = C.c_float
+            L.oracle_e2m1_decode.restype = dbl
+            L.oracle_e2m1_decode.argtypes = [C.c_uint8]
+            L.oracle_e2m1_encode.restype = C.c_uint8
+            L.oracle_e2m1_encode.argtypes = [dbl]
+            L.oracle_nvfp4_encode_scale.restype = f32
+            L.oracle_nvfp4_encode_scale.argtypes = [f32]
+            L.oracle_quant_rows_nvfp4.restype = None
+            L.oracle_quant_rows_nvfp4.argtypes = [P, i64, i64, f32, P, P]
+            L.oracle_nvfp4_decode.restype = None
+            L.oracle_nvfp4_decode.argtypes = [P, P, i64, i64, f32, P]
             _lib = L
     return _lib
 
@@ -136,6 +151,58 @@ def quant_rows(x_bf16):
     s = np.zeros((rows, cols // 32), np.uint8)
     lib().oracle_quant_rows_bf16(_p(x), rows, cols, _p(q), _p(s))
     return q, s
+
+
+def e2m1_decode(code: int) -> float:
+    return lib().oracle_e2m1_decode(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().oracle_e2m1_encode(float(v)))
+
+
+def nvfp4_encode_scale(amax: float) -> float:
+    """The fp32 tensor encode scale 448 * 6 / amax (1 for an all-zero tensor)."""
+    return float(lib().oracle_nvfp4_encode_scale(float(np.float32(amax))))
+
+
+def bf16_amax(x_bf16) -> float:
+    """max |x| of a bf16 matrix (exact)."""
+    return float(np.abs(bf16_to_f64(x_bf16)).max(initial=0.0))
+
+
+def quant_rows_nvfp4(x_bf16, S=None):
+    """Row-wise NVFP4 of a bf16 matrix -> (q [rows, cols/2] packed E2M1, s [rows, cols/16] E4M3,
+    S the fp32 encode scale used: that of x's own amax unless given)."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    if S is None:
+        S = nvfp4_encode_scale(bf16_amax(x))
+    q = np.zeros((rows, cols // 2), np.uint8)
+    s = np.zeros((rows, cols // 16), np.uint8)
+    lib().oracle_quant_rows_nvfp4(_p(x), rows, cols, float(S), _p(q), _p(s))
+    return q, s, float(S)
+
+
+def nvfp4_decode(q, s, S):
+    """Values (float64) of an NVFP4 matrix."""
+    qv = _c(q, np.uint8)
+    sv = _c(s, np.uint8)
+    rows, half = qv.shape
+    out = np.zeros((rows, 2 * half))
+    lib().oracle_nvfp4_decode(_p(qv), _p(sv), rows, 2 * half, float(S), _p(out))
+    return out
+
+
+def grouped_matmul(a, b, group_offsets):
+    """out[r] = a[r] @ b[e].T for the rows r of each group e (a [R, K], b [E, N, K], float64;
+    a library matmul per group). Rows past the last group stay 0."""
+    off = np.asarray(group_offsets, np.int64)
+    out = np.zeros((a.shape[0], b.shape[1]))
+    for e in range(off.size - 1):
+        if off[e + 1] > off[e]:
+            out[off[e]:off[e + 1]] = a[off[e]:off[e + 1]] @ b[e].T
+    return out
 
 
 def colwise_scale_rows(R_cap: int, E: int) -> int:

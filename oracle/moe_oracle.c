@@ -22,6 +22,8 @@
  *              "Transformer Engine building blocks for dropless MoE in JAX" (and
  *              its MoE-layer figure), "Optimization 1: Grouped GEMM",
  *              "Optimization 2: Expert parallelism to fuse Dispatch and Combine".
+ *   [WITTY]    "NVIDIA says its JAX stack makes dropless MoE training 10x faster"
+ *              (wittywires.com): section "What to watch".
  *   [CLARITY]  "NVIDIA's unoptimized DeepSeek-V3 baseline spends 84% of kernel
  *              time moving tokens between GPUs" (theclarity.today).
  * Where the pages leave a step open, the reading taken is stated beside the
@@ -31,6 +33,7 @@
  * (tests/test_oracle_*.py) against brute force, library routines, closed
  * forms or invariants.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -174,6 +177,105 @@ void oracle_quant_rows_bf16(const uint16_t *x, long rows, long cols, uint8_t *q,
             for (int i = 0; i < 32; i++)
                 buf[i] = oracle_bf16_to_double(x[r * cols + b * 32 + i]);
             s[r * (cols / 32) + b] = (uint8_t)quant_block(buf, 1, 32, q + r * cols + b * 32, 1);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * NVFP4 ([TEJAX] "Measured training impact with JAX + Transformer Engine" and
+ * [WITTY] "What to watch" name it as a planned addition; neither defines it).
+ * Reading taken: NVIDIA's published NVFP4 format --
+ *   elements  E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit):
+ *             magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ *   blocks    16 consecutive elements along a row share one E4M3 decode scale;
+ *   tensor    one fp32 encode scale S = 448 * 6 / amax(tensor) (S = 1 when the
+ *             tensor is all zero, at most FLT_MAX), so that the block scales
+ *             use E4M3's range;
+ *   decode    x = e2m1(q) * e4m3(sb) / S.
+ * The encoder's decisions are taken in fp32 (each operation one IEEE rounding):
+ *   sb = E4M3(rne, saturating)( (amax_block / 6) * S )
+ *   q  = E2M1(rne, saturating to 6, sign kept)( x * (S / e4m3(sb)) ), 0 when the
+ *        decoded block scale is 0.
+ * Packing: element 2i in the low nibble of byte i, element 2i+1 in the high one.
+ */
+double oracle_e2m1_decode(uint8_t code)
+{
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* Nearest E2M1 code (ties to the even mantissa bit), saturating to +-6, sign kept. */
+uint8_t oracle_e2m1_encode(double v)
+{
+    const uint8_t sign = signbit(v) ? 8 : 0;
+    const double a = fmin(fabs(v), 6.0);      /* saturating: beyond 6 is 6 */
+    int best = 0;
+    for (int c = 1; c < 8; c++) {
+        const double dc = fabs(oracle_e2m1_decode((uint8_t)c) - a);
+        const double db = fabs(oracle_e2m1_decode((uint8_t)best) - a);
+        if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1))
+            best = c;
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* The tensor's fp32 encode scale from its amax. */
+float oracle_nvfp4_encode_scale(float amax)
+{
+    if (!(amax > 0.0f))
+        return 1.0f;
+    volatile float s = 2688.0f / amax;           /* 448 * 6 */
+    return s > FLT_MAX ? FLT_MAX : s;
+}
+
+/*
+ * Row-wise NVFP4 of a bf16 matrix x[rows, cols] (cols % 16 == 0) with the
+ * tensor encode scale S (oracle_nvfp4_encode_scale of the amax the caller
+ * chooses, normally that of x): q[rows, cols/2] packed E2M1, s[rows, cols/16]
+ * E4M3 decode scales.
+ */
+void oracle_quant_rows_nvfp4(const uint16_t *x, long rows, long cols, float S, uint8_t *q, uint8_t *s)
+{
+    for (long r = 0; r < rows; r++)
+        for (long b = 0; b < cols / 16; b++) {
+            const uint16_t *blk = x + r * cols + b * 16;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; i++) {
+                const float v = (float)fabs(oracle_bf16_to_double(blk[i]));
+                if (v > amax)
+                    amax = v;
+            }
+            volatile float t = amax / 6.0f;
+            volatile float sbf = t * S;
+            const uint8_t sb = oracle_e4m3_encode((double)sbf);
+            const float ds = (float)oracle_e4m3_decode(sb);
+            s[r * (cols / 16) + b] = sb;
+            volatile float rs = ds > 0.0f ? S / ds : 0.0f;
+            for (int i = 0; i < 16; i++) {
+                volatile float v = (float)oracle_bf16_to_double(blk[i]) * rs;
+                const uint8_t c = ds > 0.0f ? oracle_e2m1_encode((double)v) : 0;
+                uint8_t *byte = q + r * (cols / 2) + b * 8 + i / 2;
+                if (i % 2 == 0)
+                    *byte = (uint8_t)((*byte & 0xF0) | c);
+                else
+                    *byte = (uint8_t)((*byte & 0x0F) | (c << 4));
+            }
+        }
+}
+
+/* Decode an NVFP4 matrix (packed q[rows, cols/2], scales s[rows, cols/16], encode scale S). */
+void oracle_nvfp4_decode(const uint8_t *q, const uint8_t *s, long rows, long cols, float S, double *out)
+{
+    for (long r = 0; r < rows; r++)
+        for (long c = 0; c < cols; c++) {
+            const uint8_t byte = q[r * (cols / 2) + c / 2];
+            const uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+            out[r * cols + c] =
+                oracle_e2m1_decode(code) * oracle_e4m3_decode(s[r * (cols / 16) + c / 16]) / (double)S;
         }
 }
 
