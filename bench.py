@@ -249,6 +249,10 @@ def run_ours(args, wl, rank, world, local_rank):
     stages = [("route", lambda: layer.stage_route(logits)), ("permute", lambda: layer.stage_permute(x)),
               ("gemm_up", layer.stage_gemm_up), ("gemm_down", layer.stage_gemm_down),
               ("combine", layer.stage_combine)]
+    if layer.nv4:
+        # NVFP4: the amax and quantisation passes before each GEMM are stages of their own
+        stages.insert(2, ("quant_x", layer.stage_quant_x))
+        stages.insert(4, ("quant_h", layer.stage_quant_h))
     if wl.backward:
         # the whole layer's backward, from dy [T, H]: combine, expert MLP (dgrad, dx, transposes,
         # wgrad), permute and router backward
@@ -391,8 +395,10 @@ def stage_report(wl, R, stage_ms, active=None):
     Ea = E if active is None else active
     idb = 2 if wl.id_bits == 16 else 4
     fp8 = wl.precision == "mxfp8"
+    nv4 = wl.precision == "nvfp4"
     b_out = 1 if fp8 else 2
-    q = (1 + 1 / 32) if fp8 else 2           # bytes per operand element (MXFP8: code + scale share)
+    # bytes per operand element: MXFP8 code + its share of a scale; NVFP4 half a byte + 1/16
+    q = (1 + 1 / 32) if fp8 else (0.5 + 1 / 16) if nv4 else 2
     bytes_ = {
         "route": T * E * 4 + T * K * (idb + 4) + (E * 4 if wl.score == "sigmoid" else 0),
         "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
@@ -403,7 +409,10 @@ def stage_report(wl, R, stage_ms, active=None):
         "route_bwd": T * E * 4 * 2 + T * K * (idb + 4),
         # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands
         "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
-        "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * q,
+        # NVFP4: amax pass + quantisation pass over x_perm (read twice, written as codes and scales)
+        "quant_x": R * H * 2 * 2 + R * H * q,
+        "quant_h": R * F * 2 + R * F * q,
+        "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * (2 if nv4 else q),
         "gemm_down": R * F * q + Ea * F * H * q + R * H * 2,
         # read dy, W2, (a | b); write dab (MXFP8: and its codes and scales)
         "dgrad_dh": R * H * q + Ea * F * H * q + R * 2 * F * 2 * 2 + (R * 2 * F * (1 + 1 / 32) if fp8 else 0),
@@ -485,7 +494,9 @@ def main():
     # dominant kernel: the GEMM stage with the largest time (one kernel launch per stage)
     dom = max((n for n in flops if n in r["stage_ms"] and n != "wgrad_gemm" and n != "dgrad_dx"),
               key=lambda n: r["stage_ms"][n])
-    fp8_ratio = 2.0 if wl.precision == "mxfp8" else 1.0
+    # dense peak of the GEMMs' operand type: the measured bf16 peak times the nominal ratio
+    # (MXFP8 2x, NVFP4 6x: 4.5 and 13.5 against 2.25 PFLOP/s dense)
+    fp8_ratio = {"mxfp8": 2.0, "nvfp4": 6.0}.get(wl.precision, 1.0)
     # The timed loop is well under a second and the SM clock stays at its maximum
     # (see "clocks"), the conditions of the burst measurement: report against the
     # burst peak, and the sustained figure beside it.
@@ -518,7 +529,8 @@ def main():
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic,
                      "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
-                                     f"{peak_kind} dense bf16 burst" + (" x2 (fp8)" if fp8_ratio > 1 else "")),
+                                     f"{peak_kind} dense bf16 burst" + ({2.0: " x2 (fp8)", 6.0: " x6 (fp4)"}
+                                                                        .get(fp8_ratio, ""))),
                      "frac_of_sustained": round(achieved / peak_sustained, 4)},
         "timing": "step = CUDA-graph replay of the whole step, CUDA events around each replay"
                   + (f" (first to last stage inside the replay: {r['inner_ms']:.4f} ms)" if r["inner_ms"] else "")

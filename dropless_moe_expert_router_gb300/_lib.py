@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmoe_gb300.so")
 _lock = threading.Lock()
 _lib = None
 
-P, I, U, SZ = C.c_void_p, C.c_int, C.c_uint, C.c_size_t
+P, I, U, SZ, LL = C.c_void_p, C.c_int, C.c_uint, C.c_size_t, C.c_longlong
 
 # name -> (restype, argtypes); names and argument order are those of include/moe_gb300.h
 SIGNATURES = {
@@ -30,6 +30,10 @@ SIGNATURES = {
     "moe_permute_backward": (I, [P, P, I, I, I, P, P]),
     "moe_route_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
     "moe_route_sigmoid_topk": (I, [P, P, I, I, I, P, I, P, U, P]),
+    "moe_amax_bf16": (I, [P, LL, I, P, P, P]),
+    "moe_quant_nvfp4": (I, [P, LL, I, P, P, P, P, P]),
+    "moe_grouped_gemm_up_nvfp4": (I, [P, P, P, P, P, P, P, I, I, I, I, P, P, P, P]),
+    "moe_grouped_gemm_down_nvfp4": (I, [P, P, P, P, P, P, P, I, I, I, I, P, P]),
     "moe_route_sigmoid_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
     "moe_packed_weights_bytes": (SZ, [I, I, I, I, I]),
     "moe_prepare_weights": (I, [P, P, P, I, I, I, I, P, P, P, P, P]),

@@ -416,6 +416,91 @@ def moe_grouped_gemm_up(x_perm: torch.Tensor, x_scales: Optional[torch.Tensor], 
     return h, h_scales
 
 
+# ---------------------------------------------------------------------- NVFP4
+def moe_amax_bf16(x: torch.Tensor, *, valid_rows: Optional[torch.Tensor] = None, amax: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """max |x| over the rows of a bf16 matrix (over the first *valid_rows rows when that device int
+    is given) -> amax [1] fp32 on the device."""
+    _want(x, "x", torch.bfloat16, None)
+    x2 = x.reshape(-1, x.shape[-1])
+    if amax is None:
+        amax = torch.empty((1,), dtype=torch.float32, device=x.device)
+    st = _lib.load().moe_amax_bf16(_ptr(x2), x2.shape[0], x2.shape[1], _ptr(valid_rows), _ptr(amax), _stream(stream))
+    _check("moe_amax_bf16", st)
+    return amax
+
+
+def moe_quant_nvfp4(x: torch.Tensor, amax: torch.Tensor, *, valid_rows: Optional[torch.Tensor] = None,
+                    q: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None, stream=None):
+    """Row-wise NVFP4 of a bf16 matrix [..., C] with the tensor encode scale of the device amax ->
+    (q [..., C/2] uint8 packed E2M1, scales [..., C/16] uint8 E4M3)."""
+    _want(x, "x", torch.bfloat16, None)
+    C_ = x.shape[-1]
+    if q is None:
+        q = torch.empty(x.shape[:-1] + (C_ // 2,), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (C_ // 16,), dtype=torch.uint8, device=x.device)
+    rows = x.numel() // C_
+    st = _lib.load().moe_quant_nvfp4(_ptr(x), rows, C_, _ptr(valid_rows), _ptr(amax), _ptr(q), _ptr(scales),
+                                     _stream(stream))
+    _check("moe_quant_nvfp4", st)
+    return q, scales
+
+
+class Nvfp4Weights(NamedTuple):
+    E: int
+    H: int
+    F: int
+    w13: torch.Tensor          # [E, 2F, H/2] packed E2M1 (the layout of PackedWeights.w13)
+    w13_scales: torch.Tensor   # [E, 2F, H/16] E4M3
+    w13_amax: torch.Tensor     # [1] fp32
+    w2: torch.Tensor           # [E, H, F/2]
+    w2_scales: torch.Tensor    # [E, H, F/16]
+    w2_amax: torch.Tensor      # [1] fp32
+
+
+def moe_prepare_weights_nvfp4(w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, stream=None) -> Nvfp4Weights:
+    """One-time: pack the logical weights (bf16) into the grouped GEMMs' layouts and quantise each
+    stacked tensor row-wise to NVFP4 along its contraction dimension, with its own amax."""
+    pw = moe_prepare_weights(w1, w3, w2, "bf16", stream=stream)
+    a13 = moe_amax_bf16(pw.w13, stream=stream)
+    q13, s13 = moe_quant_nvfp4(pw.w13, a13, stream=stream)
+    a2 = moe_amax_bf16(pw.w2, stream=stream)
+    q2, s2 = moe_quant_nvfp4(pw.w2, a2, stream=stream)
+    return Nvfp4Weights(pw.E, pw.H, pw.F, q13, s13, a13, q2, s2, a2)
+
+
+def moe_grouped_gemm_up_nvfp4(x_q: torch.Tensor, x_scales: torch.Tensor, x_amax: torch.Tensor, w: Nvfp4Weights,
+                              group_offsets: torch.Tensor, *, h: Optional[torch.Tensor] = None,
+                              h_amax: Optional[torch.Tensor] = None, ab: Optional[torch.Tensor] = None,
+                              stream=None):
+    """NVFP4 x [R_cap, H/2] -> (h [R_cap, F] bf16 = silu(x W1) * (x W3), h_amax [1] fp32)."""
+    R_cap = x_q.shape[0]
+    if h is None:
+        h = torch.empty((R_cap, w.F), dtype=torch.bfloat16, device=x_q.device)
+    if h_amax is None:
+        h_amax = torch.empty((1,), dtype=torch.float32, device=x_q.device)
+    st = _lib.load().moe_grouped_gemm_up_nvfp4(
+        _ptr(x_q), _ptr(x_scales), _ptr(x_amax), _ptr(w.w13), _ptr(w.w13_scales), _ptr(w.w13_amax),
+        _ptr(group_offsets), w.E, w.H, w.F, R_cap, _ptr(h), _ptr(h_amax), _ptr(ab), _stream(stream))
+    _check("moe_grouped_gemm_up_nvfp4", st)
+    return h, h_amax
+
+
+def moe_grouped_gemm_down_nvfp4(h_q: torch.Tensor, h_scales: torch.Tensor, h_amax: torch.Tensor, w: Nvfp4Weights,
+                                group_offsets: torch.Tensor, *, y_perm: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """NVFP4 h [R_cap, F/2] -> y_perm [R_cap, H] bf16 = h W2."""
+    R_cap = h_q.shape[0]
+    if y_perm is None:
+        y_perm = torch.empty((R_cap, w.H), dtype=torch.bfloat16, device=h_q.device)
+    st = _lib.load().moe_grouped_gemm_down_nvfp4(
+        _ptr(h_q), _ptr(h_scales), _ptr(h_amax), _ptr(w.w2), _ptr(w.w2_scales), _ptr(w.w2_amax),
+        _ptr(group_offsets), w.E, w.H, w.F, R_cap, _ptr(y_perm), _stream(stream))
+    _check("moe_grouped_gemm_down_nvfp4", st)
+    return y_perm
+
+
 class BwdWeights(NamedTuple):
     precision: str
     E: int

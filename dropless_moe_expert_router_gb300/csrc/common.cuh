@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "moe_gb300.h"
@@ -55,6 +56,51 @@ __device__ __forceinline__ float e8m0_inv_scale(int byte) {
 // Two floats -> two E4M3 codes (round to nearest even, saturate to +-448), packed lo|hi<<8.
 __device__ __forceinline__ unsigned short f32x2_to_e4m3x2(float lo, float hi) {
     return (unsigned short)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// ---------------------------------------------------------------- NVFP4 block rule
+// Tensor encode scale S = 448 * 6 / amax (fp32, one rounding; 1 for amax == 0; at most FLT_MAX).
+__device__ __forceinline__ float nvfp4_encode_scale(float amax) {
+    if (!(amax > 0.0f)) return 1.0f;
+    const float s = __fdiv_rn(2688.0f, amax);
+    return s > 3.40282347e38f ? 3.40282347e38f : s;
+}
+
+// E2M1 code of v: round to nearest on the grid 0, .5, 1, 1.5, 2, 3, 4, 6 (ties to the even
+// code), saturating to 6, sign bit kept. The magnitude code counts the grid midpoints below
+// |v|; each midpoint is taken with > or >= so that an exact tie lands on the even code.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    const float a = fabsf(v);
+    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Value of an E4M3 byte (exact).
+__device__ __forceinline__ float e4m3_value(uint32_t byte) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Encode one NVFP4 block of 16 values with tensor encode scale S: returns the 16 packed codes
+// (element i in bits 4i..4i+3) and, in *sbyte, the E4M3 decode scale E4M3((amax / 6) * S).
+__device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, uint32_t* sbyte) {
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i++) am = fmaxf(am, fabsf(f[i]));
+    const float sbf = __fmul_rn(__fdiv_rn(am, 6.0f), S);
+    const uint32_t sb = (uint32_t)f32x2_to_e4m3x2(sbf, 0.0f) & 0xffu;
+    const float ds = e4m3_value(sb);
+    uint2 out = make_uint2(0u, 0u);
+    if (ds > 0.0f) {
+        const float rs = __fdiv_rn(S, ds);
+#pragma unroll
+        for (int i = 0; i < 8; i++) out.x |= e2m1_code(__fmul_rn(f[i], rs)) << (4 * i);
+#pragma unroll
+        for (int i = 0; i < 8; i++) out.y |= e2m1_code(__fmul_rn(f[8 + i], rs)) << (4 * i);
+    }
+    *sbyte = sb;
+    return out;
 }
 
 // 8 bf16 (one uint4) -> floats.

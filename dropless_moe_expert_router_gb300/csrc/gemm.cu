@@ -74,9 +74,10 @@ enum { MODE_UP = 0, MODE_DOWN = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
 // PAIR: a tile is computed by a cluster of two CTAs with tcgen05 cta_group::2 --
 // M = 256 rows (128 per CTA), and each CTA loads only its half of the B tile,
 // so a stage is 32 KB and the ring is 6 stages deep.
-template <bool FP8, bool PAIR = false>
+template <bool FP8, bool PAIR = false, bool NV4 = false>
 struct Cfg {
     static_assert(!(FP8 && PAIR), "MXFP8 uses single-CTA tiles");
+    static_assert(!NV4 || FP8, "NVFP4 runs on the block-scaled 8-bit machinery");
     static constexpr int BK = FP8 ? 128 : 64;       // elements per k-block (128 bytes per row)
     static constexpr int UMMA_K = FP8 ? 32 : 16;    // elements per MMA instruction
     static constexpr int KSTEPS = BK / UMMA_K;      // MMAs per k-block (4)
@@ -96,7 +97,12 @@ struct Cfg {
     static constexpr int SF_CHUNK = 3 * 512;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES + SF_SLOTS * SF_SLOT_BYTES;
     static constexpr int ACC_STAGES = FP8 ? 1 : 2;
-    static constexpr int SF_COLS = 12;              // TMEM columns of one stage's scales (4 A + 8 B)
+    // TMEM columns of one stage's scales: MXFP8 4 A + 8 B for the whole k-block (the four MMAs pick
+    // a byte each); NVFP4 the same 12 for each of the four MMAs (each takes a whole word: four
+    // E4M3 scales of 16 elements)
+    static constexpr int SF_COLS = NV4 ? 48 : 12;
+    // k-blocks one 16-byte scale box per row covers: MXFP8 four (4 x 128 / 32), NVFP4 one (256 / 16)
+    static constexpr int SF_GROUP = NV4 ? 1 : 4;
     static constexpr int THREADS = FP8 ? NUM_THREADS : NUM_THREADS - 32;  // the scale warp exists for MXFP8 only
 };
 
@@ -120,6 +126,9 @@ struct GemmArgs {
     int m_tiles;                 // WGRAD: M / BM
     void* out2;                  // WGRAD split: second half [E][M][N/2]
     int st32;                    // every output row segment is 32-byte aligned: 32-byte stores
+    const float* a_amax;         // NVFP4: device amax of A's tensor (its encode scale 448 * 6 / amax)
+    const float* b_amax;         // NVFP4: device amax of B's tensor
+    float* out_amax;             // NVFP4 UP: device amax of the bf16 h written (zeroed by the caller)
 };
 
 template <bool FP8, bool PAIR = false>
@@ -260,12 +269,12 @@ __device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
     for (int i = 0; i < 4; i++) bf16x8_to_f32(s[i], v + 8 * i);
 }
 
-template <int MODE, bool FP8, bool PAIR>
+template <int MODE, bool FP8, bool PAIR, bool NV4 = false>
 __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs p) {
-    using C = Cfg<FP8, PAIR>;
+    using C = Cfg<FP8, PAIR, NV4>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -430,17 +439,37 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 const int gk = k0b + kb;                 // k-block index along the contraction
                 if (!ptx::wait_parity(&full[stage], phase, s_abort)) { ok = false; break; }
                 // MXFP8: the group's scales, rearranged by the scale warp
-                if (FP8 && (kb == 0 || (gk & 3) == 0) && !ptx::wait_parity(&sf_ready[sslot], sphase, s_abort)) {
+                if (FP8 && (NV4 || kb == 0 || (gk & 3) == 0) &&
+                    !ptx::wait_parity(&sf_ready[sslot], sphase, s_abort)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 uint8_t* sa = ring + (size_t)stage * C::STAGE_BYTES;
                 uint8_t* sb = sa + C::A_BYTES;
-                const bool group_end = kb == nkb - 1 || (gk & 3) == 3;
+                const bool group_end = NV4 || kb == nkb - 1 || (gk & 3) == 3;
                 if (lane == 0) {
                     const uint32_t a0 = ptx::smem_addr(sa), b0 = ptx::smem_addr(sb);
-                    if constexpr (FP8) {
+                    if constexpr (NV4) {
+                        // NVFP4: the slot holds this k-block's scales; chunk k (one word per row)
+                        // feeds MMA k, which covers 64 elements (32 bytes) of the k-block
+                        const uint32_t sf_t = tmem + (uint32_t)(BN + stage * C::SF_COLS);
+                        const uint32_t sfa_s = ptx::smem_addr(sfring + (size_t)sslot * C::SF_SLOT_BYTES);
+#pragma unroll
+                        for (int k = 0; k < C::KSTEPS; k++) {
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 12 * k, ptx::sdesc_plain(sfa_s + k * C::SF_CHUNK));
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 12 * k + 4,
+                                                      ptx::sdesc_plain(sfa_s + k * C::SF_CHUNK + 512));
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 12 * k + 8,
+                                                      ptx::sdesc_plain(sfa_s + k * C::SF_CHUNK + 1024));
+                        }
+#pragma unroll
+                        for (int k = 0; k < C::KSTEPS; k++)
+                            ptx::mma_nvf4(d_tmem, ptx::sdesc_k_sw128(a0 + k * 32), ptx::sdesc_k_sw128(b0 + k * 32),
+                                          ptx::idesc_nvf4(BM, BN), sf_t + 12 * k, sf_t + 12 * k + 4, (kb | k) != 0);
+                        ptx::tc_commit(&empty[stage]);
+                        ptx::tc_commit(&sf_empty[sslot]);
+                    } else if constexpr (FP8) {
                         const uint32_t sf_t = tmem + (uint32_t)(BN + stage * C::SF_COLS);
                         const uint32_t sfa_s =
                             ptx::smem_addr(sfring + (size_t)sslot * C::SF_SLOT_BYTES + (gk & 3) * C::SF_CHUNK);
@@ -515,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 return c;
             };
             auto next_group = [&](Cursor c) {
-                c.kb += 4 - ((c.ti.k0 / C::BK + c.kb) & 3);
+                c.kb += NV4 ? 1 : 4 - ((c.ti.k0 / C::BK + c.kb) & 3);
                 return c.kb < c.ti.nkb ? c : first_from(c.tile + tile_step);
             };
             Cursor ld = first_from(tile0), pr = ld;
@@ -533,7 +562,9 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                     __all_sync(FULL, ptx::mbar_test_wait(&sf_empty[ld_slot], ld_phase ^ 1u))) {
                     if (lane == 0) {
                         uint8_t* sf = sfring + (size_t)ld_slot * C::SF_SLOT_BYTES;
-                        const int kx = ((ld.ti.k0 + ld.kb * C::BK) / 32) & ~15;
+                        // scale byte of the group's first element: MXFP8 element / 32 (groups of four
+                        // k-blocks, 16-byte aligned); NVFP4 byte index (2 elements) / 8 = element / 16
+                        const int kx = NV4 ? (ld.ti.k0 + ld.kb * C::BK) / 8 : ((ld.ti.k0 + ld.kb * C::BK) / 32) & ~15;
                         ptx::mbar_arrive_expect_tx(&sf_full[ld_slot], C::SF_SLOT_BYTES);
                         ptx::tma_load_2d(sf, &tmSA, &sf_full[ld_slot], kx, ld.ti.a_row);
                         ptx::tma_load_2d(sf + BM * 16, &tmSB, &sf_full[ld_slot], kx, ld.ti.b_row);
@@ -599,6 +630,12 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
         const int rit = q * 32 + lane;           // row within this CTA's tile
         int acc = 0;
         uint32_t acc_phase = 0;
+        // NVFP4: the accumulator sums decoded products without the two tensors' encode scales;
+        // alpha = 1 / (S_A S_B) restores them. h_amax: max |h| of the bf16 h this thread wrote.
+        float alpha = 1.0f, h_amax = 0.0f;
+        if constexpr (NV4)
+            alpha = __fdiv_rn(1.0f, nvfp4_encode_scale(__ldg(p.a_amax))) *
+                    __fdiv_rn(1.0f, nvfp4_encode_scale(__ldg(p.b_amax)));
         for (int tile = tile0; tile < total_tiles; tile += tile_step) {
             const TileInfo ti = decode<MODE, FP8, PAIR>(tile, s_mtp, s_goff, p, rank);
             if (!ptx::wait_parity(&tfull[acc], acc_phase, s_abort)) break;
@@ -631,6 +668,11 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 else ptx::mbar_arrive(&tempty[acc]);
             }
             if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+            if constexpr (NV4) {
+                float* fs = reinterpret_cast<float*>(v);
+#pragma unroll
+                for (int i = 0; i < 128; i++) fs[i] *= alpha;
+            }
             const float* f = reinterpret_cast<const float*>(v);
 
             if constexpr (MODE == MODE_UP) {
@@ -647,7 +689,7 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                     float* hv = reinterpret_cast<float*>(v) + 32 * c;
 #pragma unroll
                     for (int i = 0; i < 32; i++) hv[i] = silu_f(hv[i]) * f[64 + 32 * c + i];
-                    if constexpr (FP8) {
+                    if constexpr (FP8 && !NV4) {
                         uint32_t w[8];
                         const int sbyte = quant32_in_thread(hv, w);
                         if (valid) {
@@ -656,7 +698,15 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                             if (p.h_bf16) store_bf16x32(p.h_bf16 + r * p.ldo + hcol, hv, p.st32);
                         }
                     } else {
-                        if (valid) store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + hcol, hv, p.st32);
+                        if (valid) {
+                            store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + r * p.ldo + hcol, hv, p.st32);
+                            if constexpr (NV4) {
+                                // amax of the bf16 values stored (the next quantisation's tensor scale)
+#pragma unroll
+                                for (int i = 0; i < 32; i++)
+                                    h_amax = fmaxf(h_amax, fabsf(__bfloat162float(__float2bfloat16_rn(hv[i]))));
+                            }
+                        }
                     }
                 }
             } else if constexpr (MODE == MODE_DGRAD) {
@@ -741,6 +791,12 @@ __global__ void __launch_bounds__(Cfg<FP8, PAIR>::THREADS, 1)
                 }
             }
         }
+        if constexpr (NV4 && MODE == MODE_UP) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) h_amax = fmaxf(h_amax, __shfl_xor_sync(FULL, h_amax, o));
+            if (lane == 0 && h_amax > 0.0f)
+                atomicMax(reinterpret_cast<unsigned int*>(p.out_amax), __float_as_uint(h_amax));
+        }
     }
 
     ptx::tc_fence_before();
@@ -807,10 +863,10 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64
 }
 
 // A: [a_rows][a_inner], B: [b_rows][a_inner], both K-major.
-template <int MODE, bool FP8, bool PAIR>
+template <int MODE, bool FP8, bool PAIR, bool NV4 = false>
 moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b_rows, uint64_t inner,
                        GemmArgs a, cudaStream_t s) {
-    using C = Cfg<FP8, PAIR>;
+    using C = Cfg<FP8, PAIR, NV4>;
     CUtensorMap tmA, tmB, tmSA, tmSB;
     if (!make_operand_map(&tmA, A, FP8, inner, a_rows, BM)) return MOE_ERR_CUDA;
     if (!make_operand_map(&tmB, B, FP8, inner, b_rows, C::B_ROWS)) return MOE_ERR_CUDA;
@@ -830,7 +886,7 @@ moe_status launch_gemm(const void* A, uint64_t a_rows, const void* B, uint64_t b
         a.st32 = pitch_ok && al32(a.out) && al32(a.out2) && al32(a.ab) && al32(a.h_bf16) ? 1 : 0;
     }
     const size_t smem = smem_bytes_for<FP8, PAIR>(a.E);
-    auto kern = grouped_gemm_kernel<MODE, FP8, PAIR>;
+    auto kern = grouped_gemm_kernel<MODE, FP8, PAIR, NV4>;
     // raise the kernel's dynamic shared-memory limit once per process and size (not a stream operation,
     // but keeping it out of repeated calls keeps captured launches free of other API calls)
     static int configured_smem = 0;
@@ -952,6 +1008,83 @@ static moe_status grouped_down(const void* A, const uint8_t* a_scales, const voi
     a.sf_row_bytes = Kc / 32;
     return launch_mode<MODE_DOWN>(fp8, A, (uint64_t)R_cap, B, (uint64_t)E * H, (uint64_t)Kc, a,
                                   moe_host::as_stream(stream));
+}
+
+// NVFP4 operands are passed to the kernel as bytes (two elements each): a k-block is 128
+// bytes = 256 elements, the contraction length and the tensor maps' inner extent are in bytes,
+// and each 16-byte scale box per row covers one k-block (16 scales of 16 elements).
+static moe_status check_nvfp4(const int32_t* group_offsets, int E, int H, int F, int R_cap) {
+    using namespace moe;
+    if (E < 1 || H < 256 || F < 256 || R_cap < 0 || !group_offsets) return MOE_ERR_INVALID_ARG;
+    if ((H % 256) || (F % 256)) return MOE_ERR_UNSUPPORTED;
+    if (smem_bytes_for<true>(E) > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    if ((long long)E * 2 * F > 0x7fffffffLL || (long long)E * H > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_grouped_gemm_up_nvfp4(const void* x_q, const uint8_t* x_scales, const float* x_amax,
+                                                const void* w13_q, const uint8_t* w13_scales, const float* w13_amax,
+                                                const int32_t* group_offsets, int E, int H, int F, int R_cap,
+                                                void* h, float* h_amax, void* ab_save, moe_stream_t stream) {
+    using namespace moe;
+    moe_status st = check_nvfp4(group_offsets, E, H, F, R_cap);
+    if (st != MOE_OK) return st;
+    if (!x_q || !x_scales || !x_amax || !w13_q || !w13_scales || !w13_amax || !h || !h_amax)
+        return MOE_ERR_INVALID_ARG;
+    if (!al(x_q, 128) || !al(w13_q, 128) || !al(x_scales, 16) || !al(w13_scales, 16) || !al(h, 16) ||
+        !al(ab_save, 16) || !al(x_amax, 4) || !al(w13_amax, 4) || !al(h_amax, 4))
+        return MOE_ERR_ALIGNMENT;
+    cudaStream_t s = moe_host::as_stream(stream);
+    if (cudaMemsetAsync(h_amax, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (R_cap == 0) return MOE_OK;
+    GemmArgs a{};
+    a.goff = group_offsets;
+    a.E = E;
+    a.Kdim = H / 2;
+    a.N = 2 * F;
+    a.n_tiles = 2 * F / BN;
+    a.R_cap = R_cap;
+    a.out = h;
+    a.ldo = F;
+    a.a_scales = x_scales;
+    a.b_scales = w13_scales;
+    a.sf_row_bytes = H / 16;
+    a.ab = static_cast<__nv_bfloat16*>(ab_save);
+    a.a_amax = x_amax;
+    a.b_amax = w13_amax;
+    a.out_amax = h_amax;
+    return launch_gemm<MODE_UP, true, false, true>(x_q, (uint64_t)R_cap, w13_q, (uint64_t)E * 2 * F,
+                                                    (uint64_t)(H / 2), a, s);
+}
+
+extern "C" moe_status moe_grouped_gemm_down_nvfp4(const void* h_q, const uint8_t* h_scales, const float* h_amax,
+                                                  const void* w2_q, const uint8_t* w2_scales, const float* w2_amax,
+                                                  const int32_t* group_offsets, int E, int H, int F, int R_cap,
+                                                  void* y_perm, moe_stream_t stream) {
+    using namespace moe;
+    moe_status st = check_nvfp4(group_offsets, E, H, F, R_cap);
+    if (st != MOE_OK) return st;
+    if (R_cap == 0) return MOE_OK;
+    if (!h_q || !h_scales || !h_amax || !w2_q || !w2_scales || !w2_amax || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!al(h_q, 128) || !al(w2_q, 128) || !al(h_scales, 16) || !al(w2_scales, 16) || !al(y_perm, 16) ||
+        !al(h_amax, 4) || !al(w2_amax, 4))
+        return MOE_ERR_ALIGNMENT;
+    GemmArgs a{};
+    a.goff = group_offsets;
+    a.E = E;
+    a.Kdim = F / 2;
+    a.N = H;
+    a.n_tiles = H / BN;
+    a.R_cap = R_cap;
+    a.out = y_perm;
+    a.ldo = H;
+    a.a_scales = h_scales;
+    a.b_scales = w2_scales;
+    a.sf_row_bytes = F / 16;
+    a.a_amax = h_amax;
+    a.b_amax = w2_amax;
+    return launch_gemm<MODE_DOWN, true, false, true>(h_q, (uint64_t)R_cap, w2_q, (uint64_t)E * H, (uint64_t)(F / 2),
+                                                      a, moe_host::as_stream(stream));
 }
 
 extern "C" moe_status moe_grouped_gemm_down(const void* h, const uint8_t* h_scales, const void* w2_packed,

@@ -163,6 +163,19 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D (+)= A x B for packed E2M1 operands (two elements per byte, K = 64 per instruction) with one
+// UE4M3 scale per 16 elements: each scale TMEM word holds the four scales of the instruction's
+// 64 elements of a row.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred P;\n setp.ne.b32 P, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], P;\n}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Copy 32 rows x 128 bits from shared memory into TMEM, replicated to the four 32-lane quarters.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
@@ -226,6 +239,15 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id_a, int
            | ((uint32_t)(sf_id_a & 3) << 29);  // A scale factor id
 }
 
+// Instruction descriptor of kind::mxf4nvf4 (A, B: E2M1, both K-major; scales UE4M3; the
+// scale-factor ids are 0, as each instruction uses all four bytes of its scale words).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+    return (1u << 7)                       // A format: E2M1
+           | (1u << 10)                    // B format: E2M1
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | (0u << 23)                    // scale format: UE4M3
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
 
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 __device__ __forceinline__ uint32_t cluster_ctarank() {

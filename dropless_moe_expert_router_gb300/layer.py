@@ -31,10 +31,18 @@ class MoELayer:
             raise ValueError("an expert bias steers only the sigmoid router's selection")
         self.score = score
         self.expert_bias = expert_bias      # [E] fp32 on the device; the caller may update it in place
+        if precision not in ("bf16", "mxfp8", "nvfp4"):
+            raise ValueError("precision must be 'bf16', 'mxfp8' or 'nvfp4'")
         self.fp8 = precision == "mxfp8"
+        self.nv4 = precision == "nvfp4"
+        if self.nv4 and training:
+            raise ValueError("the NVFP4 layer is forward-only")
         self.training = training
         dev = w1.device
-        self.weights = api.moe_prepare_weights(w1, w3, w2, precision, stream=stream)
+        if self.nv4:
+            self.weights = api.moe_prepare_weights_nvfp4(w1, w3, w2, stream=stream)
+        else:
+            self.weights = api.moe_prepare_weights(w1, w3, w2, precision, stream=stream)
         self.bwd_weights = api.moe_prepare_weights_bwd(w1, w3, w2, precision, stream=stream) if training else None
         R_cap = T * K
         self.R_cap = R_cap
@@ -44,6 +52,15 @@ class MoELayer:
         self.workspace = torch.empty(api.moe_permute_workspace_size(T, K, E), dtype=torch.uint8, device=dev)
         self.h = torch.empty((R_cap, F), dtype=torch.uint8 if self.fp8 else torch.bfloat16, device=dev)
         self.h_scales = torch.empty((R_cap, F // 32), dtype=torch.uint8, device=dev) if self.fp8 else None
+        if self.nv4:
+            # NVFP4 operands of the two GEMMs: x_perm and h quantised with their tensors' amax
+            u8, f32 = torch.uint8, torch.float32
+            self.x_q = torch.empty((R_cap, H // 2), dtype=u8, device=dev)
+            self.x_s = torch.empty((R_cap, H // 16), dtype=u8, device=dev)
+            self.x_amax = torch.empty((1,), dtype=f32, device=dev)
+            self.h_amax = torch.empty((1,), dtype=f32, device=dev)
+            self.h_q = torch.empty((R_cap, F // 2), dtype=u8, device=dev)
+            self.h_s = torch.empty((R_cap, F // 16), dtype=u8, device=dev)
         self.y_perm = torch.empty((R_cap, H), dtype=torch.bfloat16, device=dev)
         self.y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -80,7 +97,8 @@ class MoELayer:
     # (rank, [scan,] scatter), GEMM 2, combine 1
     @property
     def launches_per_forward(self) -> int:
-        return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E)
+        # (NVFP4 adds x_perm's amax and the quantisations of x_perm and h)
+        return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E) + (3 if self.nv4 else 0)
 
     def stage_route(self, logits, stream=None):
         if self.score == "sigmoid":
@@ -99,8 +117,29 @@ class MoELayer:
         api.moe_permute(x, self.ids, self.E, fuse_mxfp8=self.fp8, out=self.perm, workspace=self.workspace,
                         stream=stream)
 
+    def stage_quant_x(self, stream=None):
+        """NVFP4 only: x_perm's amax over the routed rows and its row-wise quantisation."""
+        if not self.nv4:
+            return
+        valid = self.perm.group_offsets[self.E:]
+        api.moe_amax_bf16(self.perm.x_perm, valid_rows=valid, amax=self.x_amax, stream=stream)
+        api.moe_quant_nvfp4(self.perm.x_perm, self.x_amax, valid_rows=valid, q=self.x_q, scales=self.x_s,
+                            stream=stream)
+
+    def stage_quant_h(self, stream=None):
+        """NVFP4 only: h quantised with the amax the up projection gathered."""
+        if not self.nv4:
+            return
+        api.moe_quant_nvfp4(self.h, self.h_amax, valid_rows=self.perm.group_offsets[self.E:], q=self.h_q,
+                            scales=self.h_s, stream=stream)
+
     def stage_gemm_up(self, stream=None):
         w = self.weights
+        if self.nv4:
+            # h (bf16) and its amax from the NVFP4 operands
+            api.moe_grouped_gemm_up_nvfp4(self.x_q, self.x_s, self.x_amax, w, self.perm.group_offsets, h=self.h,
+                                          h_amax=self.h_amax, stream=stream)
+            return
         ab = self.ab if self.training else None
         hb = self.h_bf16 if self.training else None
         st = self._lib.moe_grouped_gemm_up(
@@ -112,6 +151,10 @@ class MoELayer:
 
     def stage_gemm_down(self, stream=None):
         w = self.weights
+        if self.nv4:
+            api.moe_grouped_gemm_down_nvfp4(self.h_q, self.h_s, self.h_amax, w, self.perm.group_offsets,
+                                            y_perm=self.y_perm, stream=stream)
+            return
         st = self._lib.moe_grouped_gemm_down(
             api._ptr(self.h), api._ptr(self.h_scales), api._ptr(w.w2), api._ptr(w.w2_scales),
             api._dt_code(w.precision), api._ptr(self.perm.group_offsets), w.E, w.H, w.F, self.R_cap,
@@ -125,7 +168,9 @@ class MoELayer:
         """x [T, H] bf16 and logits [T, E] fp32 on the device -> y [T, H] bf16 (a layer-owned buffer)."""
         self.stage_route(logits, stream)
         self.stage_permute(x, stream)
+        self.stage_quant_x(stream)
         self.stage_gemm_up(stream)
+        self.stage_quant_h(stream)
         self.stage_gemm_down(stream)
         self.stage_combine(stream)
         return self.y

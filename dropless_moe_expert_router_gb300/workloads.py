@@ -20,6 +20,7 @@ no trained model or dataset behind them):
                   about 2 % of the (t,k) routes are marked invalid (-1).
 * ``heavy``       T=32768, H=7168, E=32, K=8, F=2048, MXFP8, forward plus backward;
                   logits N(0,1) plus ln p_e with p_e ~ (e+1)^-1.5.
+* ``dsv3_nvfp4``  the ``dsv3`` layer and routing with NVFP4 GEMM operands (forward).
 * ``dsv3_sigmoid`` the ``dsv3`` layer and logits with the sigmoid-score router: selection
                   on sigmoid(logit) plus a per-expert bias U(-0.05, 0.05) (a balancing
                   correction), probs renormalised over the K selected scores.
@@ -44,7 +45,7 @@ class Workload:
     E: int
     K: int
     F: int
-    precision: str = "bf16"        # "bf16" or "mxfp8" (operands of the expert GEMMs)
+    precision: str = "bf16"        # "bf16", "mxfp8" or "nvfp4" (operands of the expert GEMMs)
     bias: str = "none"             # "none", "normal", "zipf"
     bias_scale: float = 0.0        # std of the normal bias, or gamma of the Zipf bias
     zipf_s: float = 0.0
@@ -71,6 +72,8 @@ WORKLOADS = {
                         invalid_frac=0.02),
     "heavy": Workload("heavy", T=32768, H=7168, E=32, K=8, F=2048, precision="mxfp8",
                       bias="zipf", bias_scale=1.0, zipf_s=1.5, backward=True),
+    "dsv3_nvfp4": Workload("dsv3_nvfp4", T=8192, H=7168, E=32, K=4, F=2048, precision="nvfp4",
+                           bias="zipf", bias_scale=2.0, zipf_s=1.1),
     "dsv3_sigmoid": Workload("dsv3_sigmoid", T=8192, H=7168, E=32, K=4, F=2048, precision="mxfp8",
                              bias="zipf", bias_scale=2.0, zipf_s=1.1, score="sigmoid",
                              expert_bias_scale=0.05, renorm=True),

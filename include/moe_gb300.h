@@ -247,6 +247,31 @@ moe_status moe_quant_mxfp8_grouped(const void *x, int R_cap, int H,
                                    unsigned flags, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * NVFP4 operands ([TEJAX] "Measured training impact with JAX + Transformer
+ * Engine" and [WITTY] "What to watch" name NVFP4 as a planned addition and do
+ * not define it; NVIDIA's published format is taken). Elements E2M1 (0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6 and their negatives); 16 consecutive elements of a row
+ * share one E4M3 decode scale; the tensor has one fp32 encode scale
+ * S = 448 * 6 / amax (1 when amax is 0, at most FLT_MAX); a value decodes as
+ * e2m1 * e4m3(scale) / S. Encoder, in fp32 with one rounding per operation:
+ *   scale = E4M3(round to nearest even, saturating)((amax_block / 6) * S)
+ *   code  = E2M1(round to nearest even, saturating to 6, sign kept)(x * (S / e4m3(scale))),
+ *           0 when e4m3(scale) is 0.
+ * Packing: element 2i in the low nibble of byte i, 2i+1 in the high nibble.
+ *
+ * moe_amax_bf16: *amax = max |x| over rows [0, n) of x [rows, cols] bf16, with
+ *   n = rows, or min(rows, *valid_rows) when valid_rows (a device int, e.g.
+ *   &group_offsets[E]) is given; cols % 8 == 0; amax is zeroed on the stream
+ *   first. moe_quant_nvfp4: the same rows of x quantised with the encode scale of
+ *   the device *amax: q [rows, cols/2] packed codes (8-byte aligned), scales
+ *   [rows, cols/16]; rows past n are not written; cols % 16 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_amax_bf16(const void *x, long long rows, int cols, const int32_t *valid_rows,
+                         float *amax, moe_stream_t stream);
+moe_status moe_quant_nvfp4(const void *x, long long rows, int cols, const int32_t *valid_rows,
+                           const float *amax, uint8_t *q, uint8_t *scales, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Grouped SwiGLU expert MLP ([TEJAX] "Optimization 1: Grouped GEMM": one
  * kernel covers all experts, each with its actual token count, computing only
  * valid regions, with the counts kept on the device; MoE-layer figure: the
@@ -302,6 +327,30 @@ moe_status moe_grouped_gemm_down(const void *h, const uint8_t *h_scales, const v
                                  const uint8_t *w2_scales, moe_dtype dtype,
                                  const int32_t *group_offsets, int E, int H, int F, int R_cap,
                                  void *y_perm, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The grouped SwiGLU MLP's two GEMMs on NVFP4 operands (tcgen05 kind
+ * mxf4nvf4: E2M1 x E2M1 with a UE4M3 scale per 16 elements, fp32
+ * accumulation, the two tensors' encode scales divided out in the epilogue).
+ * Operands as moe_quant_nvfp4 writes them: x_q [R_cap, H/2] + x_scales
+ * [R_cap, H/16] with the device x_amax; weights in the packed layouts of
+ * moe_grouped_gemm_up (w13 [E][2F][H]) and down (w2 [E][H][F]) quantised
+ * row-wise along the contraction dimension, each stacked tensor with one amax.
+ * moe_grouped_gemm_up_nvfp4 writes h [R_cap, F] bf16 = silu(a) * b, the
+ * optional ab_save like moe_grouped_gemm_up, and *h_amax = max |h| over the
+ * rows it wrote (zeroed on the stream first), which moe_quant_nvfp4 takes to
+ * quantise h for moe_grouped_gemm_down_nvfp4 (y_perm [R_cap, H] bf16).
+ * Requires H % 256 == 0 and F % 256 == 0 (128-byte k-blocks of 256 elements);
+ * operand bases 128-byte aligned, scales 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+moe_status moe_grouped_gemm_up_nvfp4(const void *x_q, const uint8_t *x_scales, const float *x_amax,
+                                     const void *w13_q, const uint8_t *w13_scales, const float *w13_amax,
+                                     const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                                     void *h, float *h_amax, void *ab_save, moe_stream_t stream);
+moe_status moe_grouped_gemm_down_nvfp4(const void *h_q, const uint8_t *h_scales, const float *h_amax,
+                                       const void *w2_q, const uint8_t *w2_scales, const float *w2_amax,
+                                       const int32_t *group_offsets, int E, int H, int F, int R_cap,
+                                       void *y_perm, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Grouped backward of the SwiGLU expert MLP (the training step of [TEJAX]
