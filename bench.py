@@ -250,9 +250,8 @@ def run_ours(args, wl, rank, world, local_rank):
               ("gemm_up", layer.stage_gemm_up), ("gemm_down", layer.stage_gemm_down),
               ("combine", layer.stage_combine)]
     if layer.nv4:
-        # NVFP4: the amax and quantisation passes before each GEMM are stages of their own
-        stages.insert(2, ("quant_x", layer.stage_quant_x))
-        stages.insert(4, ("quant_h", layer.stage_quant_h))
+        # NVFP4: h's quantisation between the GEMMs is a stage of its own (x's is in the permute)
+        stages.insert(3, ("quant_h", layer.stage_quant_h))
     if wl.backward:
         # the whole layer's backward, from dy [T, H]: combine, expert MLP (dgrad, dx, transposes,
         # wgrad), permute and router backward
@@ -401,7 +400,9 @@ def stage_report(wl, R, stage_ms, active=None):
     q = (1 + 1 / 32) if fp8 else (0.5 + 1 / 16) if nv4 else 2
     bytes_ = {
         "route": T * E * 4 + T * K * (idb + 4) + (E * 4 if wl.score == "sigmoid" else 0),
-        "permute": T * H * 2 + R * H * b_out + (R * H // 32 if fp8 else 0) + T * K * (idb + 4) + R * 4,
+        # (NVFP4: the routed tokens' amax reads x once more; rows written as codes and scales)
+        "permute": T * H * 2 * (2 if nv4 else 1) + (R * H * q if nv4 else R * H * b_out + (R * H // 32 if fp8 else 0))
+                   + T * K * (idb + 4) + R * 4,
         "combine": R * H * 2 + T * K * 8 + T * H * 2,
         # read dy and y_perm, write dy_perm (MXFP8: and its codes and scales); route metadata and dprobs
         "combine_bwd": T * H * 2 + R * H * 2 + R * H * 2 + (R * H * (1 + 1 / 32) if fp8 else 0) + T * K * 12,
@@ -409,8 +410,6 @@ def stage_report(wl, R, stage_ms, active=None):
         "route_bwd": T * E * 4 * 2 + T * K * (idb + 4),
         # read h (or its bf16 copy), dy, x (gathered), dab in bf16; write the transposed operands
         "wgrad_transpose": R * 2 * (F + H + H + 2 * F) + R * b_out * (F + H + H + 2 * F) * (1 + (1 / 32 if fp8 else 0)),
-        # NVFP4: amax pass + quantisation pass over x_perm (read twice, written as codes and scales)
-        "quant_x": R * H * 2 * 2 + R * H * q,
         "quant_h": R * F * 2 + R * F * q,
         "gemm_up": R * H * q + Ea * H * 2 * F * q + R * F * (2 if nv4 else q),
         "gemm_down": R * F * q + Ea * F * H * q + R * H * 2,

@@ -31,6 +31,7 @@ SIGNATURES = {
     "moe_route_topk_backward": (I, [P, P, I, P, I, I, I, U, P, P]),
     "moe_route_sigmoid_topk": (I, [P, P, I, I, I, P, I, P, U, P]),
     "moe_amax_bf16": (I, [P, LL, I, P, P, P]),
+    "moe_permute_nvfp4": (I, [P, I, I, P, I, I, I, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_quant_nvfp4": (I, [P, LL, I, P, P, P, P, P]),
     "moe_grouped_gemm_up_nvfp4": (I, [P, P, P, P, P, P, P, I, I, I, I, P, P, P, P]),
     "moe_grouped_gemm_down_nvfp4": (I, [P, P, P, P, P, P, P, I, I, I, I, P, P]),

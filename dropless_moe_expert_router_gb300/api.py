@@ -142,10 +142,14 @@ def moe_permute_kernel_launches(T: int, K: int, E: int) -> int:
     return int(_lib.load().moe_permute_kernel_launches(T, K, E))
 
 
-def permute_buffers(T: int, H: int, K: int, E: int, device, fuse_mxfp8: bool = False) -> Permuted:
+def permute_buffers(T: int, H: int, K: int, E: int, device, fuse_mxfp8: bool = False,
+                    nvfp4: bool = False) -> Permuted:
     R_cap = T * K
     dev = torch.device(device)
-    if fuse_mxfp8:
+    if nvfp4:
+        xp = torch.empty((R_cap, H // 2), dtype=torch.uint8, device=dev)
+        xs = torch.empty((R_cap, H // 16), dtype=torch.uint8, device=dev)
+    elif fuse_mxfp8:
         xp = torch.empty((R_cap, H), dtype=torch.uint8, device=dev)
         xs = torch.empty((R_cap, H // 32), dtype=torch.uint8, device=dev)
     else:
@@ -176,6 +180,31 @@ def moe_permute(x: torch.Tensor, ids: torch.Tensor, E: int, *, fuse_mxfp8: bool 
         MOE_PERMUTE_FUSE_MXFP8 if fuse_mxfp8 else 0, _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_permute", st)
     return out
+
+
+def moe_permute_nvfp4(x: torch.Tensor, ids: torch.Tensor, E: int, *, amax: Optional[torch.Tensor] = None,
+                      out: Optional[Permuted] = None, workspace: Optional[torch.Tensor] = None,
+                      stream=None):
+    """moe_permute writing NVFP4 rows: the routed tokens' amax first (-> amax [1] fp32), then the
+    scatter quantises each row as it copies it (x_perm [R_cap, H/2] packed E2M1, x_perm_scales
+    [R_cap, H/16] E4M3). Returns (Permuted, amax)."""
+    _want(x, "x", torch.bfloat16, 2)
+    _want(ids, "ids", None, 2)
+    T, H = x.shape
+    K = ids.shape[1]
+    if out is None:
+        out = permute_buffers(T, H, K, E, x.device, nvfp4=True)
+    if amax is None:
+        amax = torch.empty((1,), dtype=torch.float32, device=x.device)
+    ws_bytes = moe_permute_workspace_size(T, K, E)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st = _lib.load().moe_permute_nvfp4(
+        _ptr(x), T, H, _ptr(ids), _id_code(ids.dtype), K, E, _ptr(amax), _ptr(out.x_perm), _ptr(out.x_perm_scales),
+        _ptr(out.group_sizes), _ptr(out.group_offsets), _ptr(out.row_map), _ptr(out.perm_src), _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    _check("moe_permute_nvfp4", st)
+    return out, amax
 
 
 def moe_permute_noalloc(x: torch.Tensor, ids: torch.Tensor, E: int, *, fuse_mxfp8: bool = False,

@@ -103,6 +103,27 @@ __device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, uint32_t* 
     return out;
 }
 
+// One NVFP4 block of 16 values held by two adjacent lanes (8 each, the even lane first; both
+// lanes must call): this lane's 8 packed codes, and in *sbyte the block's E4M3 scale. The same
+// arithmetic as nvfp4_block.
+__device__ __forceinline__ uint32_t nvfp4_pair(const float* f, float S, uint32_t* sbyte) {
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) am = fmaxf(am, fabsf(f[i]));
+    am = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
+    const float sbf = __fmul_rn(__fdiv_rn(am, 6.0f), S);
+    const uint32_t sb = (uint32_t)f32x2_to_e4m3x2(sbf, 0.0f) & 0xffu;
+    const float ds = e4m3_value(sb);
+    uint32_t out = 0u;
+    if (ds > 0.0f) {
+        const float rs = __fdiv_rn(S, ds);
+#pragma unroll
+        for (int i = 0; i < 8; i++) out |= e2m1_code(__fmul_rn(f[i], rs)) << (4 * i);
+    }
+    *sbyte = sb;
+    return out;
+}
+
 // 8 bf16 (one uint4) -> floats.
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
     const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);

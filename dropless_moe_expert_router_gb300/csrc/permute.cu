@@ -256,7 +256,9 @@ inline bool scan_in_block(int E, long long tiles) {
     return (long long)E * tiles <= SCAN_IN_BLOCK_MAX && ((long long)E * tiles + E + 1) * 4 <= 48 * 1024;
 }
 
-template <int KC, bool FUSE, bool SCAN>
+// FUSE: 0 bf16 rows; 1 MXFP8 rows (E4M3 + one E8M0 byte per 32, quads of lanes); 2 NVFP4 rows
+// (packed E2M1 + one E4M3 byte per 16, pairs of lanes) with the encode scale of the device *amax.
+template <int KC, int FUSE, bool SCAN>
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restrict__ x, int T, int H,
                                                            const void* __restrict__ ids, bool i16, int K, int E,
                                                            int TT, int tiles, const int* __restrict__ table,
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
                                                            int* __restrict__ group_offsets,
                                                            int* __restrict__ row_map, int* __restrict__ perm_src,
                                                            void* __restrict__ x_perm,
-                                                           uint8_t* __restrict__ scales) {
+                                                           uint8_t* __restrict__ scales,
+                                                           const float* __restrict__ amax) {
     extern __shared__ int s_dyn[];  // SCAN: table [E][tiles], then offsets [E + 1]
     const int lane = (int)lane_id();
     const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
@@ -324,6 +327,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
     }
     const int H8 = H >> 3;     // 16-byte chunks per row
     const int iters = (H8 + 31) >> 5;
+    float S = 1.0f;
+    if constexpr (FUSE == 2) S = nvfp4_encode_scale(__ldg(amax));
     for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
         const int tile = (int)(t / TT);
         int rows[KC];
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
                 in[u] = (it0 + u < iters) && j < H8;
                 v[u] = in[u] ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
             }
-            if (!FUSE) {
+            if constexpr (FUSE == 0) {
 #pragma unroll
                 for (int c = 0; c < KC; c++) {
                     unsigned m = mask[c];
@@ -370,6 +375,33 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
 #pragma unroll
                         for (int u = 0; u < U; u++)
                             if (in[u]) dst[(it0 + u) * 32] = v[u];
+                    }
+                }
+            } else if constexpr (FUSE == 2) {
+                uint32_t qv[U], sb[U];
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    if (it0 + u < iters) {  // warp-uniform: the pair shuffles see every lane
+                        float f[8];
+                        bf16x8_to_f32(v[u], f);
+                        qv[u] = nvfp4_pair(f, S, &sb[u]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < KC; c++) {
+                    unsigned m = mask[c];
+                    while (m) {
+                        const int b = __ffs(m) - 1;
+                        m &= m - 1;
+                        const int r = __shfl_sync(FULL, rows[c], b);
+#pragma unroll
+                        for (int u = 0; u < U; u++) {
+                            if (in[u]) {
+                                const int j = (it0 + u) * 32 + lane;
+                                reinterpret_cast<uint32_t*>(x_perm)[(long long)r * H8 + j] = qv[u];
+                                if ((lane & 1) == 0) scales[(long long)r * (H >> 4) + (j >> 1)] = (uint8_t)sb[u];
+                            }
+                        }
                     }
                 }
             } else {
@@ -402,6 +434,42 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
                 }
             }
         }
+    }
+}
+
+// max |x| over the tokens with at least one valid route (0 <= id < E): the amax of the rows the
+// permute copies. Warp per token; *amax zeroed by the caller; one atomic per CTA.
+__global__ void __launch_bounds__(256) amax_routed_kernel(const uint4* __restrict__ x, int T, int H,
+                                                          const void* __restrict__ ids, bool i16, int K, int E,
+                                                          float* __restrict__ amax) {
+    const int lane = (int)lane_id();
+    const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
+    const int H8 = H >> 3;
+    float m = 0.0f;
+    for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
+        bool routed = false;
+        for (int k = lane; k < K; k += 32) {
+            const int e = load_id(ids, t * K + k, i16);
+            routed |= e >= 0 && e < E;
+        }
+        if (!__any_sync(FULL, routed)) continue;        // warp-uniform
+        const uint4* src = x + t * H8;
+        for (int j = lane; j < H8; j += 32) {
+            float f[8];
+            bf16x8_to_f32(__ldg(src + j), f);
+#pragma unroll
+            for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(f[i]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    __shared__ float wmax[8];
+    if (lane == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.0f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) b = fmaxf(b, wmax[w]);
+        if (b > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(b));
     }
 }
 
@@ -510,16 +578,15 @@ extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
     return align16((size_t)E * (size_t)(tiles > 0 ? tiles : 1) * sizeof(int)) + 16;
 }
 
-extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
-                                  int E, void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes,
-                                  int32_t* group_offsets, int32_t* row_map, int32_t* perm_src,
-                                  unsigned flags, void* workspace, size_t workspace_bytes,
-                                  moe_stream_t stream) {
+// fuse_mode: 0 bf16 rows, 1 MXFP8, 2 NVFP4 (with the device amax already computed on the stream)
+static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K, int E,
+                               void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes, int32_t* group_offsets,
+                               int32_t* row_map, int32_t* perm_src, int fuse_mode, const float* amax,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     using namespace moe;
     if (T < 0 || H < 32 || (H % 32) != 0 || K < 1 || E < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
     if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
-    if (flags & ~MOE_PERMUTE_FUSE_MXFP8) return MOE_ERR_INVALID_ARG;
-    const bool fuse = (flags & MOE_PERMUTE_FUSE_MXFP8) != 0;
+    const bool fuse = fuse_mode != 0;
     if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !ids || !x_perm || !row_map || !perm_src)) return MOE_ERR_INVALID_ARG;
     if (fuse && T > 0 && !x_perm_scales) return MOE_ERR_INVALID_ARG;
@@ -585,19 +652,56 @@ extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, 
 #define MOE_SCATTER(kc, fz, sc)                                                                                  \
     perm_scatter_kernel<kc, fz, sc><<<(int)blocks, 256, ssmem, s>>>((const uint4*)x, T, H, ids, i16, K, E, TT,   \
                                                                     tiles, w.table, group_sizes, group_offsets, \
-                                                                    row_map, perm_src, x_perm, x_perm_scales)
+                                                                    row_map, perm_src, x_perm, x_perm_scales, amax)
 #define MOE_SCATTER_KC(fz, sc)        \
     if (KC == 1) MOE_SCATTER(1, fz, sc); \
     else if (KC == 2) MOE_SCATTER(2, fz, sc); \
     else MOE_SCATTER(4, fz, sc);
-    if (fuse) {
-        if (in_block) { MOE_SCATTER_KC(true, true) } else { MOE_SCATTER_KC(true, false) }
+    if (fuse_mode == 1) {
+        if (in_block) { MOE_SCATTER_KC(1, true) } else { MOE_SCATTER_KC(1, false) }
+    } else if (fuse_mode == 2) {
+        if (in_block) { MOE_SCATTER_KC(2, true) } else { MOE_SCATTER_KC(2, false) }
     } else {
-        if (in_block) { MOE_SCATTER_KC(false, true) } else { MOE_SCATTER_KC(false, false) }
+        if (in_block) { MOE_SCATTER_KC(0, true) } else { MOE_SCATTER_KC(0, false) }
     }
 #undef MOE_SCATTER_KC
 #undef MOE_SCATTER
     return moe_host::launch_status();
+}
+
+extern "C" moe_status moe_permute(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
+                                  int E, void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes,
+                                  int32_t* group_offsets, int32_t* row_map, int32_t* perm_src,
+                                  unsigned flags, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
+    if (flags & ~MOE_PERMUTE_FUSE_MXFP8) return MOE_ERR_INVALID_ARG;
+    return permute_impl(x, T, H, ids, id_dtype, K, E, x_perm, x_perm_scales, group_sizes, group_offsets, row_map,
+                        perm_src, (flags & MOE_PERMUTE_FUSE_MXFP8) ? 1 : 0, nullptr, workspace, workspace_bytes,
+                        stream);
+}
+
+extern "C" moe_status moe_permute_nvfp4(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
+                                        int E, float* x_amax, void* x_perm_q, uint8_t* x_perm_scales,
+                                        int32_t* group_sizes, int32_t* group_offsets, int32_t* row_map,
+                                        int32_t* perm_src, void* workspace, size_t workspace_bytes,
+                                        moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 32 || (H % 32) != 0 || K < 1 || E < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
+    if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
+    if (!x_amax || (T > 0 && (!x || !ids || !x_perm_scales))) return MOE_ERR_INVALID_ARG;
+    if (!moe_host::aligned(x_amax, 4) || !moe_host::aligned(x, 16)) return MOE_ERR_ALIGNMENT;
+    cudaStream_t s = moe_host::as_stream(stream);
+    // 0. the amax of the routed tokens' rows (= of the rows the scatter writes)
+    if (cudaMemsetAsync(x_amax, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (T > 0) {
+        long long blocks = ((long long)T + 7) / 8;
+        const long long cap = (long long)sm_count() * 8;
+        if (blocks > cap) blocks = cap;
+        amax_routed_kernel<<<(int)blocks, 256, 0, s>>>((const uint4*)x, T, H, ids, id_dtype == MOE_I16, K, E, x_amax);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return permute_impl(x, T, H, ids, id_dtype, K, E, x_perm_q, x_perm_scales, group_sizes, group_offsets, row_map,
+                        perm_src, 2, x_amax, workspace, workspace_bytes, stream);
 }
 
 extern "C" moe_status moe_quant_mxfp8_grouped(const void* x, int R_cap, int H, const int32_t* group_offsets,

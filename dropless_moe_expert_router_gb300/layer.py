@@ -48,15 +48,14 @@ class MoELayer:
         self.R_cap = R_cap
         self.ids = torch.empty((T, K), dtype=id_dtype, device=dev)
         self.probs = torch.empty((T, K), dtype=torch.float32, device=dev)
-        self.perm = api.permute_buffers(T, H, K, E, dev, fuse_mxfp8=self.fp8)
+        self.perm = api.permute_buffers(T, H, K, E, dev, fuse_mxfp8=self.fp8, nvfp4=self.nv4)
         self.workspace = torch.empty(api.moe_permute_workspace_size(T, K, E), dtype=torch.uint8, device=dev)
         self.h = torch.empty((R_cap, F), dtype=torch.uint8 if self.fp8 else torch.bfloat16, device=dev)
         self.h_scales = torch.empty((R_cap, F // 32), dtype=torch.uint8, device=dev) if self.fp8 else None
         if self.nv4:
-            # NVFP4 operands of the two GEMMs: x_perm and h quantised with their tensors' amax
+            # NVFP4 operands of the two GEMMs: x_perm (written by the permute) and h quantised
+            # with their tensors' amax
             u8, f32 = torch.uint8, torch.float32
-            self.x_q = torch.empty((R_cap, H // 2), dtype=u8, device=dev)
-            self.x_s = torch.empty((R_cap, H // 16), dtype=u8, device=dev)
             self.x_amax = torch.empty((1,), dtype=f32, device=dev)
             self.h_amax = torch.empty((1,), dtype=f32, device=dev)
             self.h_q = torch.empty((R_cap, F // 2), dtype=u8, device=dev)
@@ -97,8 +96,8 @@ class MoELayer:
     # (rank, [scan,] scatter), GEMM 2, combine 1
     @property
     def launches_per_forward(self) -> int:
-        # (NVFP4 adds x_perm's amax and the quantisations of x_perm and h)
-        return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E) + (3 if self.nv4 else 0)
+        # (NVFP4 adds the routed tokens' amax and the quantisation of h)
+        return 4 + api.moe_permute_kernel_launches(self.T, self.K, self.E) + (2 if self.nv4 else 0)
 
     def stage_route(self, logits, stream=None):
         if self.score == "sigmoid":
@@ -114,17 +113,12 @@ class MoELayer:
         return self.perm.group_sizes
 
     def stage_permute(self, x, stream=None):
+        if self.nv4:
+            api.moe_permute_nvfp4(x, self.ids, self.E, amax=self.x_amax, out=self.perm, workspace=self.workspace,
+                                  stream=stream)
+            return
         api.moe_permute(x, self.ids, self.E, fuse_mxfp8=self.fp8, out=self.perm, workspace=self.workspace,
                         stream=stream)
-
-    def stage_quant_x(self, stream=None):
-        """NVFP4 only: x_perm's amax over the routed rows and its row-wise quantisation."""
-        if not self.nv4:
-            return
-        valid = self.perm.group_offsets[self.E:]
-        api.moe_amax_bf16(self.perm.x_perm, valid_rows=valid, amax=self.x_amax, stream=stream)
-        api.moe_quant_nvfp4(self.perm.x_perm, self.x_amax, valid_rows=valid, q=self.x_q, scales=self.x_s,
-                            stream=stream)
 
     def stage_quant_h(self, stream=None):
         """NVFP4 only: h quantised with the amax the up projection gathered."""
@@ -137,7 +131,7 @@ class MoELayer:
         w = self.weights
         if self.nv4:
             # h (bf16) and its amax from the NVFP4 operands
-            api.moe_grouped_gemm_up_nvfp4(self.x_q, self.x_s, self.x_amax, w, self.perm.group_offsets, h=self.h,
+            api.moe_grouped_gemm_up_nvfp4(self.perm.x_perm, self.perm.x_perm_scales, self.x_amax, w, self.perm.group_offsets, h=self.h,
                                           h_amax=self.h_amax, stream=stream)
             return
         ab = self.ab if self.training else None
@@ -168,7 +162,6 @@ class MoELayer:
         """x [T, H] bf16 and logits [T, E] fp32 on the device -> y [T, H] bf16 (a layer-owned buffer)."""
         self.stage_route(logits, stream)
         self.stage_permute(x, stream)
-        self.stage_quant_x(stream)
         self.stage_gemm_up(stream)
         self.stage_quant_h(stream)
         self.stage_gemm_down(stream)

@@ -271,6 +271,19 @@ moe_status moe_amax_bf16(const void *x, long long rows, int cols, const int32_t 
 moe_status moe_quant_nvfp4(const void *x, long long rows, int cols, const int32_t *valid_rows,
                            const float *amax, uint8_t *q, uint8_t *scales, moe_stream_t stream);
 
+/* moe_permute_nvfp4: moe_permute (same routing outputs, workspace and rules)
+ * whose scatter writes NVFP4 rows: first *x_amax = max |x| over the tokens
+ * with at least one valid route (exactly the amax of the rows x_perm
+ * receives; zeroed on the stream first), then each row is quantised with that
+ * amax's encode scale as it is copied: x_perm_q [T*K, H/2] packed E2M1 (4-byte
+ * aligned), x_perm_scales [T*K, H/16] E4M3 -- the bytes moe_quant_nvfp4 would
+ * write from the bf16 permuted rows. One kernel more than moe_permute. */
+moe_status moe_permute_nvfp4(const void *x, int T, int H, const void *ids, moe_dtype id_dtype,
+                             int K, int E, float *x_amax, void *x_perm_q, uint8_t *x_perm_scales,
+                             int32_t *group_sizes, int32_t *group_offsets, int32_t *row_map,
+                             int32_t *perm_src, void *workspace, size_t workspace_bytes,
+                             moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Grouped SwiGLU expert MLP ([TEJAX] "Optimization 1: Grouped GEMM": one
  * kernel covers all experts, each with its actual token count, computing only

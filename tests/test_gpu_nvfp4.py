@@ -70,6 +70,37 @@ def test_quant_ties_and_zero_tensor():
     assert a0.item() == 0.0 and not qz.any() and not sz.any()
 
 
+@pytest.mark.parametrize("T,H,E,K,i16,invalid", [(300, 512, 8, 2, False, 0.1), (129, 7168, 32, 4, True, 0.0),
+                                                 (64, 256, 2304, 36, True, 0.05), (1, 32, 1, 1, False, 0.0)])
+def test_permute_nvfp4_matches_oracle(T, H, E, K, i16, invalid):
+    """The fused permute's NVFP4 rows are the oracle's permuted rows quantised with the amax of
+    the routed rows: a token whose routes are all invalid (and whose row holds the largest value)
+    takes no part in it. Routing outputs as moe_permute's."""
+    rng = np.random.default_rng(T * 7 + E)
+    x = rng.standard_normal((T, H)) * np.exp(rng.uniform(-3, 3, (T, 1)))
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[rng.random((T, K)) < invalid] = -1
+    if T > 1:
+        ids[T // 2, :] = -1
+        x[T // 2, 5] = 1e4
+    xb = _bf16(x)
+    dt = torch.int16 if i16 else torch.int32
+    p, amax = api.moe_permute_nvfp4(xb.cuda(), torch.from_numpy(ids).to(dt).cuda(), E)
+    torch.cuda.synchronize()
+    op = O.permute(bf16_bits(xb), ids, E)
+    R = op["R"]
+    assert np.array_equal(p.group_sizes.cpu().numpy(), op["group_sizes"])
+    assert np.array_equal(p.group_offsets.cpu().numpy(), op["group_offsets"])
+    assert np.array_equal(p.row_map.cpu().numpy(), op["row_map"])
+    assert np.array_equal(p.perm_src.cpu().numpy()[:R], op["perm_src"][:R])
+    ref_amax = O.bf16_amax(op["x_perm"][:R])
+    assert float(amax.item()) == ref_amax
+    rq, rs, _ = O.quant_rows_nvfp4(op["x_perm"][:R], S=O.nvfp4_encode_scale(ref_amax))
+    assert np.array_equal(p.x_perm.cpu().numpy()[:R], rq)
+    assert np.array_equal(p.x_perm_scales.cpu().numpy()[:R], rs)
+    assert api.moe_get_device_errors() == 0
+
+
 def _oracle_weights_nvfp4(w1, w3, w2):
     """Decoded weights (float64, logical layouts) as the GPU packs and quantises them: W1, W3 along
     H with one amax over both, W2 along F with its own amax."""
@@ -142,7 +173,7 @@ def test_nvfp4_layer_graph_replay_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
     assert torch.isfinite(out.float()).all() and out.float().abs().max() > 0
-    assert layer.launches_per_forward == 7 + api.moe_permute_kernel_launches(wl.T, wl.K, wl.E)
+    assert layer.launches_per_forward == 6 + api.moe_permute_kernel_launches(wl.T, wl.K, wl.E)
     with pytest.raises(ValueError):
         MoELayer(w1, w3, w2, T=wl.T, K=wl.K, precision="nvfp4", training=True)
 
