@@ -107,3 +107,27 @@ def test_stage_report_bytes_and_roofline_bound():
     R = wl.T * wl.K
     _, _, nbytes = bench.stage_report(wl, R, {"gemm_up": 1.0}, active=wl.E)
     assert nbytes["gemm_up"] == R * wl.H * 2 + wl.E * wl.H * 2 * wl.F * 2 + R * wl.F * 2
+
+
+def test_stage_report_nvfp4_and_sigmoid_bytes():
+    """NVFP4 operands count half a byte plus a 1/16 scale share per element; the NVFP4 permute
+    reads x twice (the routed tokens' amax, then the scatter) and writes codes and scales; the
+    up projection writes bf16 h (quantised by its own stage); the sigmoid router also reads the
+    expert bias."""
+    import bench
+    from dropless_moe_expert_router_gb300 import workloads as W
+    wl = W.get("dsv3_nvfp4")
+    T, H, E, K, F = wl.T, wl.H, wl.E, wl.K, wl.F
+    R = T * K
+    ms = {"permute": 1.0, "gemm_up": 1.0, "quant_h": 1.0, "gemm_down": 1.0}
+    out, flops, nb = bench.stage_report(wl, R, ms, active=E)
+    q = 0.5 + 1 / 16
+    assert nb["permute"] == 2 * T * H * 2 + R * H * q + T * K * (4 + 4) + R * 4
+    assert nb["gemm_up"] == R * H * q + E * H * 2 * F * q + R * F * 2
+    assert nb["quant_h"] == R * F * 2 + R * F * q
+    assert nb["gemm_down"] == R * F * q + E * F * H * q + R * H * 2
+    assert flops["gemm_up"] == 4.0 * R * H * F and "TFLOP/s" in out["gemm_up"]
+    ws = W.get("dsv3_sigmoid")
+    _, _, nb_s = bench.stage_report(ws, ws.T * ws.K, {"route": 1.0}, active=ws.E)
+    _, _, nb_m = bench.stage_report(W.get("dsv3"), ws.T * ws.K, {"route": 1.0}, active=ws.E)
+    assert nb_s["route"] - nb_m["route"] == ws.E * 4
