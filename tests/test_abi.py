@@ -59,6 +59,34 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.moe_quant_mxfp8_grouped(None, 4, 64, None, 2, None, None, 8, None) == 1  # bad flag
 
 
+def test_argument_errors_of_the_later_entry_points_need_no_gpu(lib):
+    """Sigmoid router, NVFP4 and backward entry points reject bad shapes before any CUDA call
+    (1 = MOE_ERR_INVALID_ARG, 2 = MOE_ERR_UNSUPPORTED)."""
+    # sigmoid router: K > E; E past the register-resident limit; K past 64; T = 0 is a no-op
+    assert lib.moe_route_sigmoid_topk(None, None, 4, 8, 9, None, 1, None, 0, None) == 1
+    assert lib.moe_route_sigmoid_topk(None, None, 4, 1025, 2, None, 1, None, 0, None) == 2
+    assert lib.moe_route_sigmoid_topk(None, None, 4, 100, 65, None, 1, None, 0, None) == 2
+    assert lib.moe_route_sigmoid_topk(None, None, 0, 8, 2, None, 1, None, 0, None) == 0
+    assert lib.moe_route_sigmoid_topk(None, None, 4, 8, 2, None, 1, None, 4, None) == 1     # unknown flag
+    assert lib.moe_route_sigmoid_topk_backward(None, None, 1, None, 4, 8, 9, 0, None, None) == 1
+    # NVFP4: cols not whole 16-element blocks; the GEMMs' 256-element k-blocks
+    assert lib.moe_quant_nvfp4(None, 4, 24, None, None, None, None, None) == 1
+    assert lib.moe_amax_bf16(None, 4, 12, None, None, None) == 1
+    import ctypes
+    goff = ctypes.c_void_p(256)     # non-null placeholder: the shape check returns before any use
+    assert lib.moe_grouped_gemm_up_nvfp4(None, None, None, None, None, None, goff, 2, 384, 512, 64,
+                                         None, None, None, None) == 2
+    assert lib.moe_grouped_gemm_down_nvfp4(None, None, None, None, None, None, goff, 2, 512, 640, 64,
+                                           None, None) == 2
+    assert lib.moe_grouped_gemm_up_nvfp4(None, None, None, None, None, None, None, 2, 512, 512, 64,
+                                         None, None, None, None) == 1                      # no offsets
+    assert lib.moe_permute_nvfp4(None, 4, 48, None, 1, 2, 8, None, None, None, None, None, None, None,
+                                 None, 0, None) == 1                                           # H % 32 != 0
+    # combine backward: the fused MXFP8 outputs go together and need whole 32-element blocks
+    assert lib.moe_unpermute_combine_backward(None, None, None, None, 4, 2, 72, None, None, None, None,
+                                              None) == 1
+
+
 def test_workspace_size_covers_the_tile_table(lib):
     # one int32 per (expert, token tile) plus a 16-byte counter
     assert lib.moe_permute_workspace_size(8192, 2, 8) >= 8 * (8192 // 128) * 4 + 16
