@@ -208,7 +208,8 @@ def oracle_sample(wl, x_bits, logits_np, yperm_bits, gemm_rows: int, w_bits):
     gemm_full = (t3 - t2) * R / max(1, rows.size)
     total = (t1 - t0) + (t2 - t1) + gemm_full + (t4 - t3)
     desc = (f"router, permute and combine over all {wl.T} tokens; grouped SwiGLU MLP on {rows.size} of "
-            f"{R} permuted rows, extrapolated by row count")
+            f"{R} permuted rows, extrapolated by row count"
+            + ("" if wl.precision == "bf16" else f" (bf16 operands; the workload's GEMMs run {wl.precision})"))
     return total, desc
 
 
