@@ -100,6 +100,14 @@ def lib():
             L.oracle_quant_rows_nvfp4.argtypes = [P, i64, i64, f32, P, P]
             L.oracle_nvfp4_decode.restype = None
             L.oracle_nvfp4_decode.argtypes = [P, P, i64, i64, f32, P]
+            L.oracle_double_to_bf16_n.restype = None
+            L.oracle_double_to_bf16_n.argtypes = [P, i64, P]
+            L.oracle_swiglu_n.restype = None
+            L.oracle_swiglu_n.argtypes = [P, P, i64, P]
+            L.oracle_swiglu_grad_n.restype = None
+            L.oracle_swiglu_grad_n.argtypes = [P, P, P, i64, P, P]
+            L.oracle_quant_rows_f64.restype = None
+            L.oracle_quant_rows_f64.argtypes = [P, i64, i64, P, P]
             _lib = L
     return _lib
 
@@ -119,10 +127,10 @@ def bf16_to_f64(bits) -> np.ndarray:
 
 
 def f64_to_bf16(v) -> np.ndarray:
-    L = lib()
-    flat = np.asarray(v, dtype=np.float64).ravel()
-    out = np.fromiter((L.oracle_double_to_bf16(float(x)) for x in flat), dtype=np.uint16,
-                      count=flat.size)
+    """bf16 bits of float64 values (round to nearest even), element by element in C."""
+    flat = np.ascontiguousarray(np.asarray(v, dtype=np.float64).ravel())
+    out = np.empty(flat.size, np.uint16)
+    lib().oracle_double_to_bf16_n(_p(flat), flat.size, _p(out))
     return out.reshape(np.shape(v))
 
 
@@ -139,8 +147,46 @@ def e4m3_encode(v) -> np.ndarray:
                     dtype=np.uint8).reshape(np.shape(v))
 
 
+_E4M3_TABLE = None
+
+
+def e4m3_table() -> np.ndarray:
+    """The 256 E4M3 code values (oracle_e4m3_decode of every code), float64."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        L = lib()
+        _E4M3_TABLE = np.array([L.oracle_e4m3_decode(c) for c in range(256)], np.float64)
+    return _E4M3_TABLE
+
+
+def mx_decode_rows(q, s) -> np.ndarray:
+    """Values (float64) of row-wise MXFP8 [rows, cols] codes with [rows, cols/32] scales:
+    code value times 2^(scale byte - 127) (exact in float64)."""
+    q = np.asarray(q, np.uint8)
+    sc = np.ldexp(1.0, np.asarray(s, np.int64) - 127)
+    return e4m3_table()[q] * np.repeat(sc, 32, axis=-1)
+
+
+def mx_decode_cols(q, s) -> np.ndarray:
+    """Values (float64) of column-wise MXFP8 codes of one group [rows, cols] starting at
+    row 0, scales [rows/32 (rounded up), cols]: block b covers rows 32b .. 32b + 31."""
+    q = np.asarray(q, np.uint8)
+    sc = np.ldexp(1.0, np.asarray(s, np.int64) - 127)
+    return e4m3_table()[q] * np.repeat(sc, 32, axis=0)[: q.shape[0]]
+
+
 def e8m0_scale_byte(amax: float) -> int:
     return lib().oracle_e8m0_scale_byte(float(amax))
+
+
+def quant_rows_f64(x):
+    """Row-wise 1x32 MXFP8 of a float64 matrix (unrounded values) -> (q, s)."""
+    xv = _c(x, np.float64)
+    rows, cols = xv.shape
+    q = np.zeros((rows, cols), np.uint8)
+    s = np.zeros((rows, cols // 32), np.uint8)
+    lib().oracle_quant_rows_f64(_p(xv), rows, cols, _p(q), _p(s))
+    return q, s
 
 
 def quant_rows(x_bf16):
@@ -408,3 +454,59 @@ def wgrad_expert(A: Operand, B: Operand, group_offsets, e: int, cols=None):
 def expert_of_row(group_offsets, r: int) -> int:
     off = _c(group_offsets, np.int32)
     return lib().oracle_expert_of_row(_p(off), off.size - 1, int(r))
+
+
+# ------------------------------------------------- whole-expert blocks of rows
+def swiglu(a, b) -> np.ndarray:
+    """h = silu(a) * b element by element (the SwiGLU step, in C)."""
+    av, bv = _c(a, np.float64), _c(b, np.float64)
+    h = np.empty(av.shape)
+    lib().oracle_swiglu_n(_p(av), _p(bv), av.size, _p(h))
+    return h
+
+
+def swiglu_grad(dh, a, b):
+    """(da, db) of the SwiGLU step at (a, b) applied to dh (in C)."""
+    dv, av, bv = _c(dh, np.float64), _c(a, np.float64), _c(b, np.float64)
+    da, db = np.empty(av.shape), np.empty(av.shape)
+    lib().oracle_swiglu_grad_n(_p(dv), _p(av), _p(bv), av.size, _p(da), _p(db))
+    return da, db
+
+
+def expert_swiglu_block(xv, w1v, w3v, w2v=None, h_mode=H_BF16):
+    """One expert's grouped SwiGLU MLP on a block of its rows, from operand VALUES (decoded
+    bf16 / MXFP8 / NVFP4, float64), as oracle_swiglu_rows defines it for each row:
+      a = x W1, b = x W3 (a library matmul per product, float64),
+      h = silu(a) * b; with w2v: y = round_h(h) W2.
+    xv [n, H]; w1v, w3v [H, F'] -- any F' columns of the expert's F (every output column is
+    independent of the others); w2v [F, H] (all F columns needed). round_h is bf16 (H_BF16),
+    MXFP8 1x32 along F from the unrounded h (H_MXFP8), or none (H_NONE).
+    Returns dict(a, b, h (unrounded), h_bf16 (bits, H_BF16), h_q / h_s (H_MXFP8),
+    y (float64, unrounded; with w2v))."""
+    a = np.asarray(xv) @ np.asarray(w1v)
+    b = np.asarray(xv) @ np.asarray(w3v)
+    h = swiglu(a, b)
+    out = dict(a=a, b=b, h=h)
+    if h_mode == H_BF16:
+        out["h_bf16"] = f64_to_bf16(h)
+        hr = bf16_to_f64(out["h_bf16"])
+    elif h_mode == H_MXFP8:
+        out["h_q"], out["h_s"] = quant_rows_f64(h)
+        hr = mx_decode_rows(out["h_q"], out["h_s"])
+    else:
+        hr = h
+    if w2v is not None:
+        out["y"] = hr @ np.asarray(w2v)
+    return out
+
+
+def expert_swiglu_dgrad_block(dyv, w2v_rows, a_bf16, b_bf16):
+    """One expert's SwiGLU backward on a block of its rows at F' columns, as
+    oracle_swiglu_dgrad_rows defines it per row:
+      dh = dy W2^T at those columns (a library matmul, float64), then (da, db) from dh and
+      the saved bf16 pre-activations a, b.
+    dyv [n, H] values; w2v_rows [F', H]: the rows of the expert's W2 [F, H] at the F'
+    columns (values as the backward contracts them); a_bf16, b_bf16 [n, F'] bits.
+    Returns (da, db) unrounded, float64."""
+    dh = np.asarray(dyv) @ np.asarray(w2v_rows).T
+    return swiglu_grad(dh, bf16_to_f64(a_bf16), bf16_to_f64(b_bf16))

@@ -208,19 +208,37 @@ double oracle_e2m1_decode(uint8_t code)
     return sign ? -mag : mag;
 }
 
-/* Nearest E2M1 code (ties to the even mantissa bit), saturating to +-6, sign kept. */
-uint8_t oracle_e2m1_encode(double v)
+/* The values of the 16 E2M1 codes (oracle_e2m1_decode of each), for loops over many elements. */
+static void e2m1_values(double val[16])
+{
+    for (int c = 0; c < 16; c++)
+        val[c] = oracle_e2m1_decode((uint8_t)c);
+}
+
+/* Nearest E2M1 code to v (ties to the even mantissa bit), saturating to +-6, sign kept;
+ * val holds the code values (e2m1_values). */
+static uint8_t e2m1_encode_with(const double val[16], double v)
 {
     const uint8_t sign = signbit(v) ? 8 : 0;
     const double a = fmin(fabs(v), 6.0);      /* saturating: beyond 6 is 6 */
     int best = 0;
+    double db = fabs(val[0] - a);
     for (int c = 1; c < 8; c++) {
-        const double dc = fabs(oracle_e2m1_decode((uint8_t)c) - a);
-        const double db = fabs(oracle_e2m1_decode((uint8_t)best) - a);
-        if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1))
+        const double dc = fabs(val[c] - a);
+        if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1)) {
             best = c;
+            db = dc;
+        }
     }
     return (uint8_t)(sign | best);
+}
+
+/* Nearest E2M1 code (ties to the even mantissa bit), saturating to +-6, sign kept. */
+uint8_t oracle_e2m1_encode(double v)
+{
+    double val[16];
+    e2m1_values(val);
+    return e2m1_encode_with(val, v);
 }
 
 /* The tensor's fp32 encode scale from its amax. */
@@ -240,6 +258,8 @@ float oracle_nvfp4_encode_scale(float amax)
  */
 void oracle_quant_rows_nvfp4(const uint16_t *x, long rows, long cols, float S, uint8_t *q, uint8_t *s)
 {
+    double val[16];
+    e2m1_values(val);
     for (long r = 0; r < rows; r++)
         for (long b = 0; b < cols / 16; b++) {
             const uint16_t *blk = x + r * cols + b * 16;
@@ -257,7 +277,7 @@ void oracle_quant_rows_nvfp4(const uint16_t *x, long rows, long cols, float S, u
             volatile float rs = ds > 0.0f ? S / ds : 0.0f;
             for (int i = 0; i < 16; i++) {
                 volatile float v = (float)oracle_bf16_to_double(blk[i]) * rs;
-                const uint8_t c = ds > 0.0f ? oracle_e2m1_encode((double)v) : 0;
+                const uint8_t c = ds > 0.0f ? e2m1_encode_with(val, (double)v) : 0;
                 uint8_t *byte = q + r * (cols / 2) + b * 8 + i / 2;
                 if (i % 2 == 0)
                     *byte = (uint8_t)((*byte & 0xF0) | c);
@@ -270,12 +290,16 @@ void oracle_quant_rows_nvfp4(const uint16_t *x, long rows, long cols, float S, u
 /* Decode an NVFP4 matrix (packed q[rows, cols/2], scales s[rows, cols/16], encode scale S). */
 void oracle_nvfp4_decode(const uint8_t *q, const uint8_t *s, long rows, long cols, float S, double *out)
 {
+    double val[16];
+    e2m1_values(val);
     for (long r = 0; r < rows; r++)
-        for (long c = 0; c < cols; c++) {
-            const uint8_t byte = q[r * (cols / 2) + c / 2];
-            const uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
-            out[r * cols + c] =
-                oracle_e2m1_decode(code) * oracle_e4m3_decode(s[r * (cols / 16) + c / 16]) / (double)S;
+        for (long b = 0; b < cols / 16; b++) {
+            const double scale = oracle_e4m3_decode(s[r * (cols / 16) + b]);
+            for (long c = 16 * b; c < 16 * b + 16; c++) {
+                const uint8_t byte = q[r * (cols / 2) + c / 2];
+                const uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+                out[r * cols + c] = val[code] * scale / (double)S;
+            }
         }
 }
 
@@ -755,6 +779,19 @@ static int expert_of_row(const int32_t *off, int E, long r)
 
 static double silu(double a) { return a / (1.0 + exp(-a)); }
 
+/* The SwiGLU step of one element: h = silu(a) * b. */
+static double swiglu_value(double a, double b) { return silu(a) * b; }
+
+/* Its derivatives at (a, b) applied to dh (the chain rule of the line above):
+ *   da = dh * b * silu'(a),  silu'(a) = s(a) (1 + a (1 - s(a))),  s = logistic
+ *   db = dh * silu(a) */
+static void swiglu_grad(double dh, double a, double b, double *da, double *db)
+{
+    double sg = 1.0 / (1.0 + exp(-a));
+    *da = dh * b * (sg * (1.0 + a * (1.0 - sg)));
+    *db = dh * silu(a);
+}
+
 /* Rounding applied to the intermediate h before the second GEMM. */
 enum { H_NONE = 0, H_BF16 = 1, H_MXFP8 = 2 };
 
@@ -810,7 +847,7 @@ void oracle_swiglu_rows(int x_kind, const void *x_v, const uint8_t *x_s,
             }
         }
         for (int f = 0; f < F; f++)
-            hv[f] = silu(a[f]) * b[f];
+            hv[f] = swiglu_value(a[f], b[f]);
         if (a_f64)
             memcpy(a_f64 + i * F, a, sizeof(double) * F);
         if (b_f64)
@@ -906,11 +943,8 @@ void oracle_swiglu_dgrad_rows(int dy_kind, const void *dy_v, const uint8_t *dy_s
                 acc += dyr[j] * wr[j];
             dh[f] = acc;
         }
-        for (int f = 0; f < F; f++) {
-            double sg = 1.0 / (1.0 + exp(-a[f]));
-            da[f] = dh[f] * b[f] * (sg * (1.0 + a[f] * (1.0 - sg)));
-            db[f] = dh[f] * silu(a[f]);
-        }
+        for (int f = 0; f < F; f++)
+            swiglu_grad(dh[f], a[f], b[f], &da[f], &db[f]);
         if (da_f64)
             memcpy(da_f64 + i * F, da, sizeof(double) * F);
         if (db_f64)
@@ -1000,4 +1034,42 @@ void oracle_wgrad_expert(int a_kind, const void *a_v, const uint8_t *a_s, long n
 int oracle_expert_of_row(const int32_t *group_offsets, int E, long r)
 {
     return expert_of_row(group_offsets, E, r);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Element-wise array forms (for checks that take whole experts at once)     */
+/* ------------------------------------------------------------------------ */
+
+/* out[i] = bf16 bits of v[i] (oracle_double_to_bf16 per element). */
+void oracle_double_to_bf16_n(const double *v, long n, uint16_t *out)
+{
+    for (long i = 0; i < n; i++)
+        out[i] = oracle_double_to_bf16(v[i]);
+}
+
+/* h[i] = silu(a[i]) * b[i] (the SwiGLU step of oracle_swiglu_rows). */
+void oracle_swiglu_n(const double *a, const double *b, long n, double *h)
+{
+    for (long i = 0; i < n; i++)
+        h[i] = swiglu_value(a[i], b[i]);
+}
+
+/* da[i], db[i] from dh[i], a[i], b[i] (the SwiGLU backward step of
+ * oracle_swiglu_dgrad_rows). */
+void oracle_swiglu_grad_n(const double *dh, const double *a, const double *b, long n,
+                          double *da, double *db)
+{
+    for (long i = 0; i < n; i++)
+        swiglu_grad(dh[i], a[i], b[i], &da[i], &db[i]);
+}
+
+/* Row-wise 1x32 MXFP8 quantisation of a double matrix [rows, cols] (cols % 32 == 0):
+ * the rule of oracle_quant_rows_bf16 applied to unrounded values (MXFP8 h is quantised
+ * from its unrounded value). */
+void oracle_quant_rows_f64(const double *x, long rows, long cols, uint8_t *q, uint8_t *s)
+{
+    for (long r = 0; r < rows; r++)
+        for (long b = 0; b < cols / 32; b++)
+            s[r * (cols / 32) + b] =
+                (uint8_t)quant_block(x + r * cols + b * 32, 1, 32, q + r * cols + b * 32, 1);
 }

@@ -284,3 +284,106 @@ def test_dgrad_dab_rounding_modes_follow_their_operands():
         want = np.concatenate([da[off[e]:off[e + 1]] @ w1[e].T + db[off[e]:off[e + 1]] @ w3[e].T
                                for e in range(E)])
         assert np.allclose(got["dx_f64"], want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ whole-expert blocks of rows
+def test_mx_decode_matches_torch_float8():
+    """Row-wise and column-wise MXFP8 decoding against torch's float8_e4m3fn values (a library
+    conversion) times the power-of-two scales."""
+    rng = np.random.default_rng(7)
+    x = _bf16(rng.standard_normal((70, 96)) * np.exp(rng.uniform(-6, 6, (70, 1))))
+    q, s = O.quant_rows(x)
+    tv = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(O.mx_decode_rows(q, s), tv * np.repeat(np.exp2(s.astype(np.float64) - 127), 32, axis=1))
+    off = np.array([0, 70], np.int32)
+    qc, sc = O.quant_cols_grouped(x, off)
+    tv = torch.from_numpy(qc).view(torch.float8_e4m3fn).double().numpy()
+    want = tv * np.exp2(np.repeat(sc[:3].astype(np.float64), 32, axis=0)[:70] - 127)
+    assert np.array_equal(O.mx_decode_cols(qc, sc[:3]), want)
+
+
+def test_quant_rows_f64_equals_bf16_quantiser_on_bf16_values():
+    rng = np.random.default_rng(8)
+    x = _bf16(rng.standard_normal((9, 128)) * 3)
+    assert all(np.array_equal(a, b) for a, b in zip(O.quant_rows_f64(_f(x)), O.quant_rows(x)))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "mxfp8"])
+def test_expert_block_forward_matches_row_oracle(kind):
+    """The expert-block forward (a library matmul per product) reproduces oracle_swiglu_rows:
+    pre-activations and h to 1e-12, bf16 h bit for bit, MXFP8 h codes and scales bit for bit
+    where the two float64 h agree, y to 1e-12; a subset of F columns gives those columns."""
+    x, w1, w3, w2, off = _problem(11, H=64, F=96)
+    if kind == "mxfp8":
+        x, w1, w3, w2, off = _problem(11, H=64, F=64)        # MXFP8: whole 32-blocks along H and F
+        xq, xs = O.quant_rows(x)
+        w1q, w1s = zip(*(O.quant_rows(np.ascontiguousarray(w1[e].T)) for e in range(w1.shape[0])))
+        w3q, w3s = zip(*(O.quant_rows(np.ascontiguousarray(w3[e].T)) for e in range(w3.shape[0])))
+        w2q, w2s = zip(*(O.quant_rows(np.ascontiguousarray(w2[e].T)) for e in range(w2.shape[0])))
+        ops = [O.Operand(O.MAT_MXFP8, xq, xs)] + [
+            O.Operand(O.MAT_MXFP8, np.ascontiguousarray(np.stack(q).transpose(0, 2, 1)),
+                      np.ascontiguousarray(np.stack(s).transpose(0, 2, 1)))
+            for q, s in ((w1q, w1s), (w3q, w3s), (w2q, w2s))]
+        xv = O.mx_decode_rows(xq, xs)
+        wv = [np.stack([O.mx_decode_rows(q[e], s[e]).T for e in range(len(q))])
+              for q, s in ((w1q, w1s), (w3q, w3s), (w2q, w2s))]
+        hm = O.H_MXFP8
+    else:
+        ops = [O.Operand(O.MAT_BF16, t) for t in (x, w1, w3, w2)]
+        xv, wv, hm = _f(x), [_f(w1), _f(w3), _f(w2)], O.H_BF16
+    rows = np.arange(int(off[-1]), dtype=np.int32)
+    ref = O.swiglu_rows(*ops, off, rows, h_mode=hm,
+                        want=("a_f64", "b_f64", "h_f64", "y_f64", "h_bf16", "h_q", "h_s"))
+    for e in range(off.size - 1):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        blk = O.expert_swiglu_block(xv[r0:r1], wv[0][e], wv[1][e], wv[2][e], h_mode=hm)
+        for k in ("a", "b", "h", "y"):
+            assert np.allclose(blk[k], ref[k + "_f64"][r0:r1], rtol=1e-12, atol=1e-15), k
+        if hm == O.H_BF16:
+            assert np.array_equal(blk["h_bf16"], ref["h_bf16"][r0:r1])
+        else:
+            assert np.array_equal(blk["h_q"], ref["h_q"][r0:r1]) and np.array_equal(blk["h_s"], ref["h_s"][r0:r1])
+        cols = np.array([3, 17, 40], np.int64)
+        sub = O.expert_swiglu_block(xv[r0:r1], wv[0][e][:, cols], wv[1][e][:, cols], h_mode=O.H_NONE)
+        assert np.allclose(sub["h"], ref["h_f64"][r0:r1][:, cols], rtol=1e-12, atol=1e-15)
+
+
+def test_expert_block_dgrad_matches_row_oracle():
+    """The expert-block SwiGLU backward at a subset of F columns reproduces
+    oracle_swiglu_dgrad_rows' da, db (from the same bf16 pre-activations)."""
+    x, w1, w3, w2, off = _problem(12, H=64, F=96)
+    rng = np.random.default_rng(12)
+    R_cap = x.shape[0]
+    dy = _bf16(rng.standard_normal((R_cap, 64)) * 0.3)
+    a16 = _bf16(rng.standard_normal((R_cap, 96)))
+    b16 = _bf16(rng.standard_normal((R_cap, 96)))
+    rows = np.arange(int(off[-1]), dtype=np.int32)
+    Wo = [O.Operand(O.MAT_BF16, t) for t in (w1, w3, w2)]
+    ref = O.swiglu_dgrad_rows(O.Operand(O.MAT_BF16, dy), O.Operand(O.MAT_BF16, a16), O.Operand(O.MAT_BF16, b16),
+                              *Wo, off, rows, want=("da_f64", "db_f64"))
+    cols = np.array([0, 5, 31, 95], np.int64)
+    for e in range(off.size - 1):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        da, db = O.expert_swiglu_dgrad_block(_f(dy[r0:r1]), _f(w2[e][cols]), a16[r0:r1][:, cols], b16[r0:r1][:, cols])
+        assert np.allclose(da, ref["da_f64"][r0:r1][:, cols], rtol=1e-12, atol=1e-15)
+        assert np.allclose(db, ref["db_f64"][r0:r1][:, cols], rtol=1e-12, atol=1e-15)
+
+
+def test_swiglu_steps_match_finite_differences_and_closed_forms():
+    """h = silu(a) b: silu(0) = 0, silu(a) -> a for large a, h linear in b; its gradient matches
+    central differences of the forward step."""
+    a = np.array([0.0, 30.0, -30.0, 1.5, -0.7, 2.0])
+    b = np.array([2.0, 1.0, 1.0, -0.3, 0.9, 0.0])
+    h = O.swiglu(a, b)
+    assert h[0] == 0.0 and abs(h[1] - 30.0) < 1e-9 and abs(h[2]) < 1e-9 and h[5] == 0.0
+    assert np.allclose(O.swiglu(a, 2 * b), 2 * h, rtol=0, atol=0)
+    dh = np.array([1.0, -2.0, 0.5, 1.25, -1.0, 3.0])
+    da, db = O.swiglu_grad(dh, a, b)
+    eps = 1e-6
+    fda = dh * (O.swiglu(a + eps, b) - O.swiglu(a - eps, b)) / (2 * eps)
+    fdb = dh * (O.swiglu(a, b + eps) - O.swiglu(a, b - eps)) / (2 * eps)
+    assert np.allclose(da, fda, rtol=1e-6, atol=1e-8) and np.allclose(db, fdb, rtol=1e-6, atol=1e-8)
