@@ -445,6 +445,23 @@ def moe_grouped_gemm_up(x_perm: torch.Tensor, x_scales: Optional[torch.Tensor], 
     return h, h_scales
 
 
+def moe_grouped_gemm_down(h: torch.Tensor, h_scales: Optional[torch.Tensor], w: PackedWeights,
+                          group_offsets: torch.Tensor, *, y_perm: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """Down projection y_perm = h W2[e] per group -> y_perm [R_cap, H] bf16."""
+    fp8 = w.precision == "mxfp8"
+    _want(h, "h", torch.uint8 if fp8 else torch.bfloat16, 2)
+    _want(group_offsets, "group_offsets", torch.int32, 1)
+    R_cap = h.shape[0]
+    if y_perm is None:
+        y_perm = torch.empty((R_cap, w.H), dtype=torch.bfloat16, device=h.device)
+    st = _lib.load().moe_grouped_gemm_down(
+        _ptr(h), _ptr(h_scales), _ptr(w.w2), _ptr(w.w2_scales), _dt_code(w.precision), _ptr(group_offsets),
+        w.E, w.H, w.F, R_cap, _ptr(y_perm), _stream(stream))
+    _check("moe_grouped_gemm_down", st)
+    return y_perm
+
+
 # ---------------------------------------------------------------------- NVFP4
 def moe_amax_bf16(x: torch.Tensor, *, valid_rows: Optional[torch.Tensor] = None, amax: Optional[torch.Tensor] = None,
                   stream=None) -> torch.Tensor:

@@ -3,8 +3,10 @@ transposition, wgrad) against the CPU oracle, through the C ABI.
 
 Bar: transposed operands (a data movement, plus MXFP8 codes and scales)
 bit-exact; saved pre-activations, dab, dx and dW within max|err| / max|ref|
-<= 1e-2 (bf16) or 3e-2 (MXFP8). The full heavy-skew shape compares sampled
-rows of dx and sampled columns of dW (all rows of every dW column)."""
+<= 1e-2 (bf16) or 3e-2 (MXFP8). At the full heavy-skew shape the oracle makes
+every operand itself: sampled rows of the forward and of dab / dx, and whole
+experts (every row) at sampled columns of F for a|b, h, dab and the three weight
+gradients."""
 import numpy as np
 import pytest
 import torch
@@ -73,6 +75,7 @@ def _gpu_backward(wl, ids, precision, seed=0):
     ab = torch.empty((R_cap, 2 * wl.F), dtype=torch.bfloat16, device=dev)
     h_bf16 = torch.empty((R_cap, wl.F), dtype=torch.bfloat16, device=dev) if fp8 else None
     h, hs = api.moe_grouped_gemm_up(p.x_perm, p.x_perm_scales, pw, goff, ab=ab, h_bf16=h_bf16)
+    y = api.moe_grouped_gemm_down(h, hs, pw, goff)
     dyd = dy.to(dev)
     if fp8:
         dyq, dys = api.moe_quant_mxfp8_grouped(dyd, goff)
@@ -95,7 +98,7 @@ def _gpu_backward(wl, ids, precision, seed=0):
     dW1, dW3 = api.moe_grouped_gemm_wgrad(xT, xTs, dabT, dabTs, precision, goff, R_cap, split=True)
     torch.cuda.synchronize()
     assert api.moe_get_device_errors() == 0
-    return dict(x=x, w=(w1, w3, w2), dy=dy, ab=ab, h_bf16=h_bf16, h=h, dab=dab, dx=dx, dW1=dW1, dW3=dW3,
+    return dict(x=x, w=(w1, w3, w2), dy=dy, ab=ab, h_bf16=h_bf16, h=h, hs=hs, y=y, dab=dab, dx=dx, dW1=dW1, dW3=dW3,
                 dW2=dW2, T=dict(hT=(hT, hTs), dyT=(dyT, dyTs), xT=(xT, xTs), dabT=(dabT, dabTs)))
 
 
@@ -220,20 +223,42 @@ def test_backward_small_routed(precision):
     _check_small(wl, ids, precision)
 
 
-def test_backward_heavy_sampled():
-    """Full heavy-skew training shape (T=32768, H=7168, E=32, top-8, F=2048, MXFP8):
-    dab and dx on sampled rows, dW2 on sampled output columns of three experts."""
+def _w13_col(f, half):
+    """Packed column of pre-activation column f: a (half 0) or b (half 1), 128-column blocks."""
+    return (f // 128) * 256 + half * 128 + (f % 128)
+
+
+def _chunks(n, size=4096):
+    for i in range(0, n, size):
+        yield i, min(n, i + size)
+
+
+def test_backward_heavy_full_size():
+    """Full heavy-skew training shape (T=32768, H=7168, E=32, top-8, F=2048, MXFP8). Every
+    operand on the oracle side is made by the oracle from the workload's x, W and dy.
+    Sampled rows (16 random plus the first and last row of three experts): the forward's MXFP8
+    h (decoded), its bf16 copy, y_perm and the saved a|b; dab and dx.
+    Whole experts (the smallest, the median and the largest, 350 / 2,897 / 32,708 rows) at 32
+    sampled columns of F: a|b, bf16 h and dab on every row of the expert; dW2 at those rows of
+    dW2 (256 sampled columns of H) and dW1, dW3 at those columns (256 sampled rows of H), the
+    wgrad operands being the oracle's own h, dab, x and dy in group-aware column-wise MXFP8."""
     wl = W.get("heavy")
     lg = W.logits(wl)
     ids, _ = O.route_topk(lg.numpy(), wl.K)
     g = _gpu_backward(wl, ids, "mxfp8")
     x, (w1, w3, w2), dy = g["x"], g["w"], g["dy"]
     op = O.permute(None, ids, wl.E)
-    off = op["group_offsets"]
+    off, src = op["group_offsets"], op["perm_src"]
     sizes = np.diff(off)
     nz = np.nonzero(sizes)[0]
-    experts = sorted({int(nz[np.argmax(sizes[nz])]), int(nz[np.argmin(sizes[nz])]), int(nz[len(nz) // 2])})
+    by_size = nz[np.argsort(sizes[nz], kind="stable")]
+    experts = sorted({int(by_size[0]), int(by_size[len(by_size) // 2]), int(by_size[-1])})
     rng = np.random.default_rng(0)
+    xb = bf16_bits(x)
+    xq, xs = O.quant_rows(xb)                         # MXFP8 x of every token (the permute's rows)
+    f64 = lambda bits: O.bf16_to_f64(bits)
+
+    # ---- sampled rows: the oracle's row functions
     rows = set(int(r) for r in rng.choice(int(off[-1]), 16, replace=False))
     for e in experts:
         rows.update((int(off[e]), int(off[e + 1]) - 1))
@@ -251,34 +276,65 @@ def test_backward_heavy_sampled():
         return O.Operand(O.MAT_MXFP8, q, s)
     Wf = [stack(t, _quant_along_cols_of) for t in (w1, w3, w2)]
     Wb = [stack(t, _quant_along_rows_of) for t in (w1, w3, w2)]
-    src = op["perm_src"][rows]
-    xq, xs = O.quant_rows(bf16_bits(x[torch.from_numpy(src).long()]))
     dyq, dys = O.quant_rows(bf16_bits(dy[torch.from_numpy(rows).long()]))
-    X = O.Operand(O.MAT_MXFP8, _scatter_rows(xq, rows, wl.R_cap), _scatter_rows(xs, rows, wl.R_cap))
+    X = O.Operand(O.MAT_MXFP8, _scatter_rows(xq[src[rows]], rows, wl.R_cap),
+                  _scatter_rows(xs[src[rows]], rows, wl.R_cap))
     DY = O.Operand(O.MAT_MXFP8, _scatter_rows(dyq, rows, wl.R_cap), _scatter_rows(dys, rows, wl.R_cap))
-    fw = O.swiglu_rows(X, *Wf, off, rows, h_mode=O.H_MXFP8, want=("a_f64", "b_f64"))
+    fw = O.swiglu_rows(X, *Wf, off, rows, h_mode=O.H_MXFP8,
+                       want=("a_f64", "b_f64", "h_f64", "h_q", "h_s", "y_bf16"))
+    ridx = torch.from_numpy(rows).long().cuda()
+    assert rel_err(O.mx_decode_rows(u8(g["h"].index_select(0, ridx)), u8(g["hs"].index_select(0, ridx))),
+                   O.mx_decode_rows(fw["h_q"], fw["h_s"])) <= 3e-2
+    assert rel_err(f64(bf16_bits(g["h_bf16"].index_select(0, ridx))), f64(O.f64_to_bf16(fw["h_f64"]))) <= 3e-2
+    assert rel_err(f64(bf16_bits(g["y"].index_select(0, ridx))), f64(fw["y_bf16"])) <= 3e-2
     a16, b16 = O.f64_to_bf16(fw["a_f64"]), O.f64_to_bf16(fw["b_f64"])
     full = lambda v: _scatter_rows(v, rows, wl.R_cap)
     bw = O.swiglu_dgrad_rows(DY, O.Operand(O.MAT_BF16, full(a16)), O.Operand(O.MAT_BF16, full(b16)), *Wb, off,
                              rows, w_blk_rows=0, dab_mode=O.DAB_MXFP8, want=("dx_bf16", "da_f64", "db_f64"))
-    ridx = torch.from_numpy(rows).long().cuda()
-    assert rel_err(O.bf16_to_f64(bf16_bits(g["ab"].index_select(0, ridx))),
-                   O.bf16_to_f64(_interleave(a16, b16))) <= 3e-2
-    got_dab = O.bf16_to_f64(bf16_bits(g["dab"].index_select(0, ridx)))
-    ref_dab = O.bf16_to_f64(_interleave(O.f64_to_bf16(bw["da_f64"]), O.f64_to_bf16(bw["db_f64"])))
+    assert rel_err(f64(bf16_bits(g["ab"].index_select(0, ridx))), f64(_interleave(a16, b16))) <= 3e-2
+    got_dab = f64(bf16_bits(g["dab"].index_select(0, ridx)))
+    ref_dab = f64(_interleave(O.f64_to_bf16(bw["da_f64"]), O.f64_to_bf16(bw["db_f64"])))
     assert rel_err(got_dab, ref_dab) <= 3e-2
-    assert rel_err(O.bf16_to_f64(bf16_bits(g["dx"].index_select(0, ridx))), O.bf16_to_f64(bw["dx_bf16"])) <= 3e-2
-    # dW2 = h^T dy on 8 sampled output columns of three experts; its operands are the GPU
-    # forward's bf16 h (whose rows were checked above through dab) and dy
-    cols = np.sort(rng.choice(wl.H, 8, replace=False)).astype(np.int32)
-    h16 = bf16_bits(g["h_bf16"])
-    hq = O.Operand(O.MAT_MXFP8, *O.quant_cols_grouped(h16, off))
-    dyc = np.ascontiguousarray(bf16_bits(dy)[:, cols])
-    dyqc = O.Operand(O.MAT_MXFP8, *O.quant_cols_grouped(dyc, off))
+    assert rel_err(f64(bf16_bits(g["dx"].index_select(0, ridx))), f64(bw["dx_bf16"])) <= 3e-2
+
+    # ---- whole experts at sampled columns: the oracle's expert-block functions
+    fs = np.sort(rng.choice(wl.F, 32, replace=False))
+    js = np.sort(rng.choice(wl.H, 256, replace=False))     # columns of dW2 [F, H]
+    hr = np.sort(rng.choice(wl.H, 256, replace=False))     # rows of dW1, dW3 [H, F]
+    fs_t, js_t, hr_t = (torch.from_numpy(v).long() for v in (fs, js, hr))
+    ab_cols = torch.tensor([_w13_col(int(f), 0) for f in fs] + [_w13_col(int(f), 1) for f in fs]).cuda()
+    dec = lambda qs: O.mx_decode_rows(*qs)
     for e in experts:
-        ref = O.wgrad_expert(hq, dyqc, off, e)
-        got = O.bf16_to_f64(bf16_bits(g["dW2"][e][:, torch.from_numpy(cols).long().cuda()]))
-        assert rel_err(got, ref) <= 3e-2, (e, rel_err(got, ref))
+        r0, r1 = int(off[e]), int(off[e + 1])
+        m = r1 - r0
+        tok = src[r0:r1]
+        w1c = dec(O.quant_rows(np.ascontiguousarray(bf16_bits(w1[e][:, fs_t]).T))).T    # [H, 32], blocks along H
+        w3c = dec(O.quant_rows(np.ascontiguousarray(bf16_bits(w3[e][:, fs_t]).T))).T
+        w2r = dec(O.quant_rows(bf16_bits(w2[e][fs_t])))                                 # [32, H], blocks along H
+        dyb = bf16_bits(dy[r0:r1])
+        a16, b16, h16, da16, db16 = (np.empty((m, fs.size), np.uint16) for _ in range(5))
+        for c0, c1 in _chunks(m):
+            blk = O.expert_swiglu_block(O.mx_decode_rows(xq[tok[c0:c1]], xs[tok[c0:c1]]), w1c, w3c, h_mode=O.H_BF16)
+            a16[c0:c1], b16[c0:c1], h16[c0:c1] = O.f64_to_bf16(blk["a"]), O.f64_to_bf16(blk["b"]), blk["h_bf16"]
+            da, db = O.expert_swiglu_dgrad_block(dec(O.quant_rows(dyb[c0:c1])), w2r, a16[c0:c1], b16[c0:c1])
+            da16[c0:c1], db16[c0:c1] = O.f64_to_bf16(da), O.f64_to_bf16(db)
+        rr = torch.arange(r0, r1, device="cuda")
+        got_ab = f64(bf16_bits(g["ab"].index_select(0, rr).index_select(1, ab_cols)))
+        assert rel_err(got_ab, f64(np.concatenate([a16, b16], axis=1))) <= 3e-2, e
+        got_h = f64(bf16_bits(g["h_bf16"].index_select(0, rr).index_select(1, fs_t.cuda())))
+        assert rel_err(got_h, f64(h16)) <= 3e-2, e
+        got_dab = f64(bf16_bits(g["dab"].index_select(0, rr).index_select(1, ab_cols)))
+        assert rel_err(got_dab, f64(np.concatenate([da16, db16], axis=1))) <= 3e-2, e
+        one = np.array([0, m], np.int32)
+        col = lambda v: O.Operand(O.MAT_MXFP8, *O.quant_cols_grouped(np.ascontiguousarray(v), one))
+        ref2 = O.wgrad_expert(col(h16), col(dyb[:, js]), one, 0)                           # [32, 256]
+        got2 = f64(bf16_bits(g["dW2"][e].index_select(0, fs_t.cuda()).index_select(1, js_t.cuda())))
+        assert rel_err(got2, ref2) <= 3e-2, (e, rel_err(got2, ref2))
+        xc = col(xb[:, hr][tok])
+        for dW, d16 in ((g["dW1"], da16), (g["dW3"], db16)):
+            ref = O.wgrad_expert(xc, col(d16), one, 0)                                      # [256, 32]
+            got = f64(bf16_bits(dW[e].index_select(0, hr_t.cuda()).index_select(1, fs_t.cuda())))
+            assert rel_err(got, ref) <= 3e-2, (e, rel_err(got, ref))
     assert api.moe_get_device_errors() == 0
 
 

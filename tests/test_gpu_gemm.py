@@ -39,21 +39,27 @@ def _oracle_weight_quant(w):
     return np.ascontiguousarray(np.stack(qs)), np.ascontiguousarray(np.stack(ss))
 
 
-def _sample_rows(off, n_random, seed=0):
+def _sample_rows(off, n_random, seed=0, tile_rows=None):
+    """The first and last row of every group, n_random random rows, and with tile_rows one
+    random row in every tile_rows-row tile of every group (tiles start at each group's first
+    row, as the GEMM's row tiles do)."""
     off = np.asarray(off)
     R = int(off[-1])
     rows = set()
+    g = np.random.default_rng(seed)
     for e in range(off.size - 1):
         if off[e + 1] > off[e]:
             rows.add(int(off[e]))
             rows.add(int(off[e + 1]) - 1)
-    g = np.random.default_rng(seed)
+            if tile_rows:
+                for t0 in range(int(off[e]), int(off[e + 1]), tile_rows):
+                    rows.add(int(g.integers(t0, min(t0 + tile_rows, int(off[e + 1])))))
     if R > 0:
         rows.update(int(r) for r in g.choice(R, size=min(n_random, R), replace=False))
     return np.array(sorted(rows), np.int32)
 
 
-def _run(wl, precision, n_random=None, sizes=None, seed=0):
+def _run(wl, precision, n_random=None, sizes=None, seed=0, tile_rows=None):
     """GPU: route -> permute -> packed weights -> grouped SwiGLU GEMM.
     Oracle: its own route -> permute -> quantisation -> grouped MLP on sampled rows."""
     fp8 = precision == "mxfp8"
@@ -75,7 +81,7 @@ def _run(wl, precision, n_random=None, sizes=None, seed=0):
     y_perm, h, hs = api.moe_grouped_swiglu_gemm(p.x_perm, p.x_perm_scales, pw, p.group_offsets)
     torch.cuda.synchronize()
     assert api.moe_get_device_errors() == 0
-    rows = np.arange(op["R"], dtype=np.int32) if n_random is None else _sample_rows(off, n_random, seed)
+    rows = np.arange(op["R"], dtype=np.int32) if n_random is None else _sample_rows(off, n_random, seed, tile_rows)
     # oracle operands
     if fp8:
         xq, xs = O.quant_rows(bf16_bits(x))
@@ -85,6 +91,19 @@ def _run(wl, precision, n_random=None, sizes=None, seed=0):
         wq = [_oracle_weight_quant(w) for w in (w1, w3, w2)]
         Ws = [O.Operand(O.MAT_MXFP8, q, s) for q, s in wq]
         out = O.swiglu_rows(X, *Ws, off, rows, h_mode=O.H_MXFP8, want=("y_bf16", "h_q", "h_s", "h_f64"))
+    elif rows.size > 64:
+        # many sampled rows of a wide layer: the oracle's expert-block forward, one expert at a time
+        xb = bf16_bits(x)
+        src = op["perm_src"]
+        out = dict(y_bf16=np.zeros((rows.size, wl.H), np.uint16), h_bf16=np.zeros((rows.size, wl.F), np.uint16))
+        ex = np.array([O.expert_of_row(off, int(r)) for r in rows])
+        for e in np.unique(ex):
+            sel = np.nonzero(ex == e)[0]
+            wv = [O.bf16_to_f64(bf16_bits(w[e])) for w in (w1, w3, w2)]
+            blk = O.expert_swiglu_block(O.bf16_to_f64(xb[src[rows[sel]]]), *wv, h_mode=O.H_BF16)
+            out["h_bf16"][sel] = blk["h_bf16"]
+            out["y_bf16"][sel] = O.f64_to_bf16(blk["y"])
+        wq = None
     else:
         xp = np.zeros((wl.R_cap, wl.H), np.uint16)
         xb = bf16_bits(x)
@@ -175,7 +194,15 @@ def test_gemm_bf16_pair_tiles_ragged():
 
 
 def test_gemm_bf16_mixtral_sampled():
-    _check_bf16(_run(W.get("mixtral"), "bf16", n_random=16))
+    """Full Mixtral-like shape: one random row in every 256-row CTA-pair tile of every expert
+    (72 tiles), the first and last row of every group and 16 random rows."""
+    res = _run(W.get("mixtral"), "bf16", n_random=16, tile_rows=256)
+    off = np.asarray(res["off"])
+    tiles = sum(-(-int(off[e + 1] - off[e]) // 256) for e in range(off.size - 1))
+    covered = {(O.expert_of_row(off, int(r)), (int(r) - int(off[O.expert_of_row(off, int(r))])) // 256)
+               for r in res["rows"]}
+    assert len(covered) == tiles
+    _check_bf16(res)
 
 
 def test_gemm_bf16_large_e_sampled():

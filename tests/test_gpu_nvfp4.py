@@ -158,6 +158,74 @@ def test_nvfp4_grouped_gemms_match_oracle(T, H, F, E, K):
     assert rel_err(O.bf16_to_f64(bf16_bits(y)[:R]), y_ref[:R]) <= 3e-2
 
 
+def test_nvfp4_grouped_gemms_full_dsv3_shape_sampled():
+    """The DeepSeek-V3-like NVFP4 layer at full size (T=8192, H=7168, E=32, top-4, F=2048, six
+    empty experts): the permute's amax, codes and scales on sampled rows; h on sampled rows (the
+    first and last row of every non-empty group plus 24 random rows); h's amax against the
+    oracle's over every row (the oracle computes h for all rows, one expert at a time); y_perm on
+    the sampled rows from the oracle's own NVFP4 h."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    wl = W.get("dsv3_nvfp4")
+    x = W.x(wl)
+    w1, w3, w2 = W.weights(wl)
+    ids, _ = O.route_topk(W.logits(wl).numpy(), wl.K, wl.renorm)
+    op = O.permute(bf16_bits(x), ids, wl.E)
+    R, off = op["R"], op["group_offsets"]
+    dev = torch.device("cuda")
+    nw = api.moe_prepare_weights_nvfp4(w1.to(dev), w3.to(dev), w2.to(dev))
+    p, xa = api.moe_permute_nvfp4(x.to(dev), torch.from_numpy(ids).to(dev), wl.E)
+    goff = p.group_offsets
+    h, ha = api.moe_grouped_gemm_up_nvfp4(p.x_perm, p.x_perm_scales, xa, nw, goff)
+    hq, hs = api.moe_quant_nvfp4(h, ha, valid_rows=goff[wl.E:])
+    y = api.moe_grouped_gemm_down_nvfp4(hq, hs, ha, nw, goff)
+    torch.cuda.synchronize()
+    assert api.moe_get_device_errors() == 0
+    rng = np.random.default_rng(5)
+    rows = set(int(r) for r in rng.choice(R, 24, replace=False))
+    for e in range(wl.E):
+        if off[e + 1] > off[e]:
+            rows.update((int(off[e]), int(off[e + 1]) - 1))
+    rows = np.array(sorted(rows), np.int64)
+    ridx = torch.from_numpy(rows).cuda()
+    # x: amax of the routed rows, NVFP4 codes and scales of the sampled rows
+    Sx = O.nvfp4_encode_scale(O.bf16_amax(op["x_perm"][:R]))
+    assert float(xa.item()) == O.bf16_amax(op["x_perm"][:R])
+    rq, rs, _ = O.quant_rows_nvfp4(op["x_perm"][rows], S=Sx)
+    assert np.array_equal(p.x_perm.index_select(0, ridx).cpu().numpy(), rq)
+    assert np.array_equal(p.x_perm_scales.index_select(0, ridx).cpu().numpy(), rs)
+    # weights: one encode scale per stacked tensor, blocks along the contraction dimension
+    b1, b3, b2 = bf16_bits(w1), bf16_bits(w3), bf16_bits(w2)
+    S13 = O.nvfp4_encode_scale(max(O.bf16_amax(b1), O.bf16_amax(b3)))
+    S2 = O.nvfp4_encode_scale(O.bf16_amax(b2))
+    live = [e for e in range(wl.E) if off[e + 1] > off[e]]
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as pool:   # the C oracle is reentrant
+        quant = lambda wb, S: pool.submit(O.quant_rows_nvfp4, np.ascontiguousarray(wb.T), S)
+        w13f = {e: (quant(b1[e], S13), quant(b3[e], S13)) for e in live}
+        ex_rows = {e: rows[(rows >= off[e]) & (rows < off[e + 1])] for e in live}
+        w2f = {e: quant(b2[e], S2) for e in live if ex_rows[e].size}
+        xf = {e: pool.submit(O.quant_rows_nvfp4, op["x_perm"][off[e]:off[e + 1]], Sx) for e in live}
+        dec = lambda fut: O.nvfp4_decode(*fut.result()).T
+        h_amax, h_rows, y_rows = 0.0, {}, {}
+        for e in live:
+            r0, r1 = int(off[e]), int(off[e + 1])
+            xv = O.nvfp4_decode(*xf.pop(e).result())
+            blk = O.expert_swiglu_block(xv, dec(w13f[e][0]), dec(w13f[e][1]), h_mode=O.H_BF16)
+            h_amax = max(h_amax, O.bf16_amax(blk["h_bf16"]))
+            if ex_rows[e].size:
+                h_rows[e] = blk["h_bf16"][ex_rows[e] - r0]
+                y_rows[e] = dec(w2f[e])                          # W2[e] values [F, H]
+    # h on the sampled rows, and its amax over every row
+    h_ref = np.concatenate([h_rows[e] for e in live if e in h_rows])
+    assert rel_err(O.bf16_to_f64(bf16_bits(h.index_select(0, ridx))), O.bf16_to_f64(h_ref)) <= 1e-2
+    assert abs(float(ha.item()) - h_amax) <= 1e-2 * h_amax
+    # y_perm on the sampled rows: the oracle's NVFP4 of its own h (encode scale of its amax)
+    Sh = O.nvfp4_encode_scale(h_amax)
+    y_ref = np.concatenate([O.nvfp4_decode(*O.quant_rows_nvfp4(h_rows[e], S=Sh)) @ y_rows[e]
+                            for e in live if e in h_rows])
+    assert rel_err(O.bf16_to_f64(bf16_bits(y.index_select(0, ridx))), y_ref) <= 3e-2
+
+
 def test_nvfp4_layer_graph_replay_matches_eager():
     from dropless_moe_expert_router_gb300.layer import MoELayer
     wl = W.get("dsv3_nvfp4", T=256, H=512, F=512, E=8)
