@@ -13,6 +13,16 @@
 // One warp per row. Lane l keeps the scores and keys of experts e = 32 i + l (i < NV) in
 // registers; each of the K rounds takes the lanes' best keys and an arg-max across the
 // warp (5 shuffle steps), and the winner's lane retires it. Rows are read once, coalesced.
+//
+// Exact selection. The score is rounded to fp32 once from its double value (a single
+// rounding of the logistic function), so the keys -- and with them the ids -- are those of
+// a reference that rounds the exact score once. Double arithmetic is scarce on this part,
+// so it is spent only where the decision needs it: a first pass ranks fp32 keys from expf
+// (a few ulp from the exact ones) and finds the K-th key tau; every expert whose fp32 key
+// is within a margin of tau (2^-14 max(1, |tau|), far above the fp32 keys' error) is a
+// candidate, and no other expert can be among the K largest exact keys (the K first-pass
+// winners' exact keys all beat every non-candidate's). The candidates -- K, or a few more
+// on near-ties -- get their exact scores, and the second pass ranks them.
 #include "common.cuh"
 
 #include <math.h>
@@ -31,6 +41,41 @@ __device__ __forceinline__ bool key_beats(bool aa, float av, int ai, bool ba, fl
 }
 
 __device__ __forceinline__ float logistic(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// The logistic function evaluated in double and rounded once to fp32.
+__device__ __forceinline__ float logistic_rn(float x) {
+    return __double2float_rn(1.0 / (1.0 + exp(-(double)x)));
+}
+
+// One selection round over the lanes' available slots: the warp-wide winner (largest key,
+// lower expert index on equal keys); bi = 0x7fffffff when no slot is available anywhere.
+template <int NV>
+__device__ __forceinline__ void warp_best(const float (&key)[NV], uint32_t avail, int lane, bool& ba, float& bv,
+                                          int& bi) {
+    ba = false;
+    bv = 0.0f;
+    bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {          // strict comparison over ascending i: lower index on ties
+        const bool a = (avail >> i) & 1u;
+        if (a && (!ba || key[i] > bv)) {
+            ba = true;
+            bv = key[i];
+            bi = i * 32 + lane;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const bool oa = __shfl_xor_sync(FULL, (int)ba, o) != 0;
+        const float ov = __shfl_xor_sync(FULL, bv, o);
+        const int oi = __shfl_xor_sync(FULL, bi, o);
+        if (key_beats(oa, ov, oi, ba, bv, bi)) {
+            ba = oa;
+            bv = ov;
+            bi = oi;
+        }
+    }
+}
 
 __device__ __forceinline__ void store_route_id(void* ids, bool i16, long long i, int id) {
     if (i16) static_cast<int16_t*>(ids)[i] = (int16_t)id;
@@ -66,35 +111,42 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
                 avail |= 1u << i;
             }
         }
+        // first pass on the fp32 keys: the K-th key tau
+        float tau = 0.0f;
+        {
+            uint32_t left = avail;
+            for (int k = 0; k < K; k++) {
+                bool ba;
+                float bv;
+                int bi;
+                warp_best<NV>(key, left, lane, ba, bv, bi);
+                tau = bv;
+                if (lane == (bi & 31)) left &= ~(1u << (bi >> 5));
+            }
+        }
+        // candidates: fp32 keys within the margin of tau, given their exactly rounded scores
+        const float margin = fmaxf(1.0f, fabsf(tau)) * (1.0f / 16384.0f);
+        const bool all_cand = !isfinite(tau);
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            if (!((avail >> i) & 1u)) continue;
+            if (all_cand || key[i] >= tau - margin) {
+                s[i] = logistic_rn(__ldg(l + i * 32 + lane));
+                key[i] = __fadd_rn(s[i], b[i]);
+            } else {
+                avail &= ~(1u << i);
+            }
+        }
         float out_s0 = 0.0f, out_s1 = 0.0f;
         int out_e0 = 0, out_e1 = 0;
         float Z = 0.0f;
-        for (int k = 0; k < K; k++) {
-            // this lane's best: strict comparison over ascending i keeps the lower index on ties
-            bool ba = false;
-            float bv = 0.0f;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < NV; i++) {
-                const bool a = (avail >> i) & 1u;
-                if (a && (!ba || key[i] > bv)) {
-                    ba = true;
-                    bv = key[i];
-                    bi = i * 32 + lane;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const bool oa = __shfl_xor_sync(FULL, (int)ba, o) != 0;
-                const float ov = __shfl_xor_sync(FULL, bv, o);
-                const int oi = __shfl_xor_sync(FULL, bi, o);
-                if (key_beats(oa, ov, oi, ba, bv, bi)) {
-                    ba = oa;
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            // K <= E, so a winner always exists; its lane retires it and hands over its score
+        for (int k = 0; k < K; k++) {       // second pass: the candidates' exact keys
+            bool ba;
+            float bv;
+            int bi;
+            warp_best<NV>(key, avail, lane, ba, bv, bi);
+            // at least K candidates, so a winner always exists; its lane retires it and hands
+            // over its score
             const int slot = bi >> 5;
             float mine = 0.0f;
 #pragma unroll
