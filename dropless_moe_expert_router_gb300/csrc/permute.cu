@@ -578,24 +578,36 @@ extern "C" size_t moe_permute_workspace_size(int T, int K, int E) {
     return align16((size_t)E * (size_t)(tiles > 0 ? tiles : 1) * sizeof(int)) + 16;
 }
 
+// The permute's argument checks other than the workspace's (shapes, dtypes, pointers,
+// alignment), in the order every permute entry point reports them.
+static moe_status permute_check_args(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K,
+                                     int E, const void* x_perm, const uint8_t* x_perm_scales,
+                                     const int32_t* group_sizes, const int32_t* group_offsets,
+                                     const int32_t* row_map, const int32_t* perm_src, bool fuse) {
+    if (T < 0 || H < 32 || (H % 32) != 0 || K < 1 || E < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
+    if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !ids || !x_perm || !row_map || !perm_src)) return MOE_ERR_INVALID_ARG;
+    if (fuse && T > 0 && !x_perm_scales) return MOE_ERR_INVALID_ARG;
+    if ((long long)E * 4 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    if (!moe_host::aligned(x, 16) || !moe_host::aligned(x_perm, fuse ? 8 : 16) || !moe_host::aligned(row_map, 4) ||
+        !moe_host::aligned(perm_src, 4) || !moe_host::aligned(group_sizes, 4) ||
+        !moe_host::aligned(group_offsets, 4))
+        return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
 // fuse_mode: 0 bf16 rows, 1 MXFP8, 2 NVFP4 (with the device amax already computed on the stream)
 static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe_dtype id_dtype, int K, int E,
                                void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes, int32_t* group_offsets,
                                int32_t* row_map, int32_t* perm_src, int fuse_mode, const float* amax,
                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     using namespace moe;
-    if (T < 0 || H < 32 || (H % 32) != 0 || K < 1 || E < 1 || K > E || K > 128) return MOE_ERR_INVALID_ARG;
-    if (id_dtype != MOE_I16 && id_dtype != MOE_I32) return MOE_ERR_INVALID_ARG;
-    const bool fuse = fuse_mode != 0;
-    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!x || !ids || !x_perm || !row_map || !perm_src)) return MOE_ERR_INVALID_ARG;
-    if (fuse && T > 0 && !x_perm_scales) return MOE_ERR_INVALID_ARG;
-    if ((long long)E * 4 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    const moe_status arg = permute_check_args(x, T, H, ids, id_dtype, K, E, x_perm, x_perm_scales, group_sizes,
+                                              group_offsets, row_map, perm_src, fuse_mode != 0);
+    if (arg != MOE_OK) return arg;
     if (!workspace || workspace_bytes < moe_permute_workspace_size(T, K, E)) return MOE_ERR_WORKSPACE;
-    if (!moe_host::aligned(x, 16) || !moe_host::aligned(x_perm, fuse ? 8 : 16) ||
-        !moe_host::aligned(workspace, 16) || !moe_host::aligned(row_map, 4) || !moe_host::aligned(perm_src, 4) ||
-        !moe_host::aligned(group_sizes, 4) || !moe_host::aligned(group_offsets, 4))
-        return MOE_ERR_ALIGNMENT;
+    if (!moe_host::aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
     cudaStream_t s = moe_host::as_stream(stream);
     const bool i16 = id_dtype == MOE_I16;
     const int TT = tile_tokens(E);
@@ -737,31 +749,21 @@ extern "C" moe_status moe_quant_mxfp8_grouped(const void* x, int R_cap, int H, c
 // workspace. Every GPU that loads the library holds the array until the process
 // exits; all calls on a device share it.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace moe {
 namespace {
 
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)4 << 20;  // 4 MiB
 static __device__ __align__(256) uint8_t g_permute_scratch[NOALLOC_SCRATCH_BYTES];
 
-constexpr int NOALLOC_MAX_DEVICES = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
-
-// Device address of g_permute_scratch on the current device. Host code cannot use
-// the array's name as a device address; the runtime resolves it once per device.
+// Device address of g_permute_scratch on the current device. Host code cannot use the
+// array's name as a device address; the runtime gives it per device. It is asked on every
+// call (a lookup once the module is loaded), so no address outlives a device reset or a
+// context teardown. The first call on a device may load the module: make it before any
+// stream capture.
 moe_status noalloc_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    *out = p;
     return MOE_OK;
 }
 
@@ -774,9 +776,11 @@ extern "C" moe_status moe_permute_noalloc(const void* x, int T, int H, const voi
                                           int E, void* x_perm, uint8_t* x_perm_scales, int32_t* group_sizes,
                                           int32_t* group_offsets, int32_t* row_map, int32_t* perm_src,
                                           unsigned flags, moe_stream_t stream) {
-    const size_t need = moe_permute_workspace_size(T, K, E);
-    if (need == 0) return MOE_ERR_INVALID_ARG;
-    if (need > moe::NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+    if (flags & ~MOE_PERMUTE_FUSE_MXFP8) return MOE_ERR_INVALID_ARG;
+    const moe_status arg = permute_check_args(x, T, H, ids, id_dtype, K, E, x_perm, x_perm_scales, group_sizes,
+                                              group_offsets, row_map, perm_src, (flags & MOE_PERMUTE_FUSE_MXFP8) != 0);
+    if (arg != MOE_OK) return arg;
+    if (moe_permute_workspace_size(T, K, E) > moe::NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
     void* scratch = nullptr;
     moe_status st = moe::noalloc_scratch(&scratch);
     if (st != MOE_OK) return st;

@@ -206,11 +206,14 @@ moe_status moe_permute(const void *x, int T, int H,
  * as moe_permute minus the workspace and allocates nothing: its scratch is a
  * static device array of moe_permute_noalloc_max_scratch() bytes (4 MiB),
  * held by every GPU that loads the library until the process exits.
- *  - It returns MOE_ERR_WORKSPACE, without enqueuing anything, when
- *    moe_permute_workspace_size(T, K, E) exceeds that maximum.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, once per device, with that device current); make
- *    that first call before any stream capture.
+ *  - Its argument checks (shapes, dtypes, null pointers, alignment) come first
+ *    and report what moe_permute reports; then it returns MOE_ERR_WORKSPACE,
+ *    without enqueuing anything, when moe_permute_workspace_size(T, K, E)
+ *    exceeds that maximum.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so no address outlives a device reset. The first
+ *    call on a device may load the library's device code: make that first call
+ *    before any stream capture.
  *  - All calls on a device share the one array, and it keeps the last call's
  *    contents (nothing in it needs to start at zero: each call rewrites what it
  *    reads). Calls that overlap on the GPU (other streams, or other host threads

@@ -57,10 +57,20 @@ def test_noalloc_permute_matches_workspace_permute_on_consecutive_calls():
 
 
 def test_noalloc_permute_rejects_problems_beyond_its_scratch():
+    """A problem whose count table exceeds the static scratch gets MOE_ERR_WORKSPACE before
+    anything is enqueued (the small buffers passed are never touched); argument errors are
+    reported first, as moe_permute reports them."""
     cap = api.moe_permute_noalloc_max_scratch()
-    T, K, E = 1 << 20, 2, 8192                   # needs E * T/32 * 4 bytes of table
+    T, H, K, E = 1 << 20, 64, 2, 8192                   # needs E * T/32 * 4 bytes of table
     assert api.moe_permute_workspace_size(T, K, E) > cap
     from dropless_moe_expert_router_gb300 import _lib
-    st = _lib.load().moe_permute_noalloc(None, T, 64, None, 1, K, E, None, None, None, None, None, None, 0,
-                                         None)
+    buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")       # stands for every buffer
+    ints = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    p = buf.data_ptr()
+    L = _lib.load()
+    st = L.moe_permute_noalloc(p, T, H, p, 1, K, E, p, None, ints.data_ptr(), ints.data_ptr(), p, p, 0, None)
     assert st == 3   # MOE_ERR_WORKSPACE, nothing enqueued
+    st = L.moe_permute_noalloc(p, T, H, p, 1, K, E, None, None, ints.data_ptr(), ints.data_ptr(), p, p, 0, None)
+    assert st == 1   # MOE_ERR_INVALID_ARG: the null x_perm is reported before the size
+    torch.cuda.synchronize()
+    assert not buf.any() and not ints.any()
