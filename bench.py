@@ -8,9 +8,13 @@ A step is one forward pass of the whole layer over one batch of T tokens of
 the workload (default: Mixtral-like, T=8192, H=4096, E=8, top-2, F=14336, bf16,
 synthetic seeded inputs); for the training workload (heavy skew) it is the
 forward and the whole layer's backward from the gradient of its output
-(combine, expert-MLP dgrad/dx/wgrad, permute and router backward). Each rank runs the same layer on its own batch
-(replicas: weak scaling, no collective on the data path). Rank 0 prints one
-JSON line:
+(combine, expert-MLP dgrad/dx/wgrad, permute and router backward). For the
+2,304-expert workload the permute, GEMMs and combine consume compact routes
+with about 2 % of entries -1 (the router's output, masked once before timing;
+the router still runs every step). Each rank runs the same layer on its own
+batch (replicas: weak scaling, no collective on the data path); --gpus N
+without a launcher starts the N ranks itself (torch's launcher, one process
+per GPU). Rank 0 prints one JSON line:
 
   value      tokens/s over all ranks, inputs resident in HBM; the step (every
              kernel of it) captured once as a CUDA graph -- the path is
@@ -28,10 +32,17 @@ JSON line:
              from CUDA events recorded inside the captured graph between stages
              (external event nodes, read after each replay); where the CUDA
              runtime cannot be loaded for that, from the same steps run eagerly;
+  workloads  the other workloads (DeepSeek-V3-like MXFP8, 2,304 experts, heavy-skew
+             training step, NVFP4, sigmoid router), timed the same way after the
+             headline one: step time, tokens/s, per-stage rates and their
+             dominant kernel's roofline;
   cpu_baseline  the CPU oracle (single-threaded C) timed on this host on a
-             bounded sample of the same workload (rank 0, N=1 only).
+             bounded sample of the same workload (rank 0, N=1 only), with the
+             host's core count beside the one thread it uses.
 
---impl reference times that oracle alone as the reference arm.
+--impl reference times that oracle alone as the reference arm (ms_per_step: the
+wall time of each timed sample; value: the whole batch over the extrapolated
+step time).
 """
 from __future__ import annotations
 
@@ -54,17 +65,19 @@ KERNEL_NAMES = {"gemm_up": "grouped_gemm_kernel<UP> (GEMM up + SwiGLU)",
                 "dgrad_dh": "grouped_gemm_kernel<DGRAD> (dh + SwiGLU backward)"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from an ncu capture,
-# keyed by the hash of the kernel's sources; a changed kernel reports null.
+# DRAM bytes (read + write) per launch of a workload's dominant kernel, from an ncu capture,
+# keyed by (workload, stage, hash of the GEMM's sources); a changed kernel reports null.
 TRAFFIC_BY_SOURCE = {
-    # Mixtral-like GEMM up: 2.406 GB read + 0.462 GB written (ncu dram__bytes_read.sum / _write.sum, full size)
-    "763ec371780ded6f": 2.406117632e9 + 0.46172416e9,
+    # Mixtral-like GEMM up: 2.406 GB read + 0.462 GB written (ncu dram__bytes_read.sum / _write.sum,
+    # full size, one pass)
+    ("mixtral", "gemm_up", "0ce0a4a81f5de628"): 2.406117632e9 + 0.46172416e9,
 }
 
 
 def kernel_source_hash() -> str:
+    """Hash of the grouped GEMM's own sources (the kernel file and its PTX wrappers)."""
     h = hashlib.sha1()
-    for f in ("gemm.cu", "sm100_ptx.cuh", "common.cuh"):
+    for f in ("gemm.cu", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "dropless_moe_expert_router_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -226,7 +239,7 @@ def oracle_inputs(wl):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, wl, rank, world, local_rank):
+def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
     import torch
     import torch.distributed as dist
     from dropless_moe_expert_router_gb300 import api
@@ -247,7 +260,21 @@ def run_ours(args, wl, rank, world, local_rank):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    stages = [("route", lambda: layer.stage_route(logits)), ("permute", lambda: layer.stage_permute(x)),
+    route = lambda: layer.stage_route(logits)
+    if wl.invalid_frac > 0:
+        # compact routes with invalid entries (the 2,304-expert workload: about 2 % of the [T, K]
+        # ids are -1): the router's output with the workload's mask applied once, before timing,
+        # is what the permute, the GEMMs and the combine consume in every step; the router still
+        # runs in every step, into buffers of its own
+        layer.stage_route(logits)
+        mask = W.invalid_mask(wl, seed=rank).to(dev)
+        route_ids, route_probs = layer.ids.clone(), layer.probs.clone()
+        layer.ids.masked_fill_(mask, -1)
+        layer.probs.masked_fill_(mask, 0.0)
+        torch.cuda.synchronize()
+        route = lambda: api.moe_route_topk(logits, wl.K, renorm=wl.renorm, id_dtype=route_ids.dtype, ids=route_ids,
+                                           probs=route_probs)
+    stages = [("route", route), ("permute", lambda: layer.stage_permute(x)),
               ("gemm_up", layer.stage_gemm_up), ("gemm_down", layer.stage_gemm_down),
               ("combine", layer.stage_combine)]
     if layer.nv4:
@@ -343,25 +370,34 @@ def run_ours(args, wl, rank, world, local_rank):
     y_host = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
 
     def e2e_step():
+        if wl.invalid_frac > 0:
+            # the routes keep their invalid entries: the same stages between the host copies
+            x.copy_(x_host, non_blocking=True)
+            logits.copy_(lg_host, non_blocking=True)
+            step()
+            y_host.copy_(layer.y, non_blocking=True)
+            return
         layer.forward_host(x_host, lg_host, y_host)
         if wl.backward:
             layer.backward_full(layer.x_dev, layer.logits_dev, dy)
 
-    for _ in range(max(2, args.warmup // 2)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        e2e_step()
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    if with_e2e:
+        for _ in range(max(2, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            e2e_ev[i][0].record(stream)
+            e2e_step()
+            e2e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     clocks = sampler.stop()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
     errs = api.moe_get_device_errors()
     R = int(layer.perm.group_offsets[-1].item())
     active = int((layer.perm.group_sizes > 0).sum().item())      # experts that received routes
@@ -432,6 +468,116 @@ def stage_report(wl, R, stage_ms, active=None):
     return out, flops, bytes_
 
 
+# the other workloads the default run times beside the headline one, each graph-replayed
+EXTRA_WORKLOADS = ("dsv3", "large_e", "heavy", "dsv3_nvfp4", "dsv3_sigmoid")
+
+
+def roofline(wl, r, peaks, peak_kind):
+    """The dominant kernel of a timed workload (the GEMM stage with the largest time; one launch
+    per stage) against whichever peak its algorithmic work needs longer for."""
+    stages, flops, gbytes = stage_report(wl, r["R"], r["stage_ms"], r["active"])
+    dom = max((n for n in flops if n in r["stage_ms"] and n != "wgrad_gemm" and n != "dgrad_dx"),
+              key=lambda n: r["stage_ms"][n])
+    # dense peak of the GEMMs' operand type: the measured bf16 peak times the nominal ratio
+    # (MXFP8 2x, NVFP4 6x: 4.5 and 13.5 against 2.25 PFLOP/s dense)
+    fp8_ratio = {"mxfp8": 2.0, "nvfp4": 6.0}.get(wl.precision, 1.0)
+    # The timed loop is well under a second and the SM clock stays at its maximum
+    # (see "clocks"), the conditions of the burst measurement: report against the
+    # burst peak, and the sustained figure beside it.
+    peak = peaks["bf16_tflops"] * fp8_ratio
+    peak_sustained = peaks["bf16_tflops_sustained"] * fp8_ratio
+    hbm_bound = gbytes[dom] / (peaks["hbm_gbs"] * 1e9) > flops[dom] / (peak * 1e12)
+    if hbm_bound:
+        achieved = gbytes[dom] / (r["stage_ms"][dom] * 1e-3) / 1e9
+        peak, peak_sustained = peaks["hbm_gbs"], peaks["hbm_gbs"]
+    else:
+        achieved = flops[dom] / (r["stage_ms"][dom] * 1e-3) / 1e12
+    traffic = TRAFFIC_BY_SOURCE.get((wl.name, dom, kernel_source_hash()))
+    return stages, {
+        "kernel": KERNEL_NAMES[dom], "bound": "hbm" if hbm_bound else "tensor",
+        "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "frac": round(achieved / peak, 4), "traffic": traffic,
+        "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
+                        f"{peak_kind} dense bf16 burst" + ({2.0: " x2 (fp8)", 6.0: " x6 (fp4)"}.get(fp8_ratio, ""))),
+        "frac_of_sustained": round(achieved / peak_sustained, 4)}
+
+
+def workload_config(wl, gpus):
+    return {"workload": f"{wl.name}: T={wl.T} H={wl.H} E={wl.E} top-{wl.K} F={wl.F} {wl.precision}"
+                        + (f", {wl.invalid_frac:.0%} invalid routes" if wl.invalid_frac > 0 else "")
+                        + (", forward + backward" if wl.backward else "")
+                        + (", sigmoid router" if wl.score == "sigmoid" else ""),
+            "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "F": wl.F, "precision": wl.precision,
+            "tokens_per_step_per_gpu": wl.T, "l2": "flushed before every timed step (512 MiB write)",
+            "parallelism": f"replicas x{gpus}"}
+
+
+def host_cores():
+    """Cores of this host and those this process may run on."""
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except Exception:
+        aff = os.cpu_count()
+    return {"host_cores": os.cpu_count(), "affinity_cores": aff}
+
+
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n: int) -> int:
+    """Run this command as n ranks on this node (one process per GPU) through torch's launcher,
+    rendezvous on 127.0.0.1; returns the launcher's exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
+def selftest_launch(rank, world):
+    """--selftest-launch: the rank plumbing alone, on the CPU (gloo): every rank reports a timing
+    that depends on its rank; rank 0 prints the world size and the max over ranks."""
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    got = reduce_max_over_ranks([10.0 + rank, 50.0 - rank], "cpu")
+    dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps({"selftest": "launch", "world": world, "max_ms": got}))
+    return 0
+
+
+def reference_arm(args, wl, world):
+    """The reference arm: the CPU oracle as it stands, each step a bounded sample of the workload
+    (its grouped MLP on a few rows, extrapolated by row count to the whole batch)."""
+    xb, lg, yb, wb = oracle_inputs(wl)
+    rows_per_step = max(1, args.cpu_rows // 6)
+    for _ in range(args.warmup):
+        oracle_sample(wl, xb, lg, yb, 1, wb)
+    est, wall = [], []
+    desc = ""
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        t, desc = oracle_sample(wl, xb, lg, yb, rows_per_step, wb)
+        wall.append(time.perf_counter() - t0)
+        est.append(t)
+    value = wl.T * args.steps / sum(est)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            # the wall time of each timed sample; the whole batch's step, extrapolated, beside it
+            "ms_per_step": sum(wall) / args.steps * 1e3,
+            "ms_per_step_extrapolated": sum(est) / args.steps * 1e3,
+            "timing": "value = whole-batch tokens / extrapolated step time; ms_per_step = wall time of the timed "
+                      "sample (router, permute and combine over every token, the grouped MLP on "
+                      f"{rows_per_step} rows)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl, world),
+            "cpu_baseline": dict({"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                  "sample": desc + " (per step)"}, **host_cores()),
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,46 +585,36 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="other workloads timed beside the headline one ('' for none)")
     ap.add_argument("--cpu-rows", type=int, default=24, help="grouped-MLP rows of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--selftest-launch", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(args.gpus)                  # one process per GPU, launched here
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
+    if args.selftest_launch:
+        return selftest_launch(rank, world)
 
     from dropless_moe_expert_router_gb300 import workloads as W
     wl = W.get(args.workload)
-    config = {"workload": f"{wl.name}: T={wl.T} H={wl.H} E={wl.E} top-{wl.K} F={wl.F} {wl.precision}",
-              "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "F": wl.F, "precision": wl.precision,
-              "tokens_per_step_per_gpu": wl.T, "l2": "flushed before every timed step (512 MiB write)",
-              "parallelism": f"replicas x{args.gpus}"}
+    config = workload_config(wl, world)
 
     if args.impl == "reference":
         if rank != 0:
             return 0
-        import numpy as np  # noqa: F401
-        xb, lg, yb, wb = oracle_inputs(wl)
-        rows_per_step = max(1, args.cpu_rows // 6)
-        for _ in range(args.warmup):
-            oracle_sample(wl, xb, lg, yb, 1, wb)
-        times = []
-        desc = ""
-        for _ in range(args.steps):
-            t, desc = oracle_sample(wl, xb, lg, yb, rows_per_step, wb)
-            times.append(t)
-        tot = sum(times)
-        value = wl.T * args.steps / tot
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                 "sample": desc + " (per step)"},
-                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        print(json.dumps(reference_arm(args, wl, world)))
         return 0
 
     import torch
@@ -490,26 +626,20 @@ def main():
 
     r = run_ours(args, wl, rank, world, local_rank)
     peaks, peak_kind = load_peaks()
-    stages, flops, gbytes = stage_report(wl, r["R"], r["stage_ms"], r["active"])
-    # dominant kernel: the GEMM stage with the largest time (one kernel launch per stage)
-    dom = max((n for n in flops if n in r["stage_ms"] and n != "wgrad_gemm" and n != "dgrad_dx"),
-              key=lambda n: r["stage_ms"][n])
-    # dense peak of the GEMMs' operand type: the measured bf16 peak times the nominal ratio
-    # (MXFP8 2x, NVFP4 6x: 4.5 and 13.5 against 2.25 PFLOP/s dense)
-    fp8_ratio = {"mxfp8": 2.0, "nvfp4": 6.0}.get(wl.precision, 1.0)
-    # The timed loop is well under a second and the SM clock stays at its maximum
-    # (see "clocks"), the conditions of the burst measurement: report against the
-    # burst peak, and the sustained figure beside it.
-    peak = peaks["bf16_tflops"] * fp8_ratio
-    peak_sustained = peaks["bf16_tflops_sustained"] * fp8_ratio
-    # the bound is whichever peak the algorithmic work needs longer for: tensor (FLOPs) or HBM (bytes)
-    hbm_bound = gbytes[dom] / (peaks["hbm_gbs"] * 1e9) > flops[dom] / (peak * 1e12)
-    if hbm_bound:
-        achieved = gbytes[dom] / (r["stage_ms"][dom] * 1e-3) / 1e9
-        peak, peak_sustained = peaks["hbm_gbs"], peaks["hbm_gbs"]
-    else:
-        achieved = flops[dom] / (r["stage_ms"][dom] * 1e-3) / 1e12
-    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_hash()) if (wl.name == "mixtral" and dom == "gemm_up") else None
+    stages, roof = roofline(wl, r, peaks, peak_kind)
+    extras = {}
+    for name in [n for n in args.extra.split(",") if n and n != wl.name] if args.workload == "mixtral" else []:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        xw = W.get(name)
+        rx = run_ours(args, xw, rank, world, local_rank, with_e2e=False)
+        st_x, roof_x = roofline(xw, rx, peaks, peak_kind)
+        extras[name] = {"config": workload_config(xw, world)["workload"],
+                        "value": whole_job_tokens_per_s(world, xw.T, args.steps, rx["total_ms"]),
+                        "unit": "tokens/s", "ms_per_step": rx["total_ms"] / args.steps,
+                        "gpu_launches": rx["launches"], "routes": rx["R"], "roofline": roof_x, "stages": st_x,
+                        "clocks": rx["clocks"], "device_errors": rx["errs"]}
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -522,29 +652,25 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": wl.precision, "data": "synthetic", "config": config,
         "e2e": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": r["launches"],
-        "roofline": {"kernel": KERNEL_NAMES[dom], "bound": "hbm" if hbm_bound else "tensor",
-                     "achieved": round(achieved, 1),
-                     "peak": round(peak, 1), "unit": "GB/s" if hbm_bound else "TFLOP/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": traffic,
-                     "peak_source": (f"{peak_kind} HBM copy bandwidth" if hbm_bound else
-                                     f"{peak_kind} dense bf16 burst" + ({2.0: " x2 (fp8)", 6.0: " x6 (fp4)"}
-                                                                        .get(fp8_ratio, ""))),
-                     "frac_of_sustained": round(achieved / peak_sustained, 4)},
+        "gpu_launches": r["launches"] + sum(v["gpu_launches"] for v in extras.values()),
+        "roofline": roof,
         "timing": "step = CUDA-graph replay of the whole step, CUDA events around each replay"
                   + (f" (first to last stage inside the replay: {r['inner_ms']:.4f} ms)" if r["inner_ms"] else "")
-                  + f"; stages = {r['stage_source']}; e2e = the eager host-buffer call",
+                  + f"; stages = {r['stage_source']}; e2e = the eager host-buffer call"
+                  + ("; workloads = the other workloads, timed the same way after the headline one"
+                     if extras else ""),
         "stages": stages,
         "routes": r["R"],
         "clocks": r["clocks"],
         "device_errors": r["errs"],
     }
+    if extras:
+        line["workloads"] = extras
     if world == 1 and not args.no_cpu_baseline:
         xb, lg, yb, wb = oracle_inputs(wl)
         t, desc = oracle_sample(wl, xb, lg, yb, args.cpu_rows, wb)
-        line["cpu_baseline"] = {"value": wl.T / t, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = dict({"value": wl.T / t, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                     "sample": desc}, **host_cores())
     print(json.dumps(line))
     return 0
 

@@ -32,16 +32,38 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference"
     assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["host_cores"] == os.cpu_count() and d["cpu_baseline"]["affinity_cores"] >= 1
+    # ms_per_step is the timed sample's wall time; the whole batch's step is extrapolated beside it
+    assert 0 < d["ms_per_step"] and d["ms_per_step_extrapolated"] > 0
+    assert d["value"] == pytest.approx(256 / (d["ms_per_step_extrapolated"] / 1e3), rel=1e-9)
+    assert d["n_gpus"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"].startswith("tiny")
     assert d["steps"] == 2 and d["warmup"] == 3
 
 
 def test_reference_arm_other_ranks_exit_quietly():
-    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"],
+    r = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3", "--gpus", "2"],
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_gpus_n_launches_n_ranks_itself():
+    """Without a launcher, --gpus 2 starts two ranks (torch's launcher, rendezvous on 127.0.0.1);
+    the ranks' timings are reduced with a max over gloo and rank 0 alone prints."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--selftest-launch"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert lines == [{"selftest": "launch", "world": 2, "max_ms": [11.0, 50.0]}]
+
+
+def test_gpus_disagreeing_with_world_size_is_an_error():
+    r = _run_bench(["--gpus", "2", "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+                   {"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"})
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
 
 
 def test_warmup_below_three_is_rejected():
