@@ -108,6 +108,8 @@ def lib():
             L.oracle_swiglu_grad_n.argtypes = [P, P, P, i64, P, P]
             L.oracle_quant_rows_f64.restype = None
             L.oracle_quant_rows_f64.argtypes = [P, i64, i64, P, P]
+            L.oracle_ep_recv_expert_ids.restype = None
+            L.oracle_ep_recv_expert_ids.argtypes = [P, i32, i32, i64, P]
             _lib = L
     return _lib
 
@@ -510,3 +512,15 @@ def expert_swiglu_dgrad_block(dyv, w2v_rows, a_bf16, b_bf16):
     Returns (da, db) unrounded, float64."""
     dh = np.asarray(dyv) @ np.asarray(w2v_rows).T
     return swiglu_grad(dh, bf16_to_f64(a_bf16), bf16_to_f64(b_bf16))
+
+
+# ------------------------------------------------------ expert parallelism
+def ep_recv_expert_ids(counts, R_cap: int):
+    """Local expert (int32) of each row a rank receives in the expert-parallel dispatch:
+    counts [G, E_loc] = rows from source s for local expert j, received source by source and
+    expert by expert; rows past them -> -1."""
+    c = _c(counts, np.int32)
+    G, E_loc = c.shape
+    ids = np.empty(int(R_cap), np.int32)
+    lib().oracle_ep_recv_expert_ids(_p(c), G, E_loc, int(R_cap), _p(ids))
+    return ids

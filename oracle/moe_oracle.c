@@ -1073,3 +1073,32 @@ void oracle_quant_rows_f64(const double *x, long rows, long cols, uint8_t *q, ui
             s[r * (cols / 32) + b] =
                 (uint8_t)quant_block(x + r * cols + b * 32, 1, 32, q + r * cols + b * 32, 1);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Expert parallelism: the receiving side's expert of each received row      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Expert-parallel dispatch ([TEJAX] "Optimization 2: Expert parallelism to
+ * fuse Dispatch and Combine"; [SPARSER] "Remove work that has no selected
+ * route": only the selected routes travel, each destination receives the rows
+ * of its own experts). With G ranks and E_loc experts per rank, rank g owning
+ * experts g*E_loc .. g*E_loc + E_loc - 1, every source rank sends the rows of
+ * its expert-contiguous permuted order that belong to the destination's
+ * experts; the destination receives them source rank by source rank, and
+ * within a source expert by expert, in the source's order.
+ * counts[s][j] = rows received from source s for local expert j. Received row
+ * r belongs to local expert j of the segment (s, j) that contains it (the
+ * segments laid end to end in that order); rows past the last segment, up to
+ * R_cap, get -1 (no route).
+ */
+void oracle_ep_recv_expert_ids(const int32_t *counts, int G, int E_loc, long R_cap, int32_t *ids)
+{
+    long r = 0;
+    for (int s = 0; s < G; s++)
+        for (int j = 0; j < E_loc; j++)
+            for (long i = 0; i < counts[(long)s * E_loc + j] && r < R_cap; i++)
+                ids[r++] = j;
+    for (; r < R_cap; r++)
+        ids[r] = -1;
+}
