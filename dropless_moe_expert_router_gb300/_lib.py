@@ -52,6 +52,7 @@ SIGNATURES = {
     "moe_status_string": (C.c_char_p, [I]),
     "moe_route_ids_bytes": (SZ, [I, I, I]),
     "moe_route_probs_bytes": (SZ, [I, I]),
+    "moe_ep_recv_expert_ids": (I, [P, I, I, LL, P, P]),
 }
 
 

@@ -339,6 +339,21 @@ def moe_permute_backward(dx_perm: torch.Tensor, row_map: torch.Tensor, *, dx: Op
     return dx
 
 
+# -------------------------------------------------------------------- expert parallelism
+def moe_ep_recv_expert_ids(recv_counts: torch.Tensor, R_cap: int, *, ids: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """recv_counts [G, E_loc] int32 (rows received from each source for each local expert, on the
+    device) -> ids [R_cap] int32: the local expert of each received row, -1 past them."""
+    _want(recv_counts, "recv_counts", torch.int32, 2)
+    G, E_loc = recv_counts.shape
+    if ids is None:
+        ids = torch.empty((R_cap,), dtype=torch.int32, device=recv_counts.device)
+    _want(ids, "ids", torch.int32, 1)
+    st = _lib.load().moe_ep_recv_expert_ids(_ptr(recv_counts), G, E_loc, R_cap, _ptr(ids), _stream(stream))
+    _check("moe_ep_recv_expert_ids", st)
+    return ids
+
+
 # -------------------------------------------------------------------- errors
 def moe_get_device_errors(clear: bool = True) -> int:
     v = C.c_uint32(0)

@@ -230,6 +230,28 @@ moe_status moe_permute_noalloc(const void *x, int T, int H,
                                unsigned flags, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Expert-parallel dispatch metadata ([TEJAX] "Optimization 2: Expert
+ * parallelism to fuse Dispatch and Combine"; [SPARSER] "Remove work that has
+ * no selected route": only selected routes travel, each destination receives
+ * the rows of its own experts).
+ *
+ * G ranks, E_loc experts per rank (rank g owns experts g*E_loc ..
+ * g*E_loc + E_loc - 1). Every source rank sends, from its moe_permute order,
+ * the rows of the destination's experts (they are contiguous there); the
+ * destination receives them source by source and, within a source, expert by
+ * expert. recv_counts [G][E_loc] int32 (device): rows received from source s
+ * for local expert j (the exchanged group sizes). Writes ids [R_cap] int32
+ * (device): the local expert of each received row r, i.e. j of the segment
+ * (s, j) that holds r when the segments are laid end to end in that order;
+ * rows past the last segment get -1. moe_permute of the received rows with
+ * these ids (K = 1, E = E_loc) gives the local experts' contiguous order.
+ * Requires G * E_loc <= 4096; a negative count is read as 0 and sets
+ * MOE_DEVERR_BAD_ID. Enqueues one kernel; the host never reads the counts.
+ * ------------------------------------------------------------------------ */
+moe_status moe_ep_recv_expert_ids(const int32_t *recv_counts, int G, int E_loc,
+                                  long long R_cap, int32_t *ids, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Group-aware MXFP8 quantisation ([TEJAX] "Transformer Engine building
  * blocks": group-aware MXFP8 quantization feeding the MXFP8 grouped GEMM).
  *
