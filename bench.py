@@ -20,7 +20,8 @@ per GPU). Rank 0 prints one JSON line:
              kernel of it) captured once as a CUDA graph -- the path is
              graph-capturable, group sizes stay on the device -- and every
              timed replay bracketed by CUDA events on the launching stream, L2
-             flushed (512 MiB write) before every timed step, outside the timed
+             flushed (512 MiB write, then a 512 MiB read that evicts the write's dirty
+             lines) before every timed step, outside the timed
              interval;
   e2e        the same metric through MoELayer.forward_host: pinned host inputs
              copied in and the output copied out inside the timed interval;
@@ -257,7 +258,16 @@ def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
                      expert_bias=None if W.expert_bias(wl) is None else W.expert_bias(wl).to(dev))
     del w1, w3, w2
     dy = W.dy(wl, seed=rank).to(dev) if wl.backward else None        # gradient of the layer output
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush before every timed step, outside the timed interval: a 512 MiB write evicts
+    # everything, then a 512 MiB read of another buffer evicts the write's own dirty lines (their
+    # write-back would otherwise land inside the next timed step), leaving L2 clean and holding
+    # nothing the step uses
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(128 << 20, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
     stream = torch.cuda.current_stream()
 
     route = lambda: layer.stage_route(logits)
@@ -331,7 +341,7 @@ def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
     step_ms = []
     per_stage = [[] for _ in range(ns)]
     for i in range(K):
-        flush.zero_()                                       # L2 flush, outside the timed interval
+        flush_l2()                                          # outside the timed interval
         gev[i][0].record(stream)
         graph.replay()
         gev[i][1].record(stream)
@@ -342,7 +352,7 @@ def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
             step_ms.append(gse.elapsed_ms(0, ns))      # first to last stage, inside the replay
     if not gse.ok:
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             e = ev[i]
             e[0].record(stream)
             for j, (_, fn) in enumerate(stages):
@@ -391,7 +401,7 @@ def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
             dist.barrier()
         torch.cuda.synchronize()
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             e2e_ev[i][0].record(stream)
             e2e_step()
             e2e_ev[i][1].record(stream)
@@ -508,7 +518,7 @@ def workload_config(wl, gpus):
                         + (", forward + backward" if wl.backward else "")
                         + (", sigmoid router" if wl.score == "sigmoid" else ""),
             "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "F": wl.F, "precision": wl.precision,
-            "tokens_per_step_per_gpu": wl.T, "l2": "flushed before every timed step (512 MiB write)",
+            "tokens_per_step_per_gpu": wl.T, "l2": "flushed before every timed step (512 MiB write, then a 512 MiB read of another buffer)",
             "parallelism": f"replicas x{gpus}"}
 
 
@@ -638,6 +648,7 @@ def main():
         extras[name] = {"config": workload_config(xw, world)["workload"],
                         "value": whole_job_tokens_per_s(world, xw.T, args.steps, rx["total_ms"]),
                         "unit": "tokens/s", "ms_per_step": rx["total_ms"] / args.steps,
+                        "ms_first_to_last_stage": rx["inner_ms"],
                         "gpu_launches": rx["launches"], "routes": rx["R"], "roofline": roof_x, "stages": st_x,
                         "clocks": rx["clocks"], "device_errors": rx["errs"]}
     if world > 1:

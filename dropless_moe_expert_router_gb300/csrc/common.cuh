@@ -20,6 +20,15 @@ __device__ __forceinline__ void raise_device_error(unsigned bits) { atomicOr(&g_
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may
+// start while the kernel before it on the stream is still running: pdl_wait() returns once
+// that kernel has completed and its writes are visible (immediately for a kernel launched the
+// ordinary way), so such a kernel calls it before it touches anything another kernel wrote.
+// pdl_trigger() lets the next kernel on the stream start early (it still waits for this one
+// to complete before reading what it writes).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -175,5 +184,24 @@ inline moe_status launch_status() {
 }
 
 inline cudaStream_t as_stream(moe_stream_t s) { return (cudaStream_t)s; }
+
+// Launch with programmatic stream serialization: the kernel may start before the previous
+// kernel on the stream completes, so it must call moe::pdl_wait() before reading anything that
+// kernel (or any earlier one) wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 }  // namespace moe_host

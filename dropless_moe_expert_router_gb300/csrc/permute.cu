@@ -59,6 +59,8 @@ __global__ void perm_rank_kernel(const void* __restrict__ ids, bool i16, int T, 
     const int warp = threadIdx.x >> 5, lane = (int)lane_id();
     const int nwarps = blockDim.x >> 5;
     int* cnt = s_cnt + (size_t)warp * E;
+    pdl_wait();        // the ids (and everything before this kernel) are complete
+    pdl_trigger();     // the scan / scatter may launch now; they wait for this kernel's writes
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
     const int tile = blockIdx.x * nwarps + warp;
     if (tile >= tiles) return;
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(RANK_CTA_WARPS * 32) perm_rank_cta_kernel(cons
                                                                            unsigned* __restrict__ ticket) {
     extern __shared__ __align__(16) uint16_t s_c16[];  // [warps][E]
     const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+    pdl_wait();        // the ids (and everything before this kernel) are complete
+    pdl_trigger();     // the scan / scatter may launch now; they wait for this kernel's writes
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
     const int tile = blockIdx.x;
     // zero the counters (8 E 16-bit values = E 16-byte pieces)
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) perm_scan_kernel(int E, int tile
     __shared__ bool s_last;
     const int warp = threadIdx.x >> 5, lane = (int)lane_id();
     const int nwarps = SCAN_THREADS / 32;
+    pdl_wait();        // the rank kernel's table is complete
+    pdl_trigger();
     // (a) warp per expert: exclusive scan of its per-tile counts, in place
     for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
         int* row = table + (size_t)e * tiles;
@@ -273,6 +279,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
     const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
     int* s_tab = s_dyn;
     int* s_off = s_dyn + (SCAN ? E * tiles : 0);
+    pdl_wait();        // launched early: the rank (and scan) kernels' writes are complete from here
     if constexpr (SCAN) {
         const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
         for (int i = threadIdx.x; i < E * tiles; i += blockDim.x) s_tab[i] = __ldcg(table + i);
@@ -629,8 +636,9 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
                                      (int)smem) != cudaSuccess)
                 return MOE_ERR_CUDA;
         }
-        perm_rank_cta_kernel<<<tiles, RANK_CTA_WARPS * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
-                                                                       row_map, w.ticket);
+        if (moe_host::launch_pdl(perm_rank_cta_kernel, dim3(tiles), dim3(RANK_CTA_WARPS * 32), smem, s, ids, i16, T,
+                                 K, E, TT, tiles, w.table, row_map, w.ticket) != cudaSuccess)
+            return MOE_ERR_CUDA;
     } else {
         const int wpb = rank_warps_per_block(E);
         const size_t smem = (size_t)wpb * E * sizeof(int);
@@ -639,8 +647,9 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
                 cudaSuccess)
                 return MOE_ERR_CUDA;
         }
-        perm_rank_kernel<<<(tiles + wpb - 1) / wpb, wpb * 32, smem, s>>>(ids, i16, T, K, E, TT, tiles, w.table,
-                                                                          row_map, w.ticket);
+        if (moe_host::launch_pdl(perm_rank_kernel, dim3((tiles + wpb - 1) / wpb), dim3(wpb * 32), smem, s, ids, i16,
+                                 T, K, E, TT, tiles, w.table, row_map, w.ticket) != cudaSuccess)
+            return MOE_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     // 2. scan (a separate kernel only when the count table is too large for one block's shared memory)
@@ -650,8 +659,9 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
         const int experts_per_block = SCAN_THREADS / 32;
         int sblocks = (E + experts_per_block - 1) / experts_per_block;
         if (sblocks > cap) sblocks = cap;
-        perm_scan_kernel<<<sblocks, SCAN_THREADS, 0, s>>>(E, tiles, w.table, group_sizes, group_offsets, w.ticket);
-        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe_host::launch_pdl(perm_scan_kernel, dim3(sblocks), dim3(SCAN_THREADS), 0, s, E, tiles, w.table,
+                                 group_sizes, group_offsets, w.ticket) != cudaSuccess)
+            return MOE_ERR_CUDA;
     }
     // 3. scatter: warp per token (with the scan in every block: four blocks per SM, each warp takes
     //    several tokens, so the scan of each block is spread over more rows)
@@ -662,9 +672,13 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
     const int KC = (K + 31) / 32;
     const size_t ssmem = in_block ? ((size_t)E * tiles + E + 1) * sizeof(int) : 0;
 #define MOE_SCATTER(kc, fz, sc)                                                                                  \
-    perm_scatter_kernel<kc, fz, sc><<<(int)blocks, 256, ssmem, s>>>((const uint4*)x, T, H, ids, i16, K, E, TT,   \
-                                                                    tiles, w.table, group_sizes, group_offsets, \
-                                                                    row_map, perm_src, x_perm, x_perm_scales, amax)
+    do {                                                                                                          \
+        if (moe_host::launch_pdl(perm_scatter_kernel<kc, fz, sc>, dim3((unsigned)blocks), dim3(256), ssmem, s,  \
+                                 (const uint4*)x, T, H, ids, i16, K, E, TT, tiles, (const int*)w.table,          \
+                                 group_sizes, group_offsets, row_map, perm_src, x_perm, x_perm_scales, amax) !=   \
+            cudaSuccess)                                                                                          \
+            return MOE_ERR_CUDA;                                                                                  \
+    } while (0)
 #define MOE_SCATTER_KC(fz, sc)        \
     if (KC == 1) MOE_SCATTER(1, fz, sc); \
     else if (KC == 2) MOE_SCATTER(2, fz, sc); \

@@ -60,6 +60,7 @@ template <int G, int V>
 __global__ void __launch_bounds__(256) route_small_kernel(const float* __restrict__ logits, int T, int E,
                                                           int K, void* ids, bool i16,
                                                           float* __restrict__ probs, bool renorm) {
+    pdl_trigger();   // the permute that follows may launch now (it waits for the routes)
     const int lane = (int)lane_id();
     const int gl = lane % G;
     const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -251,6 +252,7 @@ template <int V>
 __global__ void __launch_bounds__(RT, 5) route_radix_kernel(const float* __restrict__ logits, int T, int E,
                                                             int K, void* ids, bool i16, float* __restrict__ probs,
                                                             bool renorm) {
+    pdl_trigger();   // the permute that follows may launch now (it waits for the routes)
     __shared__ RadixSmem sm;
     const int tid = threadIdx.x, lane = (int)lane_id(), warp = tid >> 5;
     // the next row's logits are loaded while the current row is processed
@@ -512,6 +514,7 @@ template <int NV4, int G>
 __global__ void __launch_bounds__(FW * 32, 2) route_filter_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int K, void* ids, bool i16,
                                                                   float* __restrict__ probs, bool renorm) {
+    pdl_trigger();   // the permute that follows may launch now (it waits for the routes)
     extern __shared__ __align__(16) uint8_t fsm[];
     const int lane = (int)lane_id(), w = (int)(threadIdx.x >> 5);
     float* rowbuf = reinterpret_cast<float*>(fsm) + (size_t)w * 128 * NV4;

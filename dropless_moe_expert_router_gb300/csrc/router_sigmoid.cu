@@ -14,15 +14,17 @@
 // registers; each of the K rounds takes the lanes' best keys and an arg-max across the
 // warp (5 shuffle steps), and the winner's lane retires it. Rows are read once, coalesced.
 //
-// Exact selection. The score is rounded to fp32 once from its double value (a single
-// rounding of the logistic function), so the keys -- and with them the ids -- are those of
-// a reference that rounds the exact score once. Double arithmetic is scarce on this part,
-// so it is spent only where the decision needs it: a first pass ranks fp32 keys from expf
-// (a few ulp from the exact ones) and finds the K-th key tau; every expert whose fp32 key
-// is within a margin of tau (2^-14 max(1, |tau|), far above the fp32 keys' error) is a
-// candidate, and no other expert can be among the K largest exact keys (the K first-pass
-// winners' exact keys all beat every non-candidate's). The candidates -- K, or a few more
-// on near-ties -- get their exact scores, and the second pass ranks them.
+// Exact selection. The ids are those of the logistic rounded once to fp32 from its exact
+// value (a reference that rounds the exact score once). Double arithmetic is scarce on this
+// part, so it is spent only where the decision needs it. A first pass ranks fp32 keys from
+// expf (a few ulp from the exact ones) and takes the K largest and the next one: when every
+// gap between these K + 1 keys exceeds a margin (2^-18 max(1, |key|): nearly three times the
+// largest gap two keys a few ulp from exact can show -- expf is within 2 ulp, the add and the
+// division round once each), the exact keys have the same K largest in the same order, and the first pass
+// is the answer (probs from the fp32 scores, within a few ulp). Otherwise every expert whose
+// fp32 key is within the margin of the K-th (tau) is a candidate -- no other can be among the
+// K largest exact keys, as the first pass's K winners' exact keys all beat every other
+// expert's -- the candidates get their exactly rounded scores and a second pass ranks them.
 #include "common.cuh"
 
 #include <math.h>
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
                                                             const float* __restrict__ bias, int T, int E,
                                                             int K, void* __restrict__ ids, bool i16,
                                                             float* __restrict__ probs, bool renorm) {
+    pdl_trigger();   // the permute that follows may launch now (it waits for the routes)
     const int lane = (int)lane_id();
     const int nwarps_total = (gridDim.x * blockDim.x) >> 5;
     // the bias of this lane's experts (the same for every row)
@@ -111,49 +114,19 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
                 avail |= 1u << i;
             }
         }
-        // first pass on the fp32 keys: the K-th key tau
-        float tau = 0.0f;
-        {
-            uint32_t left = avail;
-            for (int k = 0; k < K; k++) {
-                bool ba;
-                float bv;
-                int bi;
-                warp_best<NV>(key, left, lane, ba, bv, bi);
-                tau = bv;
-                if (lane == (bi & 31)) left &= ~(1u << (bi >> 5));
-            }
-        }
-        // candidates: fp32 keys within the margin of tau, given their exactly rounded scores
-        const float margin = fmaxf(1.0f, fabsf(tau)) * (1.0f / 16384.0f);
-        const bool all_cand = !isfinite(tau);
-#pragma unroll
-        for (int i = 0; i < NV; i++) {
-            if (!((avail >> i) & 1u)) continue;
-            if (all_cand || key[i] >= tau - margin) {
-                s[i] = logistic_rn(__ldg(l + i * 32 + lane));
-                key[i] = __fadd_rn(s[i], b[i]);
-            } else {
-                avail &= ~(1u << i);
-            }
-        }
+        // K rounds of selection over the available slots: the winners in order, their scores
+        // (handed over by the winner's lane) and the sum of those scores
         float out_s0 = 0.0f, out_s1 = 0.0f;
         int out_e0 = 0, out_e1 = 0;
         float Z = 0.0f;
-        for (int k = 0; k < K; k++) {       // second pass: the candidates' exact keys
-            bool ba;
-            float bv;
-            int bi;
-            warp_best<NV>(key, avail, lane, ba, bv, bi);
-            // at least K candidates, so a winner always exists; its lane retires it and hands
-            // over its score
+        auto take = [&](int k, int bi, uint32_t& left) {
             const int slot = bi >> 5;
             float mine = 0.0f;
 #pragma unroll
             for (int i = 0; i < NV; i++)
                 if (i == slot) mine = s[i];
             const float sw = __shfl_sync(FULL, mine, bi & 31);
-            if (lane == (bi & 31)) avail &= ~(1u << slot);
+            if (lane == (bi & 31)) left &= ~(1u << slot);
             Z += sw;                                      // same order in every lane
             if (lane == (k & 31)) {
                 if (k < 32) {
@@ -163,6 +136,50 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
                     out_s1 = sw;
                     out_e1 = bi;
                 }
+            }
+        };
+        // first pass on the fp32 keys: the K largest in order, and the next one; when two of
+        // these K + 1 keys are within the margin of each other, the row takes the exact pass
+        float tau = 0.0f, prev = 0.0f;
+        bool near = false;
+        {
+            uint32_t left = avail;
+            const int rounds = K < E ? K + 1 : K;
+            for (int k = 0; k < rounds; k++) {
+                bool ba;
+                float bv;
+                int bi;
+                warp_best<NV>(key, left, lane, ba, bv, bi);   // the same in every lane
+                if (k > 0 && prev - bv <= fmaxf(1.0f, fmaxf(fabsf(prev), fabsf(bv))) * (1.0f / 262144.0f))
+                    near = true;
+                prev = bv;
+                if (k == K) break;
+                tau = bv;
+                take(k, bi, left);
+            }
+        }
+        if (near) {
+            // candidates: fp32 keys within the margin of tau, given their exactly rounded scores
+            const float margin = fmaxf(1.0f, fabsf(tau)) * (1.0f / 262144.0f);
+            const bool all_cand = !isfinite(tau);
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                if (!((avail >> i) & 1u)) continue;
+                if (all_cand || key[i] >= tau - margin) {
+                    s[i] = logistic_rn(__ldg(l + i * 32 + lane));
+                    key[i] = __fadd_rn(s[i], b[i]);
+                } else {
+                    avail &= ~(1u << i);
+                }
+            }
+            Z = 0.0f;
+            for (int k = 0; k < K; k++) {       // second pass: the candidates' exact keys
+                bool ba;
+                float bv;
+                int bi;
+                // at least K candidates, so a winner always exists
+                warp_best<NV>(key, avail, lane, ba, bv, bi);
+                take(k, bi, avail);
             }
         }
         const float inv = renorm ? 1.0f / Z : 1.0f;
