@@ -81,6 +81,10 @@ WORKLOADS = {
     # a quarter of F and half of T: about 1.5 GB on the device)
     "mixtral_prof": Workload("mixtral_prof", T=4096, H=4096, E=8, K=2, F=3584, bias="normal",
                              bias_scale=0.5, renorm=True),
+    # the 2,304-expert routing with narrow rows for profiler captures of the router and the
+    # permute's count and scan kernels (the same ids and tiles; about 0.5 GB on the device)
+    "large_e_prof": Workload("large_e_prof", T=8192, H=256, E=2304, K=36, F=128, id_bits=16,
+                             invalid_frac=0.02),
     # reduced MXFP8 training shape for profiler captures (H, F of the DeepSeek-V3-like
     # slice, 8 experts, about 2 GB on the device)
     "dsv3_prof": Workload("dsv3_prof", T=4096, H=7168, E=8, K=2, F=2048, precision="mxfp8",

@@ -30,13 +30,14 @@ def _w13_row(f, half):
 
 def _oracle_weight_quant(w):
     """Oracle MXFP8 of logical weights [E, Kc, N] along their contraction dim Kc
-    -> (q [E, Kc, N], s [E, Kc/32, N]) in the oracle's view layout."""
-    qs, ss = [], []
-    for e in range(w.shape[0]):
-        q, s = O.quant_rows(np.ascontiguousarray(bf16_bits(w[e]).T))
-        qs.append(q.T)
-        ss.append(s.T)
-    return np.ascontiguousarray(np.stack(qs)), np.ascontiguousarray(np.stack(ss))
+    -> (q [E, Kc, N], s [E, Kc/32, N]) in the oracle's view layout (experts quantised on a
+    thread pool: the C oracle is reentrant and releases the interpreter while it runs)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as pool:
+        parts = list(pool.map(lambda e: O.quant_rows(np.ascontiguousarray(bf16_bits(w[e]).T)), range(w.shape[0])))
+    return (np.ascontiguousarray(np.stack([q.T for q, _ in parts])),
+            np.ascontiguousarray(np.stack([s.T for _, s in parts])))
 
 
 def _sample_rows(off, n_random, seed=0, tile_rows=None):
