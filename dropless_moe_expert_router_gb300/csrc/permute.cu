@@ -162,14 +162,17 @@ __global__ void __launch_bounds__(RANK_CTA_WARPS * 32) perm_rank_cta_kernel(cons
         __syncwarp();
     }
     __syncthreads();
-    // per expert: exclusive prefix over the warps; the total is the tile's count
+    // per expert: exclusive prefix over the warps; the total is the tile's count (the eight
+    // counters are read before any is rewritten: one shared-memory round trip, not eight)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c[RANK_CTA_WARPS];
+#pragma unroll
+        for (int w = 0; w < RANK_CTA_WARPS; w++) c[w] = s_c16[(size_t)w * E + e];
         int run = 0;
 #pragma unroll
         for (int w = 0; w < RANK_CTA_WARPS; w++) {
-            const int c = s_c16[(size_t)w * E + e];
             s_c16[(size_t)w * E + e] = (uint16_t)run;
-            run += c;
+            run += c[w];
         }
         table[(size_t)e * tiles + tile] = run;
     }
@@ -192,21 +195,31 @@ __global__ void __launch_bounds__(SCAN_THREADS) perm_scan_kernel(int E, int tile
     const int nwarps = SCAN_THREADS / 32;
     pdl_wait();        // the rank kernel's table is complete
     pdl_trigger();
-    // (a) warp per expert: exclusive scan of its per-tile counts, in place
+    // (a) warp per expert: exclusive scan of its per-tile counts, in place; SCAN_CHUNKS rows of
+    // 32 counts are loaded before any is scanned (one memory round trip per 32 SCAN_CHUNKS)
+    constexpr int SCAN_CHUNKS = 8;
     for (int e = blockIdx.x * nwarps + warp; e < E; e += gridDim.x * nwarps) {
         int* row = table + (size_t)e * tiles;
         int carry = 0;
-        for (int j0 = 0; j0 < tiles; j0 += 32) {
-            int j = j0 + lane;
-            int v = j < tiles ? row[j] : 0;
-            int inc = v;
+        for (int j0 = 0; j0 < tiles; j0 += 32 * SCAN_CHUNKS) {
+            int v[SCAN_CHUNKS];
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                int o = __shfl_up_sync(FULL, inc, d);
-                if (lane >= d) inc += o;
+            for (int c = 0; c < SCAN_CHUNKS; c++) {
+                const int j = j0 + 32 * c + lane;
+                v[c] = j < tiles ? __ldcg(row + j) : 0;
             }
-            if (j < tiles) row[j] = carry + inc - v;
-            carry += __shfl_sync(FULL, inc, 31);
+#pragma unroll
+            for (int c = 0; c < SCAN_CHUNKS; c++) {
+                const int j = j0 + 32 * c + lane;
+                int inc = v[c];
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int o = __shfl_up_sync(FULL, inc, d);
+                    if (lane >= d) inc += o;
+                }
+                if (j < tiles) row[j] = carry + inc - v[c];
+                carry += __shfl_sync(FULL, inc, 31);
+            }
         }
         if (lane == 0) group_sizes[e] = carry;
     }
