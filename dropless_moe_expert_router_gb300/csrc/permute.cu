@@ -162,8 +162,28 @@ __global__ void __launch_bounds__(RANK_CTA_WARPS * 32) perm_rank_cta_kernel(cons
         __syncwarp();
     }
     __syncthreads();
-    // per expert: exclusive prefix over the warps; the total is the tile's count (the eight
-    // counters are read before any is rewritten: one shared-memory round trip, not eight)
+    // per expert: exclusive prefix over the warps; the total is the tile's count. With E a
+    // multiple of 8 the warps' counter rows are 16-byte aligned and eight experts go at a time,
+    // as packed 16-bit lanes (a tile holds at most 64 * 128 routes, so no lane overflows)
+    if ((E & 7) == 0) {
+        for (int g = threadIdx.x; g < E / 8; g += blockDim.x) {
+            uint4 c[RANK_CTA_WARPS];
+#pragma unroll
+            for (int w = 0; w < RANK_CTA_WARPS; w++) c[w] = reinterpret_cast<const uint4*>(s_c16 + (size_t)w * E)[g];
+            uint4 run = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int w = 0; w < RANK_CTA_WARPS; w++) {
+                reinterpret_cast<uint4*>(s_c16 + (size_t)w * E)[g] = run;
+                run = make_uint4(__vadd2(run.x, c[w].x), __vadd2(run.y, c[w].y), __vadd2(run.z, c[w].z),
+                                 __vadd2(run.w, c[w].w));
+            }
+            const unsigned tot[4] = {run.x, run.y, run.z, run.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                table[(size_t)(8 * g + i) * tiles + tile] = (int)((tot[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+        }
+    } else
+    // one expert at a time (the eight counters read before any is rewritten)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c[RANK_CTA_WARPS];
 #pragma unroll
