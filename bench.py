@@ -23,8 +23,10 @@ per GPU). Rank 0 prints one JSON line:
              flushed (512 MiB write, then a 512 MiB read that evicts the write's dirty
              lines) before every timed step, outside the timed
              interval;
-  e2e        the same metric through MoELayer.forward_host: pinned host inputs
-             copied in and the output copied out inside the timed interval;
+  e2e        the same metric through MoELayer.forward_host with pinned host
+             tensors, inside the timed interval: the logits copied in, x read
+             and y written in host memory by the permute and the combine
+             themselves (a training or NVFP4 layer copies x in and y out);
   roofline   the dominant kernel (grouped GEMM, up projection with SwiGLU):
              algorithmic FLOPs (2 * R * H * 2F) / its mean event-timed duration,
              against the measured dense bf16 burst peak (the timed loop is short

@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_route_ids_bytes": (SZ, [I, I, I]),
     "moe_route_probs_bytes": (SZ, [I, I]),
     "moe_ep_recv_expert_ids": (I, [P, I, I, LL, P, P]),
+    "moe_host_mapped_pointer": (I, [P, C.POINTER(C.c_void_p)]),
 }
 
 

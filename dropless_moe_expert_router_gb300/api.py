@@ -377,6 +377,16 @@ def moe_route_probs_bytes(T: int, K: int) -> int:
     return int(_lib.load().moe_route_probs_bytes(T, K))
 
 
+def moe_host_mapped_pointer(t: torch.Tensor) -> Optional[int]:
+    """Device address of a page-locked host tensor's data (the kernels can read and write it
+    directly), or None when the tensor is not in page-locked memory the device can address."""
+    if t.is_cuda or not t.is_contiguous() or t.numel() == 0:
+        return None
+    out = C.c_void_p()
+    st = _lib.load().moe_host_mapped_pointer(C.c_void_p(t.data_ptr()), C.byref(out))
+    return int(out.value) if st == 0 and out.value else None
+
+
 # ------------------------------------------------------------- expert GEMMs
 def _dt_code(precision: str) -> int:
     if precision == "bf16":

@@ -18,6 +18,19 @@ extern "C" moe_status moe_get_device_errors(uint32_t* flags_out, int clear) {
     return v ? MOE_ERR_DEVICE : MOE_OK;
 }
 
+extern "C" moe_status moe_host_mapped_pointer(const void* host_ptr, void** dev_ptr) {
+    if (!host_ptr || !dev_ptr) return MOE_ERR_INVALID_ARG;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host_ptr) != cudaSuccess) {
+        cudaGetLastError();   // not an error state of the context
+        return MOE_ERR_UNSUPPORTED;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return MOE_ERR_UNSUPPORTED;
+    // the device address of this byte (attr.devicePointer is that of host_ptr itself)
+    *dev_ptr = attr.devicePointer;
+    return MOE_OK;
+}
+
 extern "C" const char* moe_status_string(moe_status status) {
     switch (status) {
         case MOE_OK: return "MOE_OK";

@@ -263,13 +263,44 @@ class MoELayer:
         return self.dx_tokens, self.dlogits, dw1, dw3, dw2
 
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor,
-                     stream=None) -> torch.Tensor:
-        """End to end from host memory: copy x and logits in, run the layer, copy y out
-        (all enqueued on the stream; pinned host tensors make the copies asynchronous)."""
+                     stream=None, zero_copy=None) -> torch.Tensor:
+        """End to end from host memory: x [T, H] bf16 and logits [T, E] fp32 in, y [T, H] bf16 out
+        (all enqueued on the stream). When x_host and y_host are page-locked memory the device can
+        address (torch's pin_memory), the permute reads x and the combine writes y there directly
+        and only the logits are copied in (zero_copy None: when possible; True: required); otherwise
+        x and logits are copied in and y out (pinned tensors make those copies asynchronous), as
+        for the NVFP4 layer and for a training layer, whose backward reads the device copy of x."""
         s = stream if stream is not None else torch.cuda.current_stream()
+        xd = yd = None
+        # (a training layer keeps the device copy of x: its backward reads it)
+        if zero_copy is not False and not self.nv4 and not self.training:
+            for t, shape, dt in ((x_host, (self.T, self.H), torch.bfloat16), (y_host, (self.T, self.H), torch.bfloat16)):
+                if tuple(t.shape) != shape or t.dtype != dt:
+                    raise ValueError(f"host tensor must be {shape} {dt}")
+            xd = api.moe_host_mapped_pointer(x_host)
+            yd = api.moe_host_mapped_pointer(y_host)
+        if xd is None or yd is None:
+            if zero_copy:
+                raise ValueError("x_host and y_host must be page-locked memory the device can address")
+            with torch.cuda.stream(s):
+                self.x_dev.copy_(x_host, non_blocking=True)
+                self.logits_dev.copy_(logits_host, non_blocking=True)
+                self.forward(self.x_dev, self.logits_dev, s)
+                y_host.copy_(self.y, non_blocking=True)
+            return y_host
         with torch.cuda.stream(s):
-            self.x_dev.copy_(x_host, non_blocking=True)
             self.logits_dev.copy_(logits_host, non_blocking=True)
-            self.forward(self.x_dev, self.logits_dev, s)
-            y_host.copy_(self.y, non_blocking=True)
+            self.stage_route(self.logits_dev, s)
+            p = self.perm
+            st = self._lib.moe_permute(
+                xd, self.T, self.H, api._ptr(self.ids), api._id_code(self.ids.dtype), self.K, self.E,
+                api._ptr(p.x_perm), api._ptr(p.x_perm_scales), api._ptr(p.group_sizes), api._ptr(p.group_offsets),
+                api._ptr(p.row_map), api._ptr(p.perm_src), api.MOE_PERMUTE_FUSE_MXFP8 if self.fp8 else 0,
+                api._ptr(self.workspace), self.workspace.numel(), api._stream(s))
+            api._check("moe_permute", st)
+            self.stage_gemm_up(s)
+            self.stage_gemm_down(s)
+            st = self._lib.moe_unpermute_combine(api._ptr(self.y_perm), api._ptr(p.row_map), api._ptr(self.probs),
+                                                 self.T, self.K, self.H, yd, api._stream(s))
+            api._check("moe_unpermute_combine", st)
         return y_host

@@ -517,6 +517,15 @@ moe_status moe_debug_bounded_wait_selftest(uint32_t limit_us, moe_stream_t strea
 /* Human-readable name of a status code (static storage). */
 const char *moe_status_string(moe_status status);
 
+/* Device address of page-locked host memory (cudaHostAlloc / pinned): on systems with a
+ * unified address space the library's kernels can read their inputs from, and write their
+ * outputs to, such memory directly (moe_permute's x, moe_unpermute_combine's y), so a caller
+ * whose tensors live on the host needs no separate copy in or out. Writes *dev_ptr and returns
+ * MOE_OK when host_ptr lies in page-locked memory the current device can address,
+ * MOE_ERR_UNSUPPORTED otherwise (plain pageable memory, no mapping), MOE_ERR_INVALID_ARG for
+ * null pointers. No work is enqueued. (The pages describe no such call.) */
+moe_status moe_host_mapped_pointer(const void *host_ptr, void **dev_ptr);
+
 /* Byte sizes of the compact route ([SPARSER] "Preserve a compact route":
  * [T, K] ids instead of a [T, E] map): ids of the given dtype, and fp32 probs. */
 size_t moe_route_ids_bytes(int T, int K, moe_dtype id_dtype);

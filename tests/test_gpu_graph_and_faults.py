@@ -148,3 +148,32 @@ def test_argument_errors_come_back_as_status_codes():
     lg = torch.zeros((8, 4), device="cuda")
     with pytest.raises(api.MoeError):
         api.moe_route_topk(lg, 5)                                       # K > E
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_forward_host_reads_and_writes_page_locked_memory_directly(precision):
+    """forward_host with pinned host tensors: the permute reads x and the combine writes y in host
+    memory through their device addresses; the result equals the device forward's bit for bit, and
+    the copy path (zero_copy=False) gives the same; pageable memory is refused where required."""
+    from dropless_moe_expert_router_gb300.layer import MoELayer
+    HF = 512 if precision == "mxfp8" else 256
+    wl = W.get("tiny", T=300, H=HF, F=HF, E=8, K=2, precision=precision)
+    w1, w3, w2 = (t.cuda() for t in W.weights(wl))
+    layer = MoELayer(w1, w3, w2, T=wl.T, K=wl.K, precision=precision)
+    x, lg = W.x(wl), W.logits(wl)
+    ref = layer.forward(x.cuda(), lg.cuda()).clone()
+    xh, lh = x.pin_memory(), lg.pin_memory()
+    assert api.moe_host_mapped_pointer(xh) is not None
+    yh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    yh.fill_(7)
+    layer.forward_host(xh, lh, yh, zero_copy=True)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, ref.cpu())
+    yc = torch.empty_like(yh)
+    layer.forward_host(xh, lh, yc, zero_copy=False)
+    torch.cuda.synchronize()
+    assert torch.equal(yc, ref.cpu())
+    assert api.moe_host_mapped_pointer(torch.empty((4, 8), dtype=torch.bfloat16)) is None   # pageable
+    with pytest.raises(ValueError):
+        layer.forward_host(x, lg, torch.empty_like(x), zero_copy=True)
+    assert api.moe_get_device_errors() == 0
