@@ -20,8 +20,17 @@ from . import _lib, api
 class MoELayer:
     def __init__(self, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, *, T: int, K: int,
                  precision: str = "bf16", renorm: bool = False, id_dtype=torch.int32, training: bool = False,
-                 score: str = "softmax", expert_bias: Optional[torch.Tensor] = None, stream=None):
+                 score: str = "softmax", expert_bias: Optional[torch.Tensor] = None, stream=None,
+                 packed_weights=None):
         E, H, F = w1.shape
+        # (packed_weights: the packed forward weights of another layer with the same experts,
+        # shared instead of packed again)
+        self._args = dict(K=K, precision=precision, renorm=renorm, id_dtype=id_dtype, score=score,
+                          expert_bias=expert_bias)
+        self._w = (w1, w3, w2)
+        self._parts = None
+        self._slots = None
+        self.host_event = None      # set by forward_host: y_host holds the result once it completes
         self.E, self.H, self.F, self.T, self.K = E, H, F, T, K
         self.precision = precision
         self.renorm = renorm
@@ -39,7 +48,9 @@ class MoELayer:
             raise ValueError("the NVFP4 layer is forward-only")
         self.training = training
         dev = w1.device
-        if self.nv4:
+        if packed_weights is not None:
+            self.weights = packed_weights
+        elif self.nv4:
             self.weights = api.moe_prepare_weights_nvfp4(w1, w3, w2, stream=stream)
         else:
             self.weights = api.moe_prepare_weights(w1, w3, w2, precision, stream=stream)
@@ -262,45 +273,173 @@ class MoELayer:
         self.stage_route_backward(logits, stream)
         return self.dx_tokens, self.dlogits, dw1, dw3, dw2
 
+    def _pipeline_parts(self):
+        """Layers over consecutive slices of the tokens (an eighth, three quarters, an eighth),
+        sharing the packed weights, and the two copy streams of the sliced transfer."""
+        if self._parts is None:
+            t0 = max(1, self.T // 8)
+            sizes = [t for t in (t0, self.T - 2 * t0, t0) if t > 0] if self.T >= 3 else [self.T]
+            layers = [MoELayer(*self._w, T=t, packed_weights=self.weights, **self._args) for t in sizes]
+            dev = self.weights.w13.device
+            self._parts = (sizes, layers, torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        return self._parts
+
+    def _forward_mapped(self, xd: int, logits_host: torch.Tensor, yd: int, s) -> None:
+        """The forward with x read from, and y written to, host memory at device addresses xd, yd
+        (enqueued on stream s; the logits are copied in)."""
+        with torch.cuda.stream(s):
+            self.logits_dev.copy_(logits_host, non_blocking=True)
+            self.stage_route(self.logits_dev, s)
+            self._permute_mapped(xd, s)
+            self.stage_gemm_up(s)
+            self.stage_gemm_down(s)
+            self._combine_mapped(yd, s)
+
+    def _permute_mapped(self, xd: int, s) -> None:
+        p = self.perm
+        st = self._lib.moe_permute(
+            xd, self.T, self.H, api._ptr(self.ids), api._id_code(self.ids.dtype), self.K, self.E,
+            api._ptr(p.x_perm), api._ptr(p.x_perm_scales), api._ptr(p.group_sizes), api._ptr(p.group_offsets),
+            api._ptr(p.row_map), api._ptr(p.perm_src), api.MOE_PERMUTE_FUSE_MXFP8 if self.fp8 else 0,
+            api._ptr(self.workspace), self.workspace.numel(), api._stream(s))
+        api._check("moe_permute", st)
+
+    def _combine_mapped(self, yd: int, s) -> None:
+        st = self._lib.moe_unpermute_combine(api._ptr(self.y_perm), api._ptr(self.perm.row_map), api._ptr(self.probs),
+                                             self.T, self.K, self.H, yd, api._stream(s))
+        api._check("moe_unpermute_combine", st)
+
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor,
-                     stream=None, zero_copy=None) -> torch.Tensor:
-        """End to end from host memory: x [T, H] bf16 and logits [T, E] fp32 in, y [T, H] bf16 out
-        (all enqueued on the stream). When x_host and y_host are page-locked memory the device can
-        address (torch's pin_memory), the permute reads x and the combine writes y there directly
-        and only the logits are copied in (zero_copy None: when possible; True: required); otherwise
-        x and logits are copied in and y out (pinned tensors make those copies asynchronous), as
-        for the NVFP4 layer and for a training layer, whose backward reads the device copy of x."""
+                     stream=None, transfer: str = "auto") -> torch.Tensor:
+        """End to end from host memory: x [T, H] bf16 and logits [T, E] fp32 in, y [T, H] bf16 out.
+        The compute is enqueued on the stream; y_host holds the result once the event
+        self.host_event has completed (or after torch.cuda.synchronize()). transfer:
+
+        - "overlapped": the layer's own copy streams move x and logits in and y out through two
+          sets of device buffers used in turn, so that consecutive calls overlap. This call's
+          input copy waits only until the previous call's permute has read the other set, so it
+          runs while that call computes; its output copy runs while the next call computes. x_host
+          and logits_host must hold the inputs when the call is made: they are read in the copy
+          stream's order, not the stream's. Wants page-locked host tensors (torch's pin_memory).
+        - "sliced": the tokens go through in three consecutive slices (an eighth, three
+          quarters, an eighth). Each slice has its own route, permute, GEMMs and combine; rows are
+          independent, so the result is the whole batch's. A slice's copies overlap the other
+          slices' compute within one call, at the price of a partly filled GEMM tile per expert
+          and slice. Wants page-locked host tensors.
+        - "direct": the permute reads x and the combine writes y in page-locked host memory
+          through their device addresses; only the logits are copied in.
+        - "copy": x and logits copied in, the whole forward, y copied out, all on the stream.
+        - "auto": "overlapped" when the three host tensors are page-locked, else "copy".
+
+        A training layer always copies: its backward reads the device copy of x. The NVFP4 layer
+        neither slices (x and h are scaled by their whole tensors' amax) nor reads x directly."""
+        if transfer not in ("auto", "overlapped", "sliced", "direct", "copy"):
+            raise ValueError("transfer must be 'auto', 'overlapped', 'sliced', 'direct' or 'copy'")
+        for t, shape, dt in ((x_host, (self.T, self.H), torch.bfloat16), (y_host, (self.T, self.H), torch.bfloat16),
+                             (logits_host, (self.T, self.E), torch.float32)):
+            if tuple(t.shape) != shape or t.dtype != dt:
+                raise ValueError(f"host tensor must be {shape} {dt}")
         s = stream if stream is not None else torch.cuda.current_stream()
-        xd = yd = None
-        # (a training layer keeps the device copy of x: its backward reads it)
-        if zero_copy is not False and not self.nv4 and not self.training:
-            for t, shape, dt in ((x_host, (self.T, self.H), torch.bfloat16), (y_host, (self.T, self.H), torch.bfloat16)):
-                if tuple(t.shape) != shape or t.dtype != dt:
-                    raise ValueError(f"host tensor must be {shape} {dt}")
+        pinned = x_host.is_pinned() and y_host.is_pinned() and logits_host.is_pinned()
+        if transfer == "auto":
+            transfer = "overlapped" if pinned and not self.training else "copy"
+        if transfer != "copy" and self.training:
+            raise ValueError("a training layer copies x in: its backward reads the device copy")
+        if transfer in ("sliced", "direct") and self.nv4:
+            raise ValueError("the NVFP4 layer copies x in whole: it scales x by the whole tensor's amax")
+        if transfer in ("overlapped", "sliced") and not pinned:
+            raise ValueError(f"the {transfer} transfer wants page-locked host tensors")
+        if transfer == "overlapped":
+            self._forward_overlapped(x_host, logits_host, y_host, s)
+            return y_host
+        if transfer == "sliced":
+            self._forward_sliced(x_host, logits_host, y_host, s)
+        elif transfer == "direct":
             xd = api.moe_host_mapped_pointer(x_host)
             yd = api.moe_host_mapped_pointer(y_host)
-        if xd is None or yd is None:
-            if zero_copy:
+            if xd is None or yd is None:
                 raise ValueError("x_host and y_host must be page-locked memory the device can address")
+            self._forward_mapped(xd, logits_host, yd, s)
+        else:
             with torch.cuda.stream(s):
                 self.x_dev.copy_(x_host, non_blocking=True)
                 self.logits_dev.copy_(logits_host, non_blocking=True)
                 self.forward(self.x_dev, self.logits_dev, s)
                 y_host.copy_(self.y, non_blocking=True)
-            return y_host
-        with torch.cuda.stream(s):
-            self.logits_dev.copy_(logits_host, non_blocking=True)
-            self.stage_route(self.logits_dev, s)
-            p = self.perm
-            st = self._lib.moe_permute(
-                xd, self.T, self.H, api._ptr(self.ids), api._id_code(self.ids.dtype), self.K, self.E,
-                api._ptr(p.x_perm), api._ptr(p.x_perm_scales), api._ptr(p.group_sizes), api._ptr(p.group_offsets),
-                api._ptr(p.row_map), api._ptr(p.perm_src), api.MOE_PERMUTE_FUSE_MXFP8 if self.fp8 else 0,
-                api._ptr(self.workspace), self.workspace.numel(), api._stream(s))
-            api._check("moe_permute", st)
-            self.stage_gemm_up(s)
-            self.stage_gemm_down(s)
-            st = self._lib.moe_unpermute_combine(api._ptr(self.y_perm), api._ptr(p.row_map), api._ptr(self.probs),
-                                                 self.T, self.K, self.H, yd, api._stream(s))
-            api._check("moe_unpermute_combine", st)
+        self.host_event = torch.cuda.Event()
+        self.host_event.record(s)
         return y_host
+
+    def _forward_overlapped(self, x_host, logits_host, y_host, s) -> None:
+        if self._slots is None:
+            dev = self.x_dev.device
+            # (buffers of their own: forward's y and the copy transfer's x, logits stay untouched)
+            bufs = [(torch.empty_like(self.x_dev), torch.empty_like(self.logits_dev), torch.empty_like(self.y))
+                    for _ in range(2)]
+            self._slots = dict(bufs=bufs, next=0,
+                               cin=torch.cuda.Stream(device=dev), cout=torch.cuda.Stream(device=dev),
+                               read=[None, None], sent=[None, None])
+        sl = self._slots
+        i = sl["next"]
+        sl["next"] = i ^ 1
+        xs, ls, ys = sl["bufs"][i]
+        cin, cout = sl["cin"], sl["cout"]
+        if sl["read"][i] is not None:
+            cin.wait_event(sl["read"][i])          # this set's previous permute has read it
+        with torch.cuda.stream(cin):
+            xs.copy_(x_host, non_blocking=True)
+            ls.copy_(logits_host, non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(cin)
+        s.wait_event(arrived)
+        if sl["sent"][i] is not None:
+            s.wait_event(sl["sent"][i])            # this set's previous y has reached the host
+        with torch.cuda.stream(s):
+            self.stage_route(ls, s)
+            self.stage_permute(xs, s)
+            read = torch.cuda.Event()
+            read.record(s)
+            self.stage_gemm_up(s)
+            self.stage_quant_h(s)
+            self.stage_gemm_down(s)
+            api.moe_unpermute_combine(self.y_perm, self.perm.row_map, self.probs, y=ys, stream=s)
+            done = torch.cuda.Event()
+            done.record(s)
+        sl["read"][i] = read
+        cout.wait_event(done)
+        with torch.cuda.stream(cout):
+            y_host.copy_(ys, non_blocking=True)
+            sent = torch.cuda.Event()
+            sent.record(cout)
+        sl["sent"][i] = sent
+        self.host_event = sent
+
+    def _forward_sliced(self, x_host, logits_host, y_host, s) -> None:
+        sizes, parts, cin, cout = self._pipeline_parts()
+        start = torch.cuda.Event()
+        start.record(s)
+        cin.wait_event(start)
+        cout.wait_event(start)
+        arrived, off = [], 0
+        with torch.cuda.stream(cin):
+            for t, L in zip(sizes, parts):
+                L.x_dev.copy_(x_host[off:off + t], non_blocking=True)
+                L.logits_dev.copy_(logits_host[off:off + t], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(cin)
+                arrived.append(e)
+                off += t
+        off = 0
+        for t, L, e in zip(sizes, parts, arrived):
+            s.wait_event(e)
+            with torch.cuda.stream(s):
+                L.forward(L.x_dev, L.logits_dev, s)
+            done = torch.cuda.Event()
+            done.record(s)
+            cout.wait_event(done)
+            with torch.cuda.stream(cout):
+                y_host[off:off + t].copy_(L.y, non_blocking=True)
+            off += t
+        out = torch.cuda.Event()
+        out.record(cout)
+        s.wait_event(out)

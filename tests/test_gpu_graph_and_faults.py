@@ -150,30 +150,55 @@ def test_argument_errors_come_back_as_status_codes():
         api.moe_route_topk(lg, 5)                                       # K > E
 
 
-@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
-def test_forward_host_reads_and_writes_page_locked_memory_directly(precision):
-    """forward_host with pinned host tensors: the permute reads x and the combine writes y in host
-    memory through their device addresses; the result equals the device forward's bit for bit, and
-    the copy path (zero_copy=False) gives the same; pageable memory is refused where required."""
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8", "nvfp4"])
+def test_forward_host_transfers_give_the_device_result(precision):
+    """forward_host from page-locked host tensors, every transfer: overlapped (two sets of device
+    buffers in turn, copies on the layer's own streams), sliced (three token slices, each through
+    the whole layer), direct access (the permute reads x and the combine writes y in host memory
+    through their device addresses) and plain copies. Each result equals the device forward's bit
+    for bit once host_event has completed, also for back-to-back overlapped calls on different
+    batches with no synchronisation between them; pageable memory is refused where page-locked
+    memory is required."""
     from dropless_moe_expert_router_gb300.layer import MoELayer
-    HF = 512 if precision == "mxfp8" else 256
-    wl = W.get("tiny", T=300, H=HF, F=HF, E=8, K=2, precision=precision)
+    HF = 512 if precision != "bf16" else 256
+    wl = W.get("tiny", T=301, H=HF, F=HF, E=8, K=2, precision=precision)
     w1, w3, w2 = (t.cuda() for t in W.weights(wl))
     layer = MoELayer(w1, w3, w2, T=wl.T, K=wl.K, precision=precision)
-    x, lg = W.x(wl), W.logits(wl)
-    ref = layer.forward(x.cuda(), lg.cuda()).clone()
+    xs = [W.x(wl, seed=s) for s in range(3)]
+    lgs = [W.logits(wl, seed=s) for s in range(3)]
+    refs = [layer.forward(x.cuda(), lg.cuda()).clone().cpu() for x, lg in zip(xs, lgs)]
+    x, lg, ref = xs[0], lgs[0], refs[0]
     xh, lh = x.pin_memory(), lg.pin_memory()
-    assert api.moe_host_mapped_pointer(xh) is not None
     yh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    yh.fill_(7)
-    layer.forward_host(xh, lh, yh, zero_copy=True)
+    nv4 = precision == "nvfp4"
+    for transfer in ["copy", "auto", "overlapped"] + ([] if nv4 else ["sliced", "sliced", "direct"]):
+        yh.fill_(7)
+        layer.forward_host(xh, lh, yh, transfer=transfer)
+        layer.host_event.synchronize()
+        assert torch.equal(yh, ref), transfer
+    # back-to-back overlapped calls on three batches, twice round, each into its own output
+    xhs = [t.pin_memory() for t in xs]
+    lhs = [t.pin_memory() for t in lgs]
+    yhs = [torch.full((wl.T, wl.H), 7, dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+    for j in range(6):
+        layer.forward_host(xhs[j % 3], lhs[j % 3], yhs[j], transfer="overlapped")
     torch.cuda.synchronize()
-    assert torch.equal(yh, ref.cpu())
-    yc = torch.empty_like(yh)
-    layer.forward_host(xh, lh, yc, zero_copy=False)
+    for j in range(6):
+        assert torch.equal(yhs[j], refs[j % 3]), j
+    if nv4:                      # slices would change the amax scaling of x and h: refused
+        for transfer in ("sliced", "direct"):
+            with pytest.raises(ValueError):
+                layer.forward_host(xh, lh, yh, transfer=transfer)
+    else:
+        sizes = layer._pipeline_parts()[0]
+        assert sum(sizes) == wl.T and len(sizes) == 3
+        assert api.moe_host_mapped_pointer(xh) is not None
+        assert api.moe_host_mapped_pointer(torch.empty((4, 8), dtype=torch.bfloat16)) is None   # pageable
+    for transfer in ("overlapped", "sliced", "direct"):
+        with pytest.raises(ValueError):
+            layer.forward_host(x, lg, torch.empty_like(x), transfer=transfer)
+    yc = torch.empty_like(x)                                    # pageable: "auto" copies
+    layer.forward_host(x, lg, yc)
     torch.cuda.synchronize()
-    assert torch.equal(yc, ref.cpu())
-    assert api.moe_host_mapped_pointer(torch.empty((4, 8), dtype=torch.bfloat16)) is None   # pageable
-    with pytest.raises(ValueError):
-        layer.forward_host(x, lg, torch.empty_like(x), zero_copy=True)
+    assert torch.equal(yc, ref)
     assert api.moe_get_device_errors() == 0
