@@ -8,15 +8,17 @@
 // end-to-end", section "Remove work that has no selected route": local
 // processing visits only the selected slots of a token, found by a warp ballot):
 //
-//   1. rank    (warp per tile of TT tokens; for large E, where tiles are 32
-//              tokens, a CTA per tile whose eight warps rank contiguous eighths
-//              of the tile and are joined by a per-expert prefix): walks the tile's routes in
-//              flattened order, 32 at a time (16 such rows of ids loaded ahead,
-//              one memory latency per 512 routes); __match_any groups the lanes of
-//              one expert, so each valid route gets its rank among the tile's
-//              earlier routes of the same expert. Writes per-(expert, tile)
-//              counts to the workspace table [E][tiles] and the tile-local rank
-//              into row_map.
+//   1. rank    small E (TT = 128 tokens): a warp per tile walks the tile's routes in
+//              flattened order, 32 at a time (16 such rows of ids loaded ahead, one
+//              memory latency per 512 routes); __match_any groups the lanes of one
+//              expert, so each valid route gets its rank among the tile's earlier
+//              routes of the same expert. Large E (TT = 64 tokens): a CTA per tile
+//              sets each route's token bit in its expert's 64-bit token mask and
+//              counts the expert's routes (shared-memory atomics, order-free); a
+//              route's rank is the population of its expert's mask below its token
+//              (a tile where a token lists an expert twice is ranked in flattened
+//              order by one warp instead). Both write per-(expert, tile) counts to
+//              the workspace table [E][tiles] and the tile-local rank into row_map.
 //   2. scan    (warp per expert, then the last block to finish): exclusive scan
 //              of each expert's counts over tiles -> per-tile bases, group_sizes;
 //              the last block scans group_sizes -> group_offsets. When the table
@@ -35,7 +37,7 @@ namespace {
 
 constexpr int SCAN_THREADS = 1024;
 
-inline int tile_tokens(int E) { return E > 64 ? 32 : 128; }
+inline int tile_tokens(int E) { return E > 64 ? 64 : 128; }
 
 struct PermuteWs {
     int* table;        // [E][tiles]
@@ -104,103 +106,98 @@ __global__ void perm_rank_kernel(const void* __restrict__ ids, bool i16, int T, 
     for (int e = lane; e < E; e += 32) table[(size_t)e * tiles + tile] = cnt[e];
 }
 
-// Large E (TT = 32 tokens): one CTA of 8 warps per tile. Warp w ranks the w-th contiguous
-// eighth of the tile's routes against its own 16-bit counters (at most 512 routes each);
-// an exclusive prefix over the warps, per expert, turns the counters into each warp's base
-// (and gives the tile's counts for the table); a route's rank in the tile is its rank in
-// its warp's range plus that base -- the same rank the flattened order gives.
-constexpr int RANK_CTA_WARPS = 8;
-constexpr int RANK_CTA_MAXU = 16;  // rows of 32 routes per warp: TT * K / 8 <= 32 * 128 / 8
+// Large E (TT = 64 tokens): one CTA per tile. Every valid route sets its token's bit in its
+// expert's 64-bit token mask and adds one to its expert's count, by shared-memory atomics whose
+// order does not matter. When no token of the tile lists an expert twice (every count equals its
+// mask's population), a route's rank among the tile's earlier routes of its expert is the number
+// of the expert's tokens before its own: the rank the flattened order gives. A tile where a token
+// lists an expert twice is ranked again by one warp walking its routes in flattened order, as
+// the small-E kernel does.
+constexpr int RANK_MASK_THREADS = 1024;
 
-__global__ void __launch_bounds__(RANK_CTA_WARPS * 32) perm_rank_cta_kernel(const void* __restrict__ ids, bool i16,
-                                                                           int T, int K, int E, int TT, int tiles,
-                                                                           int* __restrict__ table,
-                                                                           int* __restrict__ row_map,
-                                                                           unsigned* __restrict__ ticket) {
-    extern __shared__ __align__(16) uint16_t s_c16[];  // [warps][E]
-    const int warp = threadIdx.x >> 5, lane = (int)lane_id();
+inline size_t rank_mask_smem(int E) { return ((size_t)E * 12 + 15) & ~(size_t)15; }   // masks, counts
+
+template <int MAXR>   // routes per thread: TT * K / RANK_MASK_THREADS rounded up
+__global__ void __launch_bounds__(RANK_MASK_THREADS) perm_rank_mask_kernel(const void* __restrict__ ids, bool i16,
+                                                                          int T, int K, int E, int TT, int tiles,
+                                                                          int* __restrict__ table,
+                                                                          int* __restrict__ row_map,
+                                                                          unsigned* __restrict__ ticket) {
+    extern __shared__ __align__(16) uint8_t s_rm[];
+    unsigned long long* mask = reinterpret_cast<unsigned long long*>(s_rm);   // [E]
+    unsigned* cnt = reinterpret_cast<unsigned*>(s_rm + (size_t)E * 8);        // [E]
     pdl_wait();        // the ids (and everything before this kernel) are complete
     pdl_trigger();     // the scan / scatter may launch now; they wait for this kernel's writes
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
     const int tile = blockIdx.x;
-    // zero the counters (8 E 16-bit values = E 16-byte pieces)
-    for (int i = threadIdx.x; i < E; i += blockDim.x) reinterpret_cast<uint4*>(s_c16)[i] = make_uint4(0, 0, 0, 0);
     const long long i0 = (long long)tile * TT * K;
     long long i1 = i0 + (long long)TT * K;
     const long long nroutes = (long long)T * K;
     if (i1 > nroutes) i1 = nroutes;
-    const long long n = i1 - i0;
-    const long long per = (n + RANK_CTA_WARPS * 32 - 1) / (RANK_CTA_WARPS * 32) * 32;   // routes of one warp
-    const long long w0 = i0 + warp * per;
-    const long long w1 = w0 + per < i1 ? w0 + per : i1;
-    int ev[RANK_CTA_MAXU], rk[RANK_CTA_MAXU];
+    const int n = (int)(i1 - i0);
+    int ev[MAXR];
 #pragma unroll
-    for (int u = 0; u < RANK_CTA_MAXU; u++) {
-        const long long i = w0 + u * 32 + lane;
-        int e = i < w1 ? load_id(ids, i, i16) : -1;
-        if (i < w1 && (e < -1 || e >= E)) {
+    for (int r = 0; r < MAXR; r++) {
+        const int j = r * RANK_MASK_THREADS + (int)threadIdx.x;
+        int e = j < n ? load_id(ids, i0 + j, i16) : -1;
+        if (j < n && (e < -1 || e >= E)) {
             raise_device_error(MOE_DEVERR_BAD_ID);
             e = -1;
         }
-        ev[u] = e;
-        rk[u] = 0;
+        ev[r] = e;
+    }
+    const int n16 = (int)(((size_t)E * 12 + 15) / 16);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(s_rm)[i] = make_uint4(0, 0, 0, 0);
+    // token of route j within the tile, j / K: the high word of j * ceil(2^32 / K) (exact for
+    // j < 2^32 / K; K = 1 is j itself)
+    const unsigned kinv = K > 1 ? 0xffffffffu / (unsigned)K + 1u : 0u;
+    auto token_of = [&](unsigned j) { return K > 1 ? __umulhi(j, kinv) : j; };
+    __syncthreads();   // the masks and counts are zero
+#pragma unroll
+    for (int r = 0; r < MAXR; r++) {
+        if (ev[r] >= 0) {
+            const unsigned j = (unsigned)(r * RANK_MASK_THREADS) + threadIdx.x;
+            atomicOr(&mask[ev[r]], 1ull << token_of(j));
+            atomicAdd(&cnt[ev[r]], 1u);
+        }
     }
     __syncthreads();
-    uint16_t* cnt = s_c16 + (size_t)warp * E;
+    // the tile's counts to the table; a token listing an expert twice leaves a count above the
+    // population of that expert's mask
+    int dup = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const unsigned c = cnt[e];
+        dup |= c != (unsigned)__popcll(mask[e]);
+        table[(size_t)e * tiles + tile] = (int)c;
+    }
+    if (!__syncthreads_or(dup)) {
 #pragma unroll
-    for (int u = 0; u < RANK_CTA_MAXU; u++) {
-        if (w0 + u * 32 >= w1) break;   // warp-uniform
-        const int e = ev[u];
+        for (int r = 0; r < MAXR; r++) {
+            const unsigned j = (unsigned)(r * RANK_MASK_THREADS) + threadIdx.x;
+            if ((int)j < n)
+                row_map[i0 + j] = ev[r] >= 0 ? __popcll(mask[ev[r]] & ((1ull << token_of(j)) - 1ull)) : -1;
+        }
+        return;
+    }
+    // a token lists an expert twice: warp 0 ranks the tile's routes in flattened order
+    if (threadIdx.x >= 32) return;
+    const int lane = (int)threadIdx.x;
+    for (int e = lane; e < E; e += 32) cnt[e] = 0u;
+    __syncwarp();
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int j = c0 + lane;
+        int e = j < n ? load_id(ids, i0 + j, i16) : -1;
+        if (e < -1 || e >= E) e = -1;                  // (flagged above)
         const unsigned grp = __match_any_sync(FULL, e);
         const int leader = __ffs(grp) - 1;
-        int old = 0;
+        unsigned old = 0u;
         if (lane == leader && e >= 0) {
             old = cnt[e];
-            cnt[e] = (uint16_t)(old + __popc(grp));
+            cnt[e] = old + (unsigned)__popc(grp);
         }
-        rk[u] = __shfl_sync(FULL, old, leader) + __popc(grp & lanemask_lt());
+        old = __shfl_sync(FULL, old, leader);
+        if (j < n) row_map[i0 + j] = e >= 0 ? (int)old + __popc(grp & lanemask_lt()) : -1;
         __syncwarp();
-    }
-    __syncthreads();
-    // per expert: exclusive prefix over the warps; the total is the tile's count. With E a
-    // multiple of 8 the warps' counter rows are 16-byte aligned and eight experts go at a time,
-    // as packed 16-bit lanes (a tile holds at most 64 * 128 routes, so no lane overflows)
-    if ((E & 7) == 0) {
-        for (int g = threadIdx.x; g < E / 8; g += blockDim.x) {
-            uint4 c[RANK_CTA_WARPS];
-#pragma unroll
-            for (int w = 0; w < RANK_CTA_WARPS; w++) c[w] = reinterpret_cast<const uint4*>(s_c16 + (size_t)w * E)[g];
-            uint4 run = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int w = 0; w < RANK_CTA_WARPS; w++) {
-                reinterpret_cast<uint4*>(s_c16 + (size_t)w * E)[g] = run;
-                run = make_uint4(__vadd2(run.x, c[w].x), __vadd2(run.y, c[w].y), __vadd2(run.z, c[w].z),
-                                 __vadd2(run.w, c[w].w));
-            }
-            const unsigned tot[4] = {run.x, run.y, run.z, run.w};
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                table[(size_t)(8 * g + i) * tiles + tile] = (int)((tot[i >> 1] >> (16 * (i & 1))) & 0xffffu);
-        }
-    } else
-    // one expert at a time (the eight counters read before any is rewritten)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int c[RANK_CTA_WARPS];
-#pragma unroll
-        for (int w = 0; w < RANK_CTA_WARPS; w++) c[w] = s_c16[(size_t)w * E + e];
-        int run = 0;
-#pragma unroll
-        for (int w = 0; w < RANK_CTA_WARPS; w++) {
-            s_c16[(size_t)w * E + e] = (uint16_t)run;
-            run += c[w];
-        }
-        table[(size_t)e * tiles + tile] = run;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < RANK_CTA_MAXU; u++) {
-        const long long i = w0 + u * 32 + lane;
-        if (i < w1) row_map[i] = ev[u] >= 0 ? rk[u] + cnt[ev[u]] : -1;
     }
 }
 
@@ -629,7 +626,8 @@ static moe_status permute_check_args(const void* x, int T, int H, const void* id
     if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !ids || !x_perm || !row_map || !perm_src)) return MOE_ERR_INVALID_ARG;
     if (fuse && T > 0 && !x_perm_scales) return MOE_ERR_INVALID_ARG;
-    if ((long long)E * 4 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    // (large E: the count kernel keeps a 64-bit token mask and a count per expert in shared memory)
+    if ((long long)E * 4 > 227 * 1024 || (E > 64 && moe::rank_mask_smem(E) > 227 * 1024)) return MOE_ERR_UNSUPPORTED;
     if (!moe_host::aligned(x, 16) || !moe_host::aligned(x_perm, fuse ? 8 : 16) || !moe_host::aligned(row_map, 4) ||
         !moe_host::aligned(perm_src, 4) || !moe_host::aligned(group_sizes, 4) ||
         !moe_host::aligned(group_offsets, 4))
@@ -661,17 +659,26 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
         return MOE_OK;
     }
     // 1. rank
-    if (TT == 32) {
-        // large E: a CTA per tile (TT * K <= 32 * 128 routes, at most 512 per warp)
-        const size_t smem = (size_t)RANK_CTA_WARPS * E * sizeof(uint16_t);
-        if (smem > 48 * 1024) {
-            if (cudaFuncSetAttribute(perm_rank_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess)
-                return MOE_ERR_CUDA;
-        }
-        if (moe_host::launch_pdl(perm_rank_cta_kernel, dim3(tiles), dim3(RANK_CTA_WARPS * 32), smem, s, ids, i16, T,
-                                 K, E, TT, tiles, w.table, row_map, w.ticket) != cudaSuccess)
-            return MOE_ERR_CUDA;
+    if (E > 64) {
+        // large E: a CTA per tile of 64 tokens (at most 64 * 128 routes, 8 per thread)
+        const size_t smem = rank_mask_smem(E);
+        const int per = (int)(((long long)TT * K + RANK_MASK_THREADS - 1) / RANK_MASK_THREADS);
+#define MOE_RANK_MASK(mr)                                                                                         \
+    do {                                                                                                           \
+        if (smem > 48 * 1024 && cudaFuncSetAttribute(perm_rank_mask_kernel<mr>,                                    \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=  \
+                                    cudaSuccess)                                                                   \
+            return MOE_ERR_CUDA;                                                                                   \
+        if (moe_host::launch_pdl(perm_rank_mask_kernel<mr>, dim3(tiles), dim3(RANK_MASK_THREADS), smem, s, ids,   \
+                                 i16, T, K, E, TT, tiles, w.table, row_map, w.ticket) != cudaSuccess)              \
+            return MOE_ERR_CUDA;                                                                                   \
+    } while (0)
+        if (per <= 1) MOE_RANK_MASK(1);
+        else if (per <= 2) MOE_RANK_MASK(2);
+        else if (per <= 3) MOE_RANK_MASK(3);
+        else if (per <= 4) MOE_RANK_MASK(4);
+        else MOE_RANK_MASK(8);
+#undef MOE_RANK_MASK
     } else {
         const int wpb = rank_warps_per_block(E);
         const size_t smem = (size_t)wpb * E * sizeof(int);

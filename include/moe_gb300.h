@@ -174,7 +174,9 @@ moe_status moe_route_sigmoid_topk_backward(const float *logits, const void *ids,
  * consecutive elements, scale byte = clamp(floor(log2(amax)) - 8 + 127, 0, 254)
  * (127 for an all-zero block), payload = E4M3(x / 2^(byte-127)) rounded to
  * nearest even and saturated to +-448.
- * Requires H % 32 == 0, 1 <= K <= E, and a workspace of
+ * Requires H % 32 == 0, 1 <= K <= min(E, 128), E <= 19370 (above 64
+ * experts the count kernel keeps a 64-bit token mask and a count per expert in
+ * shared memory; larger E gets MOE_ERR_UNSUPPORTED), and a workspace of
  * moe_permute_workspace_size(T, K, E) bytes (16-byte aligned; its contents
  * need not be initialised and are overwritten).
  * ------------------------------------------------------------------------ */

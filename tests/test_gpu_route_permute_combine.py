@@ -118,9 +118,13 @@ def test_permute_fused_mxfp8_matches_oracle(name):
 
 
 @pytest.mark.parametrize("case", ["one_token", "all_invalid", "one_expert", "k_equals_e", "e1",
-                                  "bad_ids", "int16_many_experts"])
+                                  "bad_ids", "int16_many_experts", "dup_ids", "dup_ids_many_experts",
+                                  "k128_many_experts", "k1_many_experts", "many_experts_invalid"])
 def test_permute_edge_cases(case):
-    g = torch.Generator().manual_seed(hash(case) % 1000)
+    """Edge shapes of the counting sort, bit for bit against the oracle. Above 64 experts the
+    count kernel ranks from per-expert token masks; a token that lists an expert twice (ids
+    no router here produces, but legal input) sends its tile down the flattened-order path."""
+    g = torch.Generator().manual_seed(sum(map(ord, case)))
     T, H, E, K = 300, 64, 8, 2
     if case == "one_token":
         T = 1
@@ -130,6 +134,14 @@ def test_permute_edge_cases(case):
         E, K = 1, 1
     if case == "int16_many_experts":
         T, E, K = 200, 3000, 36
+    if case == "dup_ids":
+        K = 4
+    if case in ("dup_ids_many_experts", "many_experts_invalid"):
+        T, E, K = 300, 300, 8
+    if case == "k128_many_experts":
+        T, E, K = 130, 256, 128
+    if case == "k1_many_experts":
+        T, E, K = 1000, 100, 1
     lg = torch.randn((T, E), generator=g)
     if case == "one_expert":
         lg[:, 3] += 100.0
@@ -140,6 +152,13 @@ def test_permute_edge_cases(case):
     if case == "bad_ids":
         ids[5, 0] = E + 3
         ids[7, 1] = -9
+    if case in ("dup_ids", "dup_ids_many_experts"):
+        # tokens in the first, a middle and the last tile list an expert two or three times
+        for t in (0, 5, 63, 64, 150, 299):
+            ids[t, K - 1] = ids[t, 0]
+        ids[150, K - 2] = ids[150, 0]
+    if case == "many_experts_invalid":
+        ids[torch.rand((T, K), generator=g).numpy() < 0.3] = -1
     x = (torch.randn((T, H), generator=g) * 0.1).to(torch.bfloat16)
     dt = torch.int16 if case == "int16_many_experts" else torch.int32
     api.moe_get_device_errors(clear=True)

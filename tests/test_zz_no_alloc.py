@@ -61,7 +61,7 @@ def test_noalloc_permute_rejects_problems_beyond_its_scratch():
     anything is enqueued (the small buffers passed are never touched); argument errors are
     reported first, as moe_permute reports them."""
     cap = api.moe_permute_noalloc_max_scratch()
-    T, H, K, E = 1 << 20, 64, 2, 8192                   # needs E * T/32 * 4 bytes of table
+    T, H, K, E = 1 << 20, 64, 2, 8192                   # needs E * T/64 * 4 bytes of table
     assert api.moe_permute_workspace_size(T, K, E) > cap
     from dropless_moe_expert_router_gb300 import _lib
     buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")       # stands for every buffer
