@@ -94,6 +94,18 @@ def test_workspace_size_covers_the_tile_table(lib):
     assert lib.moe_permute_workspace_size(-1, 2, 8) == 0
 
 
+def test_permute_expert_limit_needs_no_gpu(lib):
+    """Above 64 experts the count kernel holds a 64-bit token mask and a count per expert in
+    shared memory (12 bytes each, within 227 KB): E = 19370 passes the argument checks (and then
+    stops at the missing workspace), E = 19371 is unsupported. No pointer is dereferenced."""
+    import ctypes
+    g = ctypes.c_void_p(16)       # stands for the group buffers (never touched on these paths)
+    args = lambda E: (None, 0, 64, None, 1, 2, E, None, None, g, g, None, None, 0, None, 0, None)
+    assert lib.moe_permute(*args(19370)) == 3       # MOE_ERR_WORKSPACE
+    assert lib.moe_permute(*args(19371)) == 2       # MOE_ERR_UNSUPPORTED
+    assert lib.moe_permute(*args(64)) == 3
+
+
 def test_permute_launch_count(lib):
     # the count table is scanned inside the scatter kernel when it is small (<= 2048 entries)
     assert lib.moe_permute_kernel_launches(8192, 2, 8) == 2          # 8 experts x 64 tiles
