@@ -75,14 +75,21 @@ __device__ __forceinline__ float nvfp4_encode_scale(float amax) {
     return s > 3.40282347e38f ? 3.40282347e38f : s;
 }
 
-// E2M1 code of v: round to nearest on the grid 0, .5, 1, 1.5, 2, 3, 4, 6 (ties to the even
-// code), saturating to 6, sign bit kept. The magnitude code counts the grid midpoints below
-// |v|; each midpoint is taken with > or >= so that an exact tie lands on the even code.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-    const float a = fabsf(v);
-    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
-    return c | ((__float_as_uint(v) >> 28) & 8u);
+// E2M1 codes of 8 values, element i in bits 4i..4i+3: each rounded to nearest on the grid
+// 0, .5, 1, 1.5, 2, 3, 4, 6 (ties to the even code), saturating to 6, sign kept -- the
+// conversion instruction's round-to-nearest-even with saturation to the largest finite
+// value. The instruction puts its first source in the high nibble.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+    uint32_t r;
+    asm("{\n .reg .b8 q0, q1, q2, q3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n"
+        " mov.b32 %0, {q0, q1, q2, q3};\n}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
 }
 
 // Value of an E4M3 byte (exact).
@@ -103,10 +110,10 @@ __device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, uint32_t* 
     uint2 out = make_uint2(0u, 0u);
     if (ds > 0.0f) {
         const float rs = __fdiv_rn(S, ds);
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 8; i++) out.x |= e2m1_code(__fmul_rn(f[i], rs)) << (4 * i);
-#pragma unroll
-        for (int i = 0; i < 8; i++) out.y |= e2m1_code(__fmul_rn(f[8 + i], rs)) << (4 * i);
+        for (int i = 0; i < 16; i++) v[i] = __fmul_rn(f[i], rs);
+        out = make_uint2(e2m1x8(v), e2m1x8(v + 8));
     }
     *sbyte = sb;
     return out;
@@ -126,8 +133,10 @@ __device__ __forceinline__ uint32_t nvfp4_pair(const float* f, float S, uint32_t
     uint32_t out = 0u;
     if (ds > 0.0f) {
         const float rs = __fdiv_rn(S, ds);
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; i++) out |= e2m1_code(__fmul_rn(f[i], rs)) << (4 * i);
+        for (int i = 0; i < 8; i++) v[i] = __fmul_rn(f[i], rs);
+        out = e2m1x8(v);
     }
     *sbyte = sb;
     return out;
