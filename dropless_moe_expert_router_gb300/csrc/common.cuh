@@ -98,18 +98,26 @@ __device__ __forceinline__ float e4m3_value(uint32_t byte) {
     return __half2float(__half(h));
 }
 
+// The elements' multiplier of the NVFP4 rule for a block whose E4M3 decode scale is the byte b:
+// S / decode(b), one correctly rounded division; 0 where the decode is not positive (the block
+// is then all zero codes). A kernel fills a table of the 256 bytes once per CTA.
+__device__ __forceinline__ float nvfp4_rs_entry(float S, uint32_t b) {
+    const float ds = e4m3_value(b);
+    return ds > 0.0f ? __fdiv_rn(S, ds) : 0.0f;
+}
+
 // Encode one NVFP4 block of 16 values with tensor encode scale S: returns the 16 packed codes
 // (element i in bits 4i..4i+3) and, in *sbyte, the E4M3 decode scale E4M3((amax / 6) * S).
-__device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, uint32_t* sbyte) {
+// rs_tab: nvfp4_rs_entry(S, b) for every byte b.
+__device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, const float* rs_tab, uint32_t* sbyte) {
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i++) am = fmaxf(am, fabsf(f[i]));
     const float sbf = __fmul_rn(__fdiv_rn(am, 6.0f), S);
     const uint32_t sb = (uint32_t)f32x2_to_e4m3x2(sbf, 0.0f) & 0xffu;
-    const float ds = e4m3_value(sb);
+    const float rs = rs_tab[sb];
     uint2 out = make_uint2(0u, 0u);
-    if (ds > 0.0f) {
-        const float rs = __fdiv_rn(S, ds);
+    if (rs > 0.0f) {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) v[i] = __fmul_rn(f[i], rs);
@@ -122,17 +130,16 @@ __device__ __forceinline__ uint2 nvfp4_block(const float* f, float S, uint32_t* 
 // One NVFP4 block of 16 values held by two adjacent lanes (8 each, the even lane first; both
 // lanes must call): this lane's 8 packed codes, and in *sbyte the block's E4M3 scale. The same
 // arithmetic as nvfp4_block.
-__device__ __forceinline__ uint32_t nvfp4_pair(const float* f, float S, uint32_t* sbyte) {
+__device__ __forceinline__ uint32_t nvfp4_pair(const float* f, float S, const float* rs_tab, uint32_t* sbyte) {
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; i++) am = fmaxf(am, fabsf(f[i]));
     am = fmaxf(am, __shfl_xor_sync(FULL, am, 1));
     const float sbf = __fmul_rn(__fdiv_rn(am, 6.0f), S);
     const uint32_t sb = (uint32_t)f32x2_to_e4m3x2(sbf, 0.0f) & 0xffu;
-    const float ds = e4m3_value(sb);
+    const float rs = rs_tab[sb];
     uint32_t out = 0u;
-    if (ds > 0.0f) {
-        const float rs = __fdiv_rn(S, ds);
+    if (rs > 0.0f) {
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) v[i] = __fmul_rn(f[i], rs);

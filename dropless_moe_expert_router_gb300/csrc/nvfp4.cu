@@ -53,6 +53,9 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint4* __restric
                                                           const float* __restrict__ amax, uint2* __restrict__ q,
                                                           uint8_t* __restrict__ scales) {
     const float S = nvfp4_encode_scale(__ldg(amax));
+    __shared__ float s_rs[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_rs[i] = nvfp4_rs_entry(S, (uint32_t)i);
+    __syncthreads();
     const int bpr = cols / 16;
     const long long nb = valid_rows_of(rows, valid_rows) * (long long)bpr;
     for (long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x; b < nb; b += (long long)gridDim.x * blockDim.x) {
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint4* __restric
         bf16x8_to_f32(__ldg(x + 2 * b), f);
         bf16x8_to_f32(__ldg(x + 2 * b + 1), f + 8);
         uint32_t sb;
-        q[b] = nvfp4_block(f, S, &sb);
+        q[b] = nvfp4_block(f, S, s_rs, &sb);
         scales[b] = (uint8_t)sb;
     }
 }

@@ -365,7 +365,12 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
     const int H8 = H >> 3;     // 16-byte chunks per row
     const int iters = (H8 + 31) >> 5;
     float S = 1.0f;
-    if constexpr (FUSE == 2) S = nvfp4_encode_scale(__ldg(amax));
+    __shared__ float s_rs[FUSE == 2 ? 256 : 1];   // NVFP4: the elements' multiplier per scale byte
+    if constexpr (FUSE == 2) {
+        S = nvfp4_encode_scale(__ldg(amax));
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) s_rs[i] = nvfp4_rs_entry(S, (uint32_t)i);
+        __syncthreads();
+    }
     for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps_total) {
         const int tile = (int)(t / TT);
         int rows[KC];
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
         }
         const uint4* src = x + t * H8;
         // U 16-byte chunks per lane in flight before the stores (memory-level parallelism)
-        constexpr int U = 4;
+        constexpr int U = FUSE == 2 ? 2 : 4;   // (NVFP4: two, for four blocks per SM within 64 registers)
         for (int it0 = 0; it0 < iters; it0 += U) {
             uint4 v[U];
             bool in[U];
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restri
                     if (it0 + u < iters) {  // warp-uniform: the pair shuffles see every lane
                         float f[8];
                         bf16x8_to_f32(v[u], f);
-                        qv[u] = nvfp4_pair(f, S, &sb[u]);
+                        qv[u] = nvfp4_pair(f, S, s_rs, &sb[u]);
                     }
                 }
 #pragma unroll
@@ -703,16 +708,21 @@ static moe_status permute_impl(const void* x, int T, int H, const void* ids, moe
                                  group_sizes, group_offsets, w.ticket) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    // 3. scatter: warp per token (with the scan in every block: four blocks per SM, each warp takes
-    //    several tokens, so the scan of each block is spread over more rows)
+    // 3. scatter: warp per token (with the scan in every block: one wave of blocks, as many as
+    //    the SMs hold at once, each warp taking several tokens, so the scan of each block is
+    //    spread over more rows)
     const long long warps_needed = T;
-    long long blocks = (warps_needed + 7) / 8;
-    const long long bcap = (long long)cap * (in_block ? 4 : 16);
-    if (blocks > bcap) blocks = bcap;
+    const long long blocks_needed = (warps_needed + 7) / 8;
     const int KC = (K + 31) / 32;
     const size_t ssmem = in_block ? ((size_t)E * tiles + E + 1) * sizeof(int) : 0;
 #define MOE_SCATTER(kc, fz, sc)                                                                                  \
     do {                                                                                                          \
+        int per_sm = 4;                                                                                           \
+        if (sc && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, perm_scatter_kernel<kc, fz, sc>, 256,    \
+                                                                ssmem) != cudaSuccess)                            \
+            return MOE_ERR_CUDA;                                                                                  \
+        const long long bcap = (long long)cap * (sc ? (per_sm > 0 ? per_sm : 1) : 16);                            \
+        const long long blocks = blocks_needed < bcap ? blocks_needed : bcap;                                     \
         if (moe_host::launch_pdl(perm_scatter_kernel<kc, fz, sc>, dim3((unsigned)blocks), dim3(256), ssmem, s,  \
                                  (const uint4*)x, T, H, ids, i16, K, E, TT, tiles, (const int*)w.table,          \
                                  group_sizes, group_offsets, row_map, perm_src, x_perm, x_perm_scales, amax) !=   \
