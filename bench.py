@@ -633,6 +633,9 @@ def main():
                     help="other workloads timed beside the headline one ('' for none)")
     ap.add_argument("--cpu-rows", type=int, default=24, help="grouped-MLP rows of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer leg (for profiler launch lists of the device steps alone; "
+                         "the line's e2e is then null)")
     ap.add_argument("--selftest-launch", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -668,7 +671,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
 
-    r = run_ours(args, wl, rank, world, local_rank)
+    r = run_ours(args, wl, rank, world, local_rank, with_e2e=not args.no_e2e)
     peaks, peak_kind = load_peaks()
     stages, roof = roofline(wl, r, peaks, peak_kind)
     extras = {}
@@ -695,18 +698,20 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.precision, "data": "synthetic", "config": config,
-        "e2e": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_ms"]), "unit": "tokens/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "transfer": "overlapped" if r["e2e_overlap"] else r["e2e_serial_transfer"],
-                "serial": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_serial_ms"]),
-                           "transfer": r["e2e_serial_transfer"],
-                           "timing": "each call alone, L2 flushed before it, events around it"}},
+        "e2e": None if args.no_e2e else {
+            "value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_ms"]), "unit": "tokens/s",
+            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+            "transfer": "overlapped" if r["e2e_overlap"] else r["e2e_serial_transfer"],
+            "serial": {"value": whole_job_tokens_per_s(world, wl.T, args.steps, r["e2e_serial_ms"]),
+                       "transfer": r["e2e_serial_transfer"],
+                       "timing": "each call alone, L2 flushed before it, events around it"}},
         "gpu_launches": r["launches"] + sum(v["gpu_launches"] for v in extras.values()),
         "roofline": roof,
         "timing": "step = CUDA-graph replay of the whole step, CUDA events around each replay"
                   + (f" (first to last stage inside the replay: {r['inner_ms']:.4f} ms)" if r["inner_ms"] else "")
                   + f"; stages = {r['stage_source']}; e2e = "
-                  + ("K consecutive MoELayer.forward_host calls (overlapped transfer) as one timed region, "
+                  + ("not run (--no-e2e)" if args.no_e2e else
+                     "K consecutive MoELayer.forward_host calls (overlapped transfer) as one timed region, "
                      "from the first input copy to the last output copy" if r["e2e_overlap"]
                      else "events around each MoELayer.forward_host call")
                   + ("; workloads = the other workloads, timed the same way after the headline one"
