@@ -432,6 +432,9 @@ def run_ours(args, wl, rank, world, local_rank, with_e2e=True):
                 dist.barrier()
             torch.cuda.synchronize()
             flush_l2()
+            # (the first input copy runs on the layer's copy stream, which does not wait for the
+            # start event: with the device idle when the event is recorded, it cannot start early)
+            torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for i in range(K):
