@@ -18,8 +18,9 @@ namespace {
 
 // KC * 32 route slots per token, CHUNKS 16-byte chunks per lane and route, RB routes in flight.
 // UNIT: every weight is 1 (the permute backward: the sum of a token's rows); probs is not read.
+// (four blocks per SM, 64 registers, where that needs no spills: KC * CHUNKS <= 4)
 template <int KC, int CHUNKS, int RB, bool UNIT = false>
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
+__global__ void __launch_bounds__(256, KC * CHUNKS <= 4 ? 4 : 1) combine_kernel(const uint4* __restrict__ y_perm,
                                                       const int* __restrict__ row_map,
                                                       const float* __restrict__ probs, int T, int K, int H,
                                                       uint4* __restrict__ y) {
