@@ -150,7 +150,7 @@ namespace {
 // dy_perm values are also quantised to MXFP8 along the row (1x32 blocks, four
 // lanes per block), the codes and scales of the next GEMM's operand.
 template <int KC, int RB, bool Q>
-__global__ void __launch_bounds__(256) combine_backward_kernel(const uint4* __restrict__ dy,
+__global__ void __launch_bounds__(256, KC == 1 ? 3 : 1) combine_backward_kernel(const uint4* __restrict__ dy,
                                                                const uint4* __restrict__ y_perm,
                                                                const int* __restrict__ row_map,
                                                                const float* __restrict__ probs, int T, int K,
