@@ -510,7 +510,8 @@ __device__ __forceinline__ void write_ranked(const unsigned long long* cand, con
 
 // G: group maxima per lane for the threshold (32 G >= K); element (j, c) of a lane
 // belongs to group (4 j + c) mod G.
-template <int NV4, int G>
+// FULL: E == 128 NV4, so every lane holds all NV4 float4 slots of a row (no absent slots).
+template <int NV4, int G, bool FULL>
 __global__ void __launch_bounds__(FW * 32, 2) route_filter_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int K, void* ids, bool i16,
                                                                   float* __restrict__ probs, bool renorm) {
@@ -545,7 +546,8 @@ __global__ void __launch_bounds__(FW * 32, 2) route_filter_kernel(const float* _
         const float4* rb = reinterpret_cast<const float4*>(rowbuf);
 #pragma unroll
         for (int j = 0; j < NV4; j++) {
-            const float4 f = j < nq ? rb[j * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const float4 f =
+                FULL || j < nq ? rb[j * 32 + lane] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             x[j][0] = f.x;
             x[j][1] = f.y;
             x[j][2] = f.z;
@@ -732,7 +734,7 @@ __global__ void __launch_bounds__(FW * 32, 2) route_filter_kernel(const float* _
     }
 }
 
-template <int NV4, int G>
+template <int NV4, int G, bool FULL>
 cudaError_t launch_filter(const float* logits, int T, int E, int K, void* ids, bool i16, float* probs,
                           bool renorm, cudaStream_t s) {
     constexpr size_t smem = filter_smem_bytes<NV4>();
@@ -741,23 +743,27 @@ cudaError_t launch_filter(const float* logits, int T, int E, int K, void* ids, b
         int dev = 0, sms = 0, per = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaError_t e = cudaFuncSetAttribute(route_filter_kernel<NV4, G>,
+        cudaError_t e = cudaFuncSetAttribute(route_filter_kernel<NV4, G, FULL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_filter_kernel<NV4, G>, FW * 32, smem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_filter_kernel<NV4, G, FULL>, FW * 32, smem);
         resident = sms * (per > 0 ? per : 1);
     }
     const long long need = ((long long)T + FW - 1) / FW;
     const int blocks = (int)(need < resident ? need : resident);
-    route_filter_kernel<NV4, G><<<blocks, FW * 32, smem, s>>>(logits, T, E, K, ids, i16, probs, renorm);
+    route_filter_kernel<NV4, G, FULL><<<blocks, FW * 32, smem, s>>>(logits, T, E, K, ids, i16, probs, renorm);
     return cudaGetLastError();
 }
 
 template <int NV4>
 cudaError_t launch_filter_k(const float* logits, int T, int E, int K, void* ids, bool i16, float* probs,
                             bool renorm, cudaStream_t s) {
-    if (K <= 128 && K > 64) return launch_filter<NV4, 8>(logits, T, E, K, ids, i16, probs, renorm, s);
-    return launch_filter<NV4, 4>(logits, T, E, K, ids, i16, probs, renorm, s);
+    const bool full = E == 128 * NV4;
+    if (K <= 128 && K > 64)
+        return full ? launch_filter<NV4, 8, true>(logits, T, E, K, ids, i16, probs, renorm, s)
+                    : launch_filter<NV4, 8, false>(logits, T, E, K, ids, i16, probs, renorm, s);
+    return full ? launch_filter<NV4, 4, true>(logits, T, E, K, ids, i16, probs, renorm, s)
+                : launch_filter<NV4, 4, false>(logits, T, E, K, ids, i16, probs, renorm, s);
 }
 
 template <int G, int V>
