@@ -28,7 +28,7 @@ class MoELayer:
         self._args = dict(K=K, precision=precision, renorm=renorm, id_dtype=id_dtype, score=score,
                           expert_bias=expert_bias)
         self._w = (w1, w3, w2)
-        self._parts = None
+        self._slice_layers = None
         self._slots = None
         self.host_event = None      # set by forward_host: y_host holds the result once it completes
         self.E, self.H, self.F, self.T, self.K = E, H, F, T, K
@@ -273,16 +273,16 @@ class MoELayer:
         self.stage_route_backward(logits, stream)
         return self.dx_tokens, self.dlogits, dw1, dw3, dw2
 
-    def _pipeline_parts(self):
+    def _slices(self):
         """Layers over consecutive slices of the tokens (an eighth, three quarters, an eighth),
         sharing the packed weights, and the two copy streams of the sliced transfer."""
-        if self._parts is None:
+        if self._slice_layers is None:
             t0 = max(1, self.T // 8)
             sizes = [t for t in (t0, self.T - 2 * t0, t0) if t > 0] if self.T >= 3 else [self.T]
             layers = [MoELayer(*self._w, T=t, packed_weights=self.weights, **self._args) for t in sizes]
             dev = self.weights.w13.device
-            self._parts = (sizes, layers, torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
-        return self._parts
+            self._slice_layers = (sizes, layers, torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        return self._slice_layers
 
     def _forward_mapped(self, xd: int, logits_host: torch.Tensor, yd: int, s) -> None:
         """The forward with x read from, and y written to, host memory at device addresses xd, yd
@@ -415,7 +415,7 @@ class MoELayer:
         self.host_event = sent
 
     def _forward_sliced(self, x_host, logits_host, y_host, s) -> None:
-        sizes, parts, cin, cout = self._pipeline_parts()
+        sizes, parts, cin, cout = self._slices()
         start = torch.cuda.Event()
         start.record(s)
         cin.wait_event(start)

@@ -190,7 +190,7 @@ def test_forward_host_transfers_give_the_device_result(precision):
             with pytest.raises(ValueError):
                 layer.forward_host(xh, lh, yh, transfer=transfer)
     else:
-        sizes = layer._pipeline_parts()[0]
+        sizes = layer._slices()[0]
         assert sum(sizes) == wl.T and len(sizes) == 3
         assert api.moe_host_mapped_pointer(xh) is not None
         assert api.moe_host_mapped_pointer(torch.empty((4, 8), dtype=torch.bfloat16)) is None   # pageable
