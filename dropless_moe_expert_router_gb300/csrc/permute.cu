@@ -294,8 +294,10 @@ inline bool scan_in_block(int E, long long tiles) {
 
 // FUSE: 0 bf16 rows; 1 MXFP8 rows (E4M3 + one E8M0 byte per 32, quads of lanes); 2 NVFP4 rows
 // (packed E2M1 + one E4M3 byte per 16, pairs of lanes) with the encode scale of the device *amax.
+// (MXFP8 with the scan in every block: held to 64 registers, four blocks per SM in its one wave)
 template <int KC, int FUSE, bool SCAN>
-__global__ void __launch_bounds__(256) perm_scatter_kernel(const uint4* __restrict__ x, int T, int H,
+__global__ void __launch_bounds__(256, FUSE == 1 && SCAN ? 4 : 1)
+    perm_scatter_kernel(const uint4* __restrict__ x, int T, int H,
                                                            const void* __restrict__ ids, bool i16, int K, int E,
                                                            int TT, int tiles, const int* __restrict__ table,
                                                            int* __restrict__ group_sizes,
